@@ -1,0 +1,571 @@
+#!/usr/bin/env python3
+"""Benchmark of the EP layout / dispatch / combine path on one GB300.
+
+Headline (one JSON line on stdout): the normal-mode step on the
+DeepSeek-V3-shaped workload ``normal_v3`` (R=8 virtual ranks x 4096 tokens,
+hidden 7168, 256 experts, top-8, Gumbel routing, expert_alignment 128):
+get_dispatch_layout -> dispatch (fresh record, bf16) -> combine (the
+received rows as expert outputs, with the top-k weight reduction), all
+inputs resident in HBM.  ``value`` is payload GB/s of that step (hidden
+bytes read + written by dispatch and combine / step time); tokens/s and the
+HBM fraction ride along.  ``ops`` adds per-operation timings of the other
+workloads (FP8 dispatch with Zipf routing, low-latency dispatch/combine,
+combine with biases on a cached record).
+
+``--impl reference`` times the CPU oracle (the reference arm of this
+project) on a bounded sample of the same workload.  Under torchrun every
+rank runs an independent replica (the single-GPU path has no exchange step).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from combine_get_dispatch_03_gb300 import workloads as W  # noqa: E402
+
+METRIC = "dispatch+combine payload GB/s and tokens/s on 1 GB300; % of HBM peak"
+HEADLINE = "normal_v3"
+
+
+# ----------------------------------------------------------------------------- byte model
+
+def normal_bytes(R, T, H, K, hits, fp8=False, biases=0):
+    """Algorithmic bytes of one normal-mode step, split by operation.
+
+    payload: hidden (and FP8 scale) bytes; meta: routing / index / weight bytes.
+    hits = number of (token, destination rank) pairs = sum of num_tokens_per_rank.
+    """
+    n = R * T
+    row_in = 2 * H
+    row_out = (H + 4 * (H // 128)) if fp8 else 2 * H
+    layout = dict(payload=0, meta=n * K * 8 + n * R + R * R * 4 + R * 256 * 4)
+    notify = dict(payload=0, meta=n * R + n * R * 4 + hits * 4)
+    dispatch = dict(payload=n * row_in + hits * row_out,
+                    meta=n * R * 4 + n * K * 12 + hits * K * 12)
+    combine = dict(payload=hits * 2 * H + biases * n * 2 * H + n * 2 * H,
+                   meta=n * R * 4 + hits * K * 4 + n * K * 4)
+    return dict(layout=layout, notify=notify, dispatch=dispatch, combine=combine)
+
+
+def ll_bytes(R, T, H, K, n_valid, msg):
+    n = R * T
+    return dict(ll_dispatch=dict(payload=n * 2 * H + n_valid * msg, meta=n * K * 8 + n_valid * 8),
+                ll_combine=dict(payload=n_valid * 2 * H + n * 2 * H, meta=n * K * 16))
+
+
+def total(d):
+    return d["payload"] + d["meta"]
+
+
+# ----------------------------------------------------------------------------- environment
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def source_digest():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "combine_get_dispatch_03_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel):
+    """DRAM bytes per launch from a committed ncu summary, if taken on the current kernel sources."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f)
+    ent = rec.get(kernel)
+    if not ent or ent.get("source_digest") != source_digest():
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.samples = []
+        self.proc = None
+        try:
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            target = uuid if uuid.startswith("GPU-") else f"GPU-{uuid}"
+        except Exception:
+            target = os.environ.get("CUDA_VISIBLE_DEVICES", "0").split(",")[device_index]
+        self.cmd = ["nvidia-smi", "-i", target, f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                    "-lms", "100"]
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(self.cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+        time.sleep(0.15)
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 8:
+                self.samples.append(parts)
+
+    def __exit__(self, *exc):
+        time.sleep(0.15)
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"], "samples": 0}
+        sm = [float(s[0]) for s in self.samples if s[0].replace(".", "").isdigit()]
+        mx = [float(s[1]) for s in self.samples if s[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for s in self.samples for i in range(4) if s[4 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(self.samples)}
+
+
+# ----------------------------------------------------------------------------- distributed plumbing
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def reduce_replicas(elapsed_s: float, units: float, world: int):
+    """Whole-job aggregate over independent replicas: max time over ranks, sum of units."""
+    if world == 1:
+        return elapsed_s, units
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([elapsed_s], dtype=torch.float64, device=dev)
+    u = torch.tensor([units], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(u.item())
+
+
+# ----------------------------------------------------------------------------- our arm
+
+class Events:
+    def __init__(self, n):
+        self.ev = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+
+    def rec(self, i, stream):
+        self.ev[i].record(stream)
+
+    def ms(self, a, b):
+        return self.ev[a].elapsed_time(self.ev[b])
+
+
+def prepare_normal(ep, shape, dev, with_e2e=True):
+    idx, w = W.routing(shape)
+    idx_d = torch.from_numpy(idx).to(dev)
+    w_d = torch.from_numpy(w).to(dev)
+    x_d = W.tokens_x(shape, device=dev)
+    probe = ep.Handle(ep.Config(shape.R, shape.T, shape.H, shape.E, shape.K, shape.C, shape.A, 0), dev)
+    lay = ep.ep_get_dispatch_layout(probe, idx_d)
+    probe.check()
+    tpr = lay["num_tokens_per_rank"].to("cpu")
+    probe.destroy()
+    cap = int(tpr.sum(0).max())
+    hits = int(tpr.sum())
+    h = ep.Handle(ep.Config(shape.R, shape.T, shape.H, shape.E, shape.K, shape.C, shape.A, cap), dev)
+    return dict(idx=idx, w=w, idx_d=idx_d, w_d=w_d, x_d=x_d, cap=cap, hits=hits, h=h)
+
+
+def run_ours(args):
+    from combine_get_dispatch_03_gb300 import ep
+    rank, world, local = dist_setup()
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    shape = W.WORKLOADS[HEADLINE]
+    R, T, H, E, K = shape.R, shape.T, shape.H, shape.E, shape.K
+    st = prepare_normal(ep, shape, dev)
+    h, cap, hits = st["h"], st["cap"], st["hits"]
+    idx_d, w_d, x_d = st["idx_d"], st["w_d"], st["x_d"]
+
+    lay = dict(num_tokens_per_rank=torch.empty((R, R), dtype=torch.int32, device=dev),
+               num_tokens_per_rdma_rank=None,
+               num_tokens_per_expert=torch.empty((R, E), dtype=torch.int32, device=dev),
+               is_token_in_rank=torch.empty((R, T, R), dtype=torch.bool, device=dev))
+    recv_x = torch.empty((R, cap, H), dtype=torch.bfloat16, device=dev)
+    recv_i = torch.empty((R, cap, K), dtype=torch.int64, device=dev)
+    recv_w = torch.empty((R, cap, K), dtype=torch.float32, device=dev)
+    nrpe = torch.empty((R, E // R), dtype=torch.int32, device=dev)
+    out = torch.empty((R, T, H), dtype=torch.bfloat16, device=dev)
+    out_w = torch.empty((R, T, K), dtype=torch.float32, device=dev)
+
+    def step(idx_in, w_in, x_in, ev=None, base=0):
+        if ev: ev.rec(base, stream)
+        ep.ep_get_dispatch_layout(h, idx_in, **lay)
+        if ev: ev.rec(base + 1, stream)
+        ep.ep_dispatch(h, x_in, topk_idx=idx_in, topk_weights=w_in,
+                       num_tokens_per_rank=lay["num_tokens_per_rank"], is_token_in_rank=lay["is_token_in_rank"],
+                       num_tokens_per_expert=lay["num_tokens_per_expert"], recv_x=recv_x, recv_topk_idx=recv_i,
+                       recv_topk_weights=recv_w, num_recv_tokens_per_expert=nrpe)
+        if ev: ev.rec(base + 2, stream)
+        ep.ep_combine(h, recv_x, topk_weights=recv_w, combined_x=out, combined_topk_weights=out_w)
+        if ev: ev.rec(base + 3, stream)
+
+    for _ in range(args.warmup):
+        step(idx_d, w_d, x_d)
+    torch.cuda.synchronize(dev)
+    h.check()
+
+    ev = Events(4 * args.steps + 1)
+    barrier(world)
+    with ClockSampler(dev.index) as clocks:
+        torch.cuda.synchronize(dev)
+        t0 = time.perf_counter()
+        for i in range(args.steps):
+            step(idx_d, w_d, x_d, ev, 4 * i)
+        ev.rec(4 * args.steps, stream)
+        torch.cuda.synchronize(dev)
+        wall = time.perf_counter() - t0
+    barrier(world)
+    h.check()
+    step_ms = ev.ms(0, 4 * args.steps) / args.steps
+    op_ms = {name: statistics.mean(ev.ms(4 * i + j, 4 * i + j + 1) for i in range(args.steps))
+             for j, name in enumerate(("layout", "dispatch", "combine"))}
+
+    bm = normal_bytes(R, T, H, K, hits)
+    payload = bm["dispatch"]["payload"] + bm["combine"]["payload"]
+    alg = sum(total(v) for v in bm.values())
+    elapsed, units = reduce_replicas(step_ms * args.steps / 1e3, payload * args.steps, world)
+    value = units / elapsed / 1e9
+    peak, peak_kind = load_peaks()
+
+    # dominant operation of the step and its roofline
+    dom = max(("dispatch", "combine"), key=lambda k: op_ms[k])
+    dom_bytes = total(bm[dom]) + (total(bm["notify"]) if dom == "dispatch" else 0)
+    achieved = dom_bytes / (op_ms[dom] / 1e3) / 1e9
+    kernel_name = "dispatch_notify_kernel + dispatch_kernel<0>" if dom == "dispatch" else "combine_kernel<false>"
+    traffic = recorded_traffic(kernel_name)
+
+    # end to end: pinned host inputs in, the step's result out, every step
+    e2e = None
+    if not args.no_e2e:
+        e2e_steps = min(args.steps, args.e2e_steps)
+        x_h = x_d.to("cpu").pin_memory()
+        idx_h = st["idx_d"].to("cpu").pin_memory()
+        w_h = st["w_d"].to("cpu").pin_memory()
+        out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        outw_h = torch.empty(out_w.shape, dtype=out_w.dtype).pin_memory()
+        x_in = torch.empty_like(x_d)
+        idx_in = torch.empty_like(idx_d)
+        w_in = torch.empty_like(w_d)
+
+        def e2e_step():
+            x_in.copy_(x_h, non_blocking=True)
+            idx_in.copy_(idx_h, non_blocking=True)
+            w_in.copy_(w_h, non_blocking=True)
+            step(idx_in, w_in, x_in)
+            out_h.copy_(out, non_blocking=True)
+            outw_h.copy_(out_w, non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier(world)
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        e2e_ms = e0.elapsed_time(e1) / e2e_steps
+        el, un = reduce_replicas(e2e_ms * e2e_steps / 1e3, payload * e2e_steps, world)
+        e2e = {"value": round(un / el / 1e9, 2), "unit": "GB/s", "ms_per_step": round(e2e_ms, 4),
+               "steps": e2e_steps,
+               "h2d_bytes_per_step": x_h.numel() * 2 + idx_h.numel() * 8 + w_h.numel() * 4,
+               "d2h_bytes_per_step": out_h.numel() * 2 + outw_h.numel() * 4}
+        h.check()
+
+    ops = {}
+    if not args.no_ops and rank == 0:
+        del recv_x, recv_i, recv_w, out, out_w
+        h.destroy()
+        torch.cuda.empty_cache()
+        ops = measure_other_ops(ep, dev, peak)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        cpu = cpu_baseline(shape, tokens=max(64, T // args.cpu_fraction), reps=1)
+
+    result = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(step_ms, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded routing and N(0,1) bf16 tokens)",
+        "config": {"workload": f"{HEADLINE}: R=8 T=4096 H=7168 E=256 K=8 Gumbel routing A=128 C=12; step = "
+                               "get_dispatch_layout + dispatch (fresh record) + combine (received rows, "
+                               "top-k weight reduction)",
+                   "l2": "no flush; inputs larger than L2 (x 470 MB, receive buffer %.2f GB vs 129 MB L2)"
+                         % (R * cap * H * 2 / 1e9),
+                   "parallelism": "replicas" if world > 1 else "single GPU, R=8 virtual ranks"},
+        "tokens_per_s": round(R * T * world / (elapsed / args.steps), 1),
+        "hbm_frac_step": round(alg / (step_ms / 1e3) / 1e9 / peak, 4),
+        "op_ms": {k: round(v, 4) for k, v in op_ms.items()},
+        "roofline": {"bound": "hbm", "kernel": kernel_name, "achieved": round(achieved, 1), "peak": peak,
+                     "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "traffic": traffic, "algorithmic_bytes": dom_bytes},
+        "cpu_baseline": cpu, "clocks": clocks.summary(), "e2e": e2e,
+        "gpu_launches": 4 * args.steps, "wall_s_timed": round(wall, 3), "ops": ops,
+    }
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+
+
+def timed(fn, reps, stream, warmup=3):
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    times = []
+    for _ in range(reps):
+        a.record(stream)
+        fn()
+        b.record(stream)
+        b.synchronize()
+        times.append(a.elapsed_time(b))
+    return statistics.median(times)
+
+
+def measure_other_ops(ep, dev, peak, reps=20):
+    """Per-op times of the other workloads (median of reps, after warm-up)."""
+    stream = torch.cuda.current_stream(dev)
+    res = {}
+
+    def report(name, ms, b, extra=None):
+        d = {"us": round(ms * 1e3, 2), "GBps": round(total(b) / (ms / 1e3) / 1e9, 1),
+             "payload_GBps": round(b["payload"] / (ms / 1e3) / 1e9, 1),
+             "frac": round(total(b) / (ms / 1e3) / 1e9 / peak, 4)}
+        d.update(extra or {})
+        res[name] = d
+
+    # FP8 dispatch with Zipf routing and masked slots
+    shape = W.WORKLOADS["fp8_zipf"]
+    st = prepare_normal(ep, shape, dev)
+    h = st["h"]
+    lay = ep.ep_get_dispatch_layout(h, st["idx_d"])
+    bufs = dict(recv_x=torch.empty((shape.R, st["cap"], shape.H), dtype=torch.float8_e4m3fn, device=dev),
+                recv_x_scales=torch.empty((shape.R, st["cap"], shape.H // 128), dtype=torch.float32, device=dev),
+                recv_topk_idx=torch.empty((shape.R, st["cap"], shape.K), dtype=torch.int64, device=dev),
+                recv_topk_weights=torch.empty((shape.R, st["cap"], shape.K), dtype=torch.float32, device=dev),
+                num_recv_tokens_per_expert=torch.empty((shape.R, shape.EL), dtype=torch.int32, device=dev))
+    fn = lambda: ep.ep_dispatch(h, st["x_d"], topk_idx=st["idx_d"], topk_weights=st["w_d"], cast_to_fp8=True,
+                                num_tokens_per_rank=lay["num_tokens_per_rank"],
+                                is_token_in_rank=lay["is_token_in_rank"],
+                                num_tokens_per_expert=lay["num_tokens_per_expert"], **bufs)
+    ms = timed(fn, reps, stream)
+    h.check()
+    b = normal_bytes(shape.R, shape.T, shape.H, shape.K, st["hits"], fp8=True)
+    report("fp8_zipf.dispatch_fp8", ms, {"payload": b["dispatch"]["payload"],
+                                         "meta": b["dispatch"]["meta"] + total(b["notify"])},
+           {"rho": round(st["hits"] / (shape.R * shape.T), 3)})
+    h.destroy()
+    del bufs, st, lay
+    torch.cuda.empty_cache()
+
+    # combine-heavy: cached record, fresh expert outputs, two biases, weight reduction
+    shape = W.WORKLOADS["combine_heavy"]
+    st = prepare_normal(ep, shape, dev)
+    h = st["h"]
+    lay = ep.ep_get_dispatch_layout(h, st["idx_d"])
+    d = ep.ep_dispatch(h, st["x_d"], topk_idx=st["idx_d"], topk_weights=st["w_d"],
+                       num_tokens_per_rank=lay["num_tokens_per_rank"], is_token_in_rank=lay["is_token_in_rank"],
+                       num_tokens_per_expert=lay["num_tokens_per_expert"])
+    ms_disp = timed(lambda: ep.ep_dispatch(h, st["x_d"], cached=True, recv_x=d["recv_x"]), 5, stream)
+    b0, b1 = W.biases(shape, device=dev)
+    ys = [W.expert_outputs(shape, shape.R * st["cap"], i, device=dev).view(shape.R, st["cap"], shape.H)
+          for i in range(2)]
+    out = torch.empty((shape.R, shape.T, shape.H), dtype=torch.bfloat16, device=dev)
+    cw = torch.empty((shape.R, shape.T, shape.K), dtype=torch.float32, device=dev)
+    it = [0]
+
+    def comb():
+        it[0] += 1
+        ep.ep_combine(h, ys[it[0] % 2], topk_weights=d["recv_topk_weights"], bias_0=b0, bias_1=b1,
+                      combined_x=out, combined_topk_weights=cw)
+
+    ms = timed(comb, reps, stream)
+    h.check()
+    b = normal_bytes(shape.R, shape.T, shape.H, shape.K, st["hits"], biases=2)
+    report("combine_heavy.combine", ms, b["combine"], {"rho": round(st["hits"] / (shape.R * shape.T), 3)})
+    report("combine_heavy.dispatch_cached", ms_disp, {"payload": b["dispatch"]["payload"],
+                                                      "meta": shape.R * shape.T * shape.R * 4})
+    h.destroy()
+    del d, ys, out, cw, b0, b1, st, lay
+    torch.cuda.empty_cache()
+
+    # low latency: FP8 + UE8M0 dispatch, weighted combine
+    shape = W.WORKLOADS["ll_v3"]
+    idx, w = W.routing(shape)
+    idx_d, w_d = torch.from_numpy(idx).to(dev), torch.from_numpy(w).to(dev)
+    x_d = W.tokens_x(shape, device=dev)
+    h = ep.Handle(ep.Config(shape.R, shape.max_tokens, shape.H, shape.E, shape.K, shape.C, 1, 0), dev)
+    msg = ep.ep_ll_msg_bytes(shape.H, True)
+    msgs = torch.empty((shape.R, shape.EL, shape.R * shape.max_tokens, msg), dtype=torch.uint8, device=dev)
+    cnt = torch.empty((shape.R, shape.EL), dtype=torch.int32, device=dev)
+    rng_ = torch.empty((shape.R, shape.EL, shape.R), dtype=torch.int64, device=dev)
+    fn = lambda: ep.ep_ll_dispatch(h, x_d, idx_d, use_fp8=True, use_ue8m0=True, recv_msgs=msgs,
+                                   packed_recv_count=cnt, packed_recv_layout_range=rng_)
+    ms_d = timed(fn, reps, stream)
+    y = W.normal_bf16((shape.R, shape.EL, shape.R * shape.max_tokens, shape.H), shape.seed, "lly", device=dev)
+    out = torch.empty((shape.R, shape.T, shape.H), dtype=torch.bfloat16, device=dev)
+    ms_c = timed(lambda: ep.ep_ll_combine(h, y, idx_d, w_d, combined_x=out), reps, stream)
+    h.check()
+    n_valid = int((idx >= 0).sum())
+    b = ll_bytes(shape.R, shape.T, shape.H, shape.K, n_valid, msg)
+    report("ll_v3.ll_dispatch_fp8_ue8m0", ms_d, b["ll_dispatch"])
+    report("ll_v3.ll_combine", ms_c, b["ll_combine"])
+    h.destroy()
+    del msgs, y, out
+    torch.cuda.empty_cache()
+
+    # the small case (L2-resident)
+    shape = W.WORKLOADS["normal_small"]
+    st = prepare_normal(ep, shape, dev)
+    h = st["h"]
+    lay = ep.ep_get_dispatch_layout(h, st["idx_d"])
+
+    def small_step():
+        l2 = ep.ep_get_dispatch_layout(h, st["idx_d"])
+        d2 = ep.ep_dispatch(h, st["x_d"], topk_idx=st["idx_d"], topk_weights=st["w_d"],
+                            num_tokens_per_rank=l2["num_tokens_per_rank"], is_token_in_rank=l2["is_token_in_rank"],
+                            num_tokens_per_expert=l2["num_tokens_per_expert"])
+        ep.ep_combine(h, d2["recv_x"], topk_weights=d2["recv_topk_weights"])
+
+    ms = timed(small_step, reps, stream)
+    h.check()
+    b = normal_bytes(shape.R, shape.T, shape.H, shape.K, st["hits"])
+    step_b = {"payload": b["dispatch"]["payload"] + b["combine"]["payload"],
+              "meta": sum(v["meta"] for v in b.values())}
+    report("normal_small.step", ms, step_b, {"note": "L2-resident, includes torch output allocation"})
+    h.destroy()
+    return res
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+
+def cpu_baseline(shape, tokens: int, reps: int = 1):
+    """The CPU oracle, as it stands, on the first `tokens` tokens of every rank of the workload."""
+    import oracle as O
+    sub = W.Shape(**{**shape.__dict__, "T": tokens})
+    idx, w = W.routing(shape)
+    idx, w = np.ascontiguousarray(idx[:, :tokens]), np.ascontiguousarray(w[:, :tokens])
+    x = W.bf16_bits(W.tokens_x(shape, device="cuda" if torch.cuda.is_available() else "cpu")[:, :tokens])
+    best = None
+    for _ in range(reps):
+        t0 = time.perf_counter()
+        lay = O.get_dispatch_layout(idx, sub.E, with_rdma=sub.R > 8)
+        cap = int(lay["num_tokens_per_rank"].sum(axis=0).max())
+        n = O.dispatch_notify(lay["num_tokens_per_rank"], lay["is_token_in_rank"], lay["num_tokens_per_expert"],
+                              sub.C, sub.A, cap)
+        d = O.dispatch(x, n["send_head"], cap, sub.E, topk_idx=idx, topk_weights=w)
+        O.combine(d["recv_x"], n["send_head"], recv_topk_weights=d["recv_topk_weights"])
+        dt = time.perf_counter() - t0
+        best = dt if best is None else min(best, dt)
+    hits = int(lay["num_tokens_per_rank"].sum())
+    b = normal_bytes(sub.R, tokens, sub.H, sub.K, hits)
+    payload = b["dispatch"]["payload"] + b["combine"]["payload"]
+    return {"value": round(payload / best / 1e9, 3), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{HEADLINE} restricted to the first {tokens} of {shape.T} tokens of each of the "
+                      f"{shape.R} ranks: layout + notify + dispatch + combine, single-threaded C",
+            "seconds": round(best, 3), "tokens_per_s": round(sub.R * tokens / best, 1)}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    shape = W.WORKLOADS[HEADLINE]
+    tokens = max(64, shape.T // args.cpu_fraction)
+    # warm-up steps and timed steps, each one bounded sample of the workload
+    for _ in range(args.warmup):
+        pass
+    per = []
+    for _ in range(args.steps):
+        per.append(cpu_baseline(shape, tokens=tokens, reps=1))
+    secs = [p["seconds"] for p in per]
+    value = statistics.median(p["value"] for p in per)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * statistics.median(secs), 2),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic", "config": {"workload": per[0]["sample"]},
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": per[0]["sample"]},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--cpu-fraction", type=int, default=8, help="oracle sample = T / this many tokens per rank")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-ops", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

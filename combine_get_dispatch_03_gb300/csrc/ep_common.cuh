@@ -1,0 +1,131 @@
+// ep_common.cuh -- device helpers shared by the EP kernels (sm_103a).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/ep.h"
+
+namespace ep {
+
+constexpr int kWarpSize = 32;
+constexpr unsigned kFullMask = 0xffffffffu;
+constexpr int kMaxRanks = 32;
+constexpr int kMaxTopk = 32;
+constexpr int kMaxExperts = 2048;
+constexpr int kFp8Group = 128;
+
+// First device-detected error wins; the host reads the word through ep_handle_status().
+__device__ __forceinline__ void report(int32_t* status, ep_status code) {
+    atomicCAS(status, 0, static_cast<int32_t>(code));
+}
+
+__device__ __forceinline__ int lane_id() { return threadIdx.x & (kWarpSize - 1); }
+
+__device__ __forceinline__ unsigned lanemask_lt() {
+    unsigned m;
+    asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+    return m;
+}
+
+// 16-byte read of data that no thread writes during the kernel; no L1 allocation.
+__device__ __forceinline__ int4 ld_stream_v4(const int4* p) {
+    int4 v;
+    asm("ld.global.nc.L1::no_allocate.v4.s32 {%0,%1,%2,%3}, [%4];"
+        : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+        : "l"(p));
+    return v;
+}
+
+// 16-byte store that is not kept in L1.
+__device__ __forceinline__ void st_stream_v4(int4* p, const int4& v) {
+    asm volatile("st.global.L1::no_allocate.v4.s32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y),
+                 "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
+__device__ __forceinline__ void st_stream_v2(int2* p, const int2& v) {
+    asm volatile("st.global.L1::no_allocate.v2.s32 [%0], {%1,%2};" ::"l"(p), "r"(v.x), "r"(v.y) : "memory");
+}
+
+// bf16 pair packed in a 32-bit word -> two floats (exact).
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+__device__ __forceinline__ void unpack8(const int4& v, float (&f)[8]) {
+    const uint32_t w[4] = {static_cast<uint32_t>(v.x), static_cast<uint32_t>(v.y), static_cast<uint32_t>(v.z),
+                           static_cast<uint32_t>(v.w)};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        f[2 * i] = bf16_lo(w[i]);
+        f[2 * i + 1] = bf16_hi(w[i]);
+    }
+}
+
+// Eight floats -> eight bf16 (round to nearest even) packed in 16 bytes.
+__device__ __forceinline__ int4 pack8_bf16(const float (&f)[8]) {
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        __nv_bfloat162 p = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);  // .x = low half
+        w[i] = *reinterpret_cast<uint32_t*>(&p);
+    }
+    return make_int4(static_cast<int>(w[0]), static_cast<int>(w[1]), static_cast<int>(w[2]),
+                     static_cast<int>(w[3]));
+}
+
+// Two floats -> two e4m3 codes (round to nearest even, saturate to +-448); `a` in the low byte.
+__device__ __forceinline__ uint16_t e4m3x2(float a, float b) {
+    return static_cast<uint16_t>(__nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3));
+}
+
+// Per-128-channel FP8 scale of one group whose |x| maximum is `amax_raw`.
+//   amax = max(amax_raw, 1e-4); s = amax / 448 (IEEE division)
+//   round_scale == false: scale = s,   multiplier = 448 / amax (IEEE division)
+//   round_scale == true:  e = smallest integer with 2^e >= s, read off the
+//                         bits of s; scale = 2^e, multiplier = 2^-e
+struct Fp8Scale {
+    float scale;
+    float mult;
+    int exponent;
+};
+
+__device__ __forceinline__ Fp8Scale fp8_scale(float amax_raw, bool round_scale) {
+    const float amax = fmaxf(amax_raw, 1e-4f);
+    const float s = __fdiv_rn(amax, 448.0f);
+    Fp8Scale r;
+    if (!round_scale) {
+        r.scale = s;
+        r.mult = __fdiv_rn(448.0f, amax);
+        r.exponent = 0;
+    } else {
+        // s is a positive normal binary32 (s >= 1e-4/448 > 2^-126).
+        const uint32_t u = __float_as_uint(s);
+        const int biased = static_cast<int>(u >> 23);
+        const int e = (u & 0x7fffffu) ? biased - 126 : biased - 127;
+        r.exponent = e;
+        r.scale = __uint_as_float(static_cast<uint32_t>(e + 127) << 23);
+        r.mult = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
+    }
+    return r;
+}
+
+// Eight bf16 (one int4) times `mult`, cast to eight e4m3 codes (8 bytes).
+__device__ __forceinline__ int2 cast8_e4m3(const float (&f)[8], float mult) {
+    uint32_t lo = static_cast<uint32_t>(e4m3x2(__fmul_rn(f[0], mult), __fmul_rn(f[1], mult))) |
+                  (static_cast<uint32_t>(e4m3x2(__fmul_rn(f[2], mult), __fmul_rn(f[3], mult))) << 16);
+    uint32_t hi = static_cast<uint32_t>(e4m3x2(__fmul_rn(f[4], mult), __fmul_rn(f[5], mult))) |
+                  (static_cast<uint32_t>(e4m3x2(__fmul_rn(f[6], mult), __fmul_rn(f[7], mult))) << 16);
+    return make_int2(static_cast<int>(lo), static_cast<int>(hi));
+}
+
+__device__ __forceinline__ float absmax8(const float (&f)[8]) {
+    float m = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(f[i]));
+    return m;
+}
+
+}  // namespace ep

@@ -1,0 +1,315 @@
+// ep_dispatch.cu -- normal-mode dispatch and combine data movement.
+//
+// Dispatch ("第 4 章 V1：布局、dispatch 与 combine" §4.1): each source token
+// row is read from HBM once and written to every destination rank that hosts
+// one of its experts, at the row the notify kernel assigned (send_head).  In
+// FP8 mode the per-128-channel amax, scale and e4m3 cast happen in registers
+// between the read and the writes ("DeepEP Normal vs Low-Latency
+// 双模式深度分析", low-latency dispatch excerpt: per-group amax, scale,
+// inverse scale, cast).
+//
+// Combine (same chapter §4.2 and §4.4): each output token gathers the rows
+// that its destination ranks hold, adds them in fp32 in ascending rank order
+// after the two optional biases, and writes bf16 (or fp32) once; the top-k
+// weights are summed separately over the same ranks.
+//
+// Both are HBM-bound permutations (about 0 flops per byte): a persistent
+// grid of (SM count x resident CTAs), one warp per token, 16-byte vector
+// accesses with several in flight per lane.
+#include "ep_common.cuh"
+#include "ep_kernels.h"
+
+namespace ep {
+
+namespace {
+
+constexpr int kDispatchUnroll = 4;  // 16-byte vectors in flight per lane (payload read)
+constexpr int kCombineUnroll = 2;   // 16-byte columns per lane per pass
+constexpr int kCombineFanIn = 4;    // source rows loaded together before accumulation
+
+// Row of rank `lane` for token g, or -1 (not sent / past capacity).
+__device__ __forceinline__ int32_t dest_row(const int32_t* send_head, int64_t g, int R, int64_t cap, int lane) {
+    int32_t row = -1;
+    if (lane < R) {
+        row = __ldg(send_head + g * R + lane);
+        if (row >= cap) row = -1;
+    }
+    return row;
+}
+
+template <int kMode>
+__global__ void __launch_bounds__(kDispatchThreads)
+    dispatch_kernel(int R, int T, int H, int K, int EL, int64_t cap, const void* __restrict__ x,
+                    const float* __restrict__ x_scales, const int64_t* __restrict__ topk_idx,
+                    const float* __restrict__ topk_weights, const int32_t* __restrict__ send_head,
+                    void* __restrict__ recv_x, float* __restrict__ recv_x_scales,
+                    int64_t* __restrict__ recv_topk_idx, float* __restrict__ recv_topk_weights) {
+    constexpr int kWarps = kDispatchThreads / kWarpSize;
+    const int lane = lane_id();
+    const int64_t n_tokens = static_cast<int64_t>(R) * T;
+    const int G = H / kFp8Group;
+
+    for (int64_t g = static_cast<int64_t>(blockIdx.x) * kWarps + threadIdx.x / kWarpSize; g < n_tokens;
+         g += static_cast<int64_t>(gridDim.x) * kWarps) {
+        const int32_t row = dest_row(send_head, g, R, cap, lane);
+        const unsigned dst = __ballot_sync(kFullMask, row >= 0);
+        if (dst == 0u) continue;
+
+        // Top-k metadata of each destination.
+        if (recv_topk_idx != nullptr || recv_topk_weights != nullptr) {
+            int64_t e = -1;
+            float w = 0.0f;
+            if (lane < K) {
+                e = __ldg(topk_idx + g * K + lane);
+                if (topk_weights != nullptr) w = __ldg(topk_weights + g * K + lane);
+            }
+            for (unsigned m = dst; m; m &= m - 1) {
+                const int r = __ffs(m) - 1;
+                const int64_t rr = __shfl_sync(kFullMask, row, r);
+                if (lane < K) {
+                    const bool mine = e >= 0 && static_cast<int>(e) / EL == r;
+                    const int64_t o = (static_cast<int64_t>(r) * cap + rr) * K + lane;
+                    if (recv_topk_idx != nullptr) recv_topk_idx[o] = mine ? e % EL : -1;
+                    if (recv_topk_weights != nullptr) recv_topk_weights[o] = mine ? w : 0.0f;
+                }
+            }
+        }
+
+        if constexpr (kMode == kModeBf16 || kMode == kModeFp8In) {
+            // Byte copy of the row (bf16: 2H bytes; FP8 input: H bytes) plus FP8 scales.
+            const int n16 = kMode == kModeBf16 ? H / 8 : H / 16;
+            const int4* src = reinterpret_cast<const int4*>(x) + g * n16;
+            int4* base = reinterpret_cast<int4*>(recv_x);
+            for (int i0 = 0; i0 < n16; i0 += kWarpSize * kDispatchUnroll) {
+                int4 v[kDispatchUnroll];
+#pragma unroll
+                for (int u = 0; u < kDispatchUnroll; ++u) {
+                    const int i = i0 + u * kWarpSize + lane;
+                    if (i < n16) v[u] = ld_stream_v4(src + i);
+                }
+                for (unsigned m = dst; m; m &= m - 1) {
+                    const int r = __ffs(m) - 1;
+                    const int64_t rr = __shfl_sync(kFullMask, row, r);
+                    int4* d = base + (static_cast<int64_t>(r) * cap + rr) * n16;
+#pragma unroll
+                    for (int u = 0; u < kDispatchUnroll; ++u) {
+                        const int i = i0 + u * kWarpSize + lane;
+                        if (i < n16) st_stream_v4(d + i, v[u]);
+                    }
+                }
+            }
+            if constexpr (kMode == kModeFp8In) {
+                const float* ssrc = x_scales + g * G;
+                for (unsigned m = dst; m; m &= m - 1) {
+                    const int r = __ffs(m) - 1;
+                    const int64_t rr = __shfl_sync(kFullMask, row, r);
+                    float* d = recv_x_scales + (static_cast<int64_t>(r) * cap + rr) * G;
+                    for (int i = lane; i < G; i += kWarpSize) d[i] = __ldg(ssrc + i);
+                }
+            }
+        } else {
+            // bf16 -> e4m3 with one fp32 scale per 128 channels.  Lane l of a
+            // warp pass covers 8 channels; lanes 0-15 and 16-31 each hold one group.
+            const int n16 = H / 8;
+            const int4* src = reinterpret_cast<const int4*>(x) + g * n16;
+            int2* base = reinterpret_cast<int2*>(recv_x);
+            for (int i0 = 0; i0 < n16; i0 += kWarpSize * kDispatchUnroll) {
+                int4 v[kDispatchUnroll];
+#pragma unroll
+                for (int u = 0; u < kDispatchUnroll; ++u) {
+                    const int i = i0 + u * kWarpSize + lane;
+                    v[u] = i < n16 ? ld_stream_v4(src + i) : make_int4(0, 0, 0, 0);
+                }
+                int2 q[kDispatchUnroll];
+                float sc[kDispatchUnroll];
+#pragma unroll
+                for (int u = 0; u < kDispatchUnroll; ++u) {
+                    float f[8];
+                    unpack8(v[u], f);
+                    float amax = absmax8(f);
+#pragma unroll
+                    for (int off = 8; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, off));
+                    const Fp8Scale fs = fp8_scale(amax, false);
+                    q[u] = cast8_e4m3(f, fs.mult);
+                    sc[u] = fs.scale;
+                }
+                for (unsigned m = dst; m; m &= m - 1) {
+                    const int r = __ffs(m) - 1;
+                    const int64_t rr = __shfl_sync(kFullMask, row, r);
+                    const int64_t drow = static_cast<int64_t>(r) * cap + rr;
+                    int2* d = base + drow * n16;
+#pragma unroll
+                    for (int u = 0; u < kDispatchUnroll; ++u) {
+                        const int i = i0 + u * kWarpSize + lane;
+                        if (i < n16) {
+                            st_stream_v2(d + i, q[u]);
+                            if ((lane & 15) == 0) recv_x_scales[drow * G + i / 16] = sc[u];
+                        }
+                    }
+                }
+            }
+        }
+    }
+}
+
+template <bool kOutF32>
+__global__ void __launch_bounds__(kCombineThreads)
+    combine_kernel(int R, int T, int H, int K, int64_t cap, const int32_t* __restrict__ send_head,
+                   const int4* __restrict__ y, const float* __restrict__ recv_w, const int4* __restrict__ bias0,
+                   const int4* __restrict__ bias1, void* __restrict__ out, float* __restrict__ cw) {
+    constexpr int kWarps = kCombineThreads / kWarpSize;
+    const int lane = lane_id();
+    const int64_t n_tokens = static_cast<int64_t>(R) * T;
+    const int n16 = H / 8;
+
+    for (int64_t g = static_cast<int64_t>(blockIdx.x) * kWarps + threadIdx.x / kWarpSize; g < n_tokens;
+         g += static_cast<int64_t>(gridDim.x) * kWarps) {
+        const int32_t row = dest_row(send_head, g, R, cap, lane);
+        const unsigned src_ranks = __ballot_sync(kFullMask, row >= 0);
+
+        if (cw != nullptr && recv_w != nullptr) {
+            float acc = 0.0f;
+            for (unsigned m = src_ranks; m; m &= m - 1) {
+                const int r = __ffs(m) - 1;
+                const int64_t rr = __shfl_sync(kFullMask, row, r);
+                if (lane < K) acc = acc + __ldg(recv_w + (static_cast<int64_t>(r) * cap + rr) * K + lane);
+            }
+            if (lane < K) cw[g * K + lane] = acc;
+        }
+
+        for (int i0 = 0; i0 < n16; i0 += kWarpSize * kCombineUnroll) {
+            float acc[kCombineUnroll][8];
+#pragma unroll
+            for (int u = 0; u < kCombineUnroll; ++u) {
+                const int i = i0 + u * kWarpSize + lane;
+                float f0[8], f1[8];
+#pragma unroll
+                for (int q = 0; q < 8; ++q) f0[q] = f1[q] = 0.0f;
+                if (i < n16) {
+                    if (bias0 != nullptr) unpack8(ld_stream_v4(bias0 + g * n16 + i), f0);
+                    if (bias1 != nullptr) unpack8(ld_stream_v4(bias1 + g * n16 + i), f1);
+                }
+#pragma unroll
+                for (int q = 0; q < 8; ++q) acc[u][q] = __fadd_rn(f0[q], f1[q]);
+            }
+            unsigned m = src_ranks;
+            while (m) {
+                int rk[kCombineFanIn];
+                int64_t rr[kCombineFanIn];
+#pragma unroll
+                for (int j = 0; j < kCombineFanIn; ++j) {
+                    rk[j] = m ? __ffs(m) - 1 : -1;
+                    if (m) m &= m - 1;
+                    rr[j] = __shfl_sync(kFullMask, row, rk[j] < 0 ? 0 : rk[j]);
+                }
+                int4 v[kCombineFanIn][kCombineUnroll];
+#pragma unroll
+                for (int j = 0; j < kCombineFanIn; ++j)
+#pragma unroll
+                    for (int u = 0; u < kCombineUnroll; ++u) {
+                        const int i = i0 + u * kWarpSize + lane;
+                        if (rk[j] >= 0 && i < n16)
+                            v[j][u] = ld_stream_v4(y + (static_cast<int64_t>(rk[j]) * cap + rr[j]) * n16 + i);
+                    }
+#pragma unroll
+                for (int j = 0; j < kCombineFanIn; ++j) {
+                    if (rk[j] < 0) continue;
+#pragma unroll
+                    for (int u = 0; u < kCombineUnroll; ++u) {
+                        float f[8];
+                        unpack8(v[j][u], f);
+#pragma unroll
+                        for (int q = 0; q < 8; ++q) acc[u][q] = __fadd_rn(acc[u][q], f[q]);
+                    }
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < kCombineUnroll; ++u) {
+                const int i = i0 + u * kWarpSize + lane;
+                if (i >= n16) continue;
+                if constexpr (kOutF32) {
+                    float4* o = reinterpret_cast<float4*>(out) + (g * n16 + i) * 2;
+                    o[0] = make_float4(acc[u][0], acc[u][1], acc[u][2], acc[u][3]);
+                    o[1] = make_float4(acc[u][4], acc[u][5], acc[u][6], acc[u][7]);
+                } else {
+                    reinterpret_cast<int4*>(out)[g * n16 + i] = pack8_bf16(acc[u]);
+                }
+            }
+        }
+    }
+}
+
+template <typename Kernel>
+int resident_blocks(Kernel k, int threads, int num_sms) {
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, threads, 0) != cudaSuccess || per_sm < 1)
+        per_sm = 1;
+    return per_sm * num_sms;
+}
+
+int clamp_grid(int planned, int64_t warps_needed, int warps_per_block) {
+    const int64_t need = (warps_needed + warps_per_block - 1) / warps_per_block;
+    return static_cast<int>(need < planned ? (need > 0 ? need : 1) : planned);
+}
+
+}  // namespace
+
+cudaError_t plan_dispatch_combine(LaunchPlan* plan) {
+    const int n = plan->num_sms;
+    plan->dispatch_blocks[kModeBf16] = resident_blocks(dispatch_kernel<kModeBf16>, kDispatchThreads, n);
+    plan->dispatch_blocks[kModeCastFp8] = resident_blocks(dispatch_kernel<kModeCastFp8>, kDispatchThreads, n);
+    plan->dispatch_blocks[kModeFp8In] = resident_blocks(dispatch_kernel<kModeFp8In>, kDispatchThreads, n);
+    plan->combine_blocks[0] = resident_blocks(combine_kernel<false>, kCombineThreads, n);
+    plan->combine_blocks[1] = resident_blocks(combine_kernel<true>, kCombineThreads, n);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_dispatch(const LaunchPlan& plan, int mode, int R, int T, int H, int K, int EL, int64_t cap,
+                            const void* x, const float* x_scales, const int64_t* topk_idx,
+                            const float* topk_weights, const int32_t* send_head, void* recv_x,
+                            float* recv_x_scales, int64_t* recv_topk_idx, float* recv_topk_weights,
+                            cudaStream_t stream) {
+    const int64_t n_tokens = static_cast<int64_t>(R) * T;
+    if (n_tokens == 0) return cudaSuccess;
+    const int grid = clamp_grid(plan.dispatch_blocks[mode], n_tokens, kDispatchThreads / kWarpSize);
+    switch (mode) {
+        case kModeBf16:
+            dispatch_kernel<kModeBf16><<<grid, kDispatchThreads, 0, stream>>>(
+                R, T, H, K, EL, cap, x, x_scales, topk_idx, topk_weights, send_head, recv_x, recv_x_scales,
+                recv_topk_idx, recv_topk_weights);
+            break;
+        case kModeCastFp8:
+            dispatch_kernel<kModeCastFp8><<<grid, kDispatchThreads, 0, stream>>>(
+                R, T, H, K, EL, cap, x, x_scales, topk_idx, topk_weights, send_head, recv_x, recv_x_scales,
+                recv_topk_idx, recv_topk_weights);
+            break;
+        default:
+            dispatch_kernel<kModeFp8In><<<grid, kDispatchThreads, 0, stream>>>(
+                R, T, H, K, EL, cap, x, x_scales, topk_idx, topk_weights, send_head, recv_x, recv_x_scales,
+                recv_topk_idx, recv_topk_weights);
+            break;
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const LaunchPlan& plan, bool out_fp32, int R, int T, int H, int K, int64_t cap,
+                           const int32_t* send_head, const void* y, const float* recv_topk_weights,
+                           const void* bias0, const void* bias1, void* out, float* combined_topk_weights,
+                           cudaStream_t stream) {
+    const int64_t n_tokens = static_cast<int64_t>(R) * T;
+    if (n_tokens == 0) return cudaSuccess;
+    const int grid = clamp_grid(plan.combine_blocks[out_fp32 ? 1 : 0], n_tokens, kCombineThreads / kWarpSize);
+    const int4* yv = static_cast<const int4*>(y);
+    const int4* b0 = static_cast<const int4*>(bias0);
+    const int4* b1 = static_cast<const int4*>(bias1);
+    if (out_fp32)
+        combine_kernel<true><<<grid, kCombineThreads, 0, stream>>>(R, T, H, K, cap, send_head, yv, recv_topk_weights,
+                                                                  b0, b1, out, combined_topk_weights);
+    else
+        combine_kernel<false><<<grid, kCombineThreads, 0, stream>>>(R, T, H, K, cap, send_head, yv,
+                                                                   recv_topk_weights, b0, b1, out,
+                                                                   combined_topk_weights);
+    return cudaGetLastError();
+}
+
+}  // namespace ep

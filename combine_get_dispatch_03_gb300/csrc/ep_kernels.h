@@ -1,0 +1,63 @@
+// ep_kernels.h -- host-side launchers of the EP kernels (internal to the library).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/ep.h"
+
+namespace ep {
+
+// Launch shapes, chosen once per device when a handle is created.
+struct LaunchPlan {
+    int num_sms = 0;
+    int dispatch_blocks[3] = {0, 0, 0};  // per payload mode
+    int combine_blocks[2] = {0, 0};      // bf16 out, fp32 out
+    int ll_dispatch_blocks[2] = {0, 0};  // bf16, fp8
+    int ll_combine_blocks = 0;
+};
+
+constexpr int kLayoutThreads = 1024;
+constexpr int kNotifyThreads = 1024;
+constexpr int kDispatchThreads = 512;
+constexpr int kCombineThreads = 512;
+constexpr int kLLCountThreads = 512;
+constexpr int kLLDispatchThreads = 512;
+constexpr int kLLCombineThreads = 512;
+
+enum DispatchMode { kModeBf16 = 0, kModeCastFp8 = 1, kModeFp8In = 2 };
+
+cudaError_t plan_launches(LaunchPlan* plan, int device, int num_experts);
+
+cudaError_t launch_get_dispatch_layout(const int64_t* topk_idx, int R, int T, int K, int E,
+                                       int32_t* tpr, int32_t* tprdma, int32_t* tpe, uint8_t* itr,
+                                       int32_t* status, cudaStream_t stream);
+
+cudaError_t launch_dispatch_notify(int R, int T, int E, int C, int A, int64_t cap, const int32_t* tpr,
+                                   const uint8_t* itr, const int32_t* tpe, int32_t* rank_prefix,
+                                   int32_t* channel_prefix, int32_t* recv_channel_prefix, int32_t* num_recv,
+                                   int32_t* send_head, int32_t* recv_src_idx, int32_t* num_recv_per_expert,
+                                   int32_t* status, cudaStream_t stream);
+
+cudaError_t launch_dispatch(const LaunchPlan& plan, int mode, int R, int T, int H, int K, int EL, int64_t cap,
+                            const void* x, const float* x_scales, const int64_t* topk_idx,
+                            const float* topk_weights, const int32_t* send_head, void* recv_x,
+                            float* recv_x_scales, int64_t* recv_topk_idx, float* recv_topk_weights,
+                            cudaStream_t stream);
+
+cudaError_t launch_combine(const LaunchPlan& plan, bool out_fp32, int R, int T, int H, int K, int64_t cap,
+                           const int32_t* send_head, const void* y, const float* recv_topk_weights,
+                           const void* bias0, const void* bias1, void* out, float* combined_topk_weights,
+                           cudaStream_t stream);
+
+cudaError_t launch_ll_dispatch(const LaunchPlan& plan, int R, int T, int maxT, int H, int K, int E,
+                               const void* x, const int64_t* topk_idx, bool use_fp8, bool round_scale,
+                               bool use_ue8m0, int32_t* slot, int32_t* cnt, void* recv_msgs,
+                               int32_t* packed_recv_count, int64_t* layout_range, int32_t* stats,
+                               int32_t* status, cudaStream_t stream);
+
+cudaError_t launch_ll_combine(const LaunchPlan& plan, int R, int T, int maxT, int H, int K, int E,
+                              const void* y, const int64_t* topk_idx, const float* topk_weights,
+                              const int32_t* slot, void* out, cudaStream_t stream);
+
+}  // namespace ep

@@ -1,0 +1,365 @@
+// ep_ll.cu -- low-latency (LL) dispatch and combine.
+//
+// LL dispatch ("DeepEP Normal vs Low-Latency 双模式深度分析", low-latency
+// dispatch and receive-layout excerpts; "Normal vs Low-Latency: 双通信哲学在
+// DeepEP V1/V2/DeepGEMM 中的三系统比较", message package; "第 4 章 V1：布局、
+// dispatch 与 combine" §4.3): every valid top-k slot (s, t, k) becomes one
+// message -- 16-byte header {t, 0, 0, 0}, payload, FP8 scales -- in the receive
+// rows of its expert e: recv_msgs[e][row] with e = d*EL + j.  The pages take a
+// slot with an atomicAdd on a per-expert counter, whose order depends on
+// timing; here the rows are fixed beforehand so the layout is deterministic:
+//   1. ll_count (one CTA per source rank): stable rank of each slot among the
+//      slots of the same (source, expert), in (token, k) order, and the count;
+//   2. ll_finish (E threads): begin of each source block = prefix over
+//      sources; packed_recv_count, packed_recv_layout_range, receive stats;
+//   3. ll_dispatch (one warp per token): read + cast the row once, write the
+//      message to each of its K destinations; the final row of every slot
+//      stays in the handle for the combine.
+// LL combine (§4.3): one warp per token gathers its K expert outputs and
+// accumulates w_k * y in fp32 with fused multiply-adds in slot order.
+#include "ep_common.cuh"
+#include "ep_kernels.h"
+
+namespace ep {
+
+namespace {
+
+constexpr int kLLCountWarps = kLLCountThreads / kWarpSize;
+constexpr int kLLUnroll = 4;
+constexpr int kLLCombineUnroll = 2;
+constexpr int kLLCombineFanIn = 4;
+
+__global__ void __launch_bounds__(kLLCountThreads)
+    ll_count_kernel(int R, int T, int maxT, int K, int E, const int64_t* __restrict__ topk_idx,
+                    int32_t* __restrict__ slot, int32_t* __restrict__ cnt, int32_t* status) {
+    extern __shared__ int32_t smem[];
+    int32_t* s_warp = smem;                   // [kLLCountWarps][E]: per-warp count -> exclusive prefix
+    int32_t* s_run = smem + kLLCountWarps * E;  // [E]: slots of this source seen so far
+    const int s = blockIdx.x;
+    const int tid = threadIdx.x;
+    const int lane = lane_id();
+    const int warp = tid / kWarpSize;
+    const int n = T * K;
+    const int64_t* idx_s = topk_idx + static_cast<int64_t>(s) * T * K;
+    int32_t* slot_s = slot + static_cast<int64_t>(s) * maxT * K;
+
+    for (int e = tid; e < E; e += kLLCountThreads) s_run[e] = 0;
+    for (int base = 0; base < n; base += kLLCountThreads) {
+        for (int i = tid; i < kLLCountWarps * E; i += kLLCountThreads) s_warp[i] = 0;
+        __syncthreads();
+        const int i = base + tid;
+        int e = -1;
+        if (i < n) {
+            const int64_t v = __ldg(idx_s + i);
+            if (v >= 0 && v < E) e = static_cast<int>(v);
+            else if (v != -1) report(status, EP_ERR_BAD_EXPERT);
+        }
+        const unsigned peers = __match_any_sync(kFullMask, e);
+        const int before = __popc(peers & lanemask_lt());
+        if (e >= 0 && before == 0) s_warp[warp * E + e] = __popc(peers);
+        __syncthreads();
+        for (int x = tid; x < E; x += kLLCountThreads) {
+            int32_t run = s_run[x];
+            for (int w = 0; w < kLLCountWarps; ++w) {
+                const int32_t c = s_warp[w * E + x];
+                s_warp[w * E + x] = run;
+                run += c;
+            }
+            s_run[x] = run;
+        }
+        __syncthreads();
+        if (i < n) slot_s[i] = e >= 0 ? s_warp[warp * E + e] + before : -1;
+        __syncthreads();
+    }
+    for (int e = tid; e < E; e += kLLCountThreads) cnt[static_cast<int64_t>(s) * E + e] = s_run[e];
+}
+
+__global__ void ll_finish_kernel(int R, int maxT, int E, const int32_t* __restrict__ cnt,
+                                 int32_t* __restrict__ packed_recv_count, int64_t* __restrict__ layout_range,
+                                 int32_t* __restrict__ stats, int32_t* status) {
+    const int64_t slots = static_cast<int64_t>(R) * maxT;
+    for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < E; e += gridDim.x * blockDim.x) {
+        int64_t begin = 0;
+        for (int s = 0; s < R; ++s) {
+            const int32_t c = __ldg(cnt + static_cast<int64_t>(s) * E + e);
+            layout_range[static_cast<int64_t>(e) * R + s] =
+                static_cast<int64_t>((static_cast<uint64_t>(c) << 32) | static_cast<uint32_t>(begin));
+            begin += c;
+        }
+        if (begin > slots) report(status, EP_ERR_CAPACITY);
+        const int32_t n = static_cast<int32_t>(begin < slots ? begin : slots);
+        packed_recv_count[e] = n;
+        if (stats != nullptr) stats[e] += n;
+    }
+}
+
+// One warp per source token.  kFp8: e4m3 payload + scales (fp32, or UE8M0 bytes).
+template <bool kFp8>
+__global__ void __launch_bounds__(kLLDispatchThreads)
+    ll_dispatch_kernel(int R, int T, int maxT, int H, int K, int E, const int4* __restrict__ x,
+                       const int64_t* __restrict__ topk_idx, bool round_scale, bool use_ue8m0,
+                       int32_t* __restrict__ slot, const int64_t* __restrict__ layout_range,
+                       uint8_t* __restrict__ recv_msgs, int64_t msg_bytes) {
+    constexpr int kWarps = kLLDispatchThreads / kWarpSize;
+    const int lane = lane_id();
+    const int64_t n_tokens = static_cast<int64_t>(R) * T;
+    const int64_t slots = static_cast<int64_t>(R) * maxT;
+    const int n16 = H / 8;
+    const int G = H / kFp8Group;
+
+    for (int64_t g = static_cast<int64_t>(blockIdx.x) * kWarps + threadIdx.x / kWarpSize; g < n_tokens;
+         g += static_cast<int64_t>(gridDim.x) * kWarps) {
+        const int s = static_cast<int>(g / T);
+        const int t = static_cast<int>(g - static_cast<int64_t>(s) * T);
+        // Lane k owns slot k: destination expert and final row.
+        int e = -1;
+        int64_t row = -1;
+        if (lane < K) {
+            const int64_t v = __ldg(topk_idx + g * K + lane);
+            int32_t* sp = slot + (static_cast<int64_t>(s) * maxT + t) * K + lane;
+            const int32_t pos = *sp;
+            if (v >= 0 && v < E && pos >= 0) {
+                e = static_cast<int>(v);
+                row = (__ldg(layout_range + static_cast<int64_t>(e) * R + s) & 0xffffffffLL) + pos;
+                if (row >= slots) row = -1;
+            }
+            *sp = row >= 0 ? static_cast<int32_t>(row) : -1;
+        }
+        const unsigned dst = __ballot_sync(kFullMask, row >= 0);
+        if (dst == 0u) continue;
+
+        // Header {t, 0, 0, 0}.
+        for (unsigned m = dst; m; m &= m - 1) {
+            const int k = __ffs(m) - 1;
+            const int ek = __shfl_sync(kFullMask, e, k);
+            const int64_t rk = __shfl_sync(kFullMask, row, k);
+            if (lane == 0)
+                st_stream_v4(reinterpret_cast<int4*>(recv_msgs + (static_cast<int64_t>(ek) * slots + rk) * msg_bytes),
+                             make_int4(t, 0, 0, 0));
+        }
+
+        const int4* src = x + g * n16;
+        if constexpr (!kFp8) {
+            for (int i0 = 0; i0 < n16; i0 += kWarpSize * kLLUnroll) {
+                int4 v[kLLUnroll];
+#pragma unroll
+                for (int u = 0; u < kLLUnroll; ++u) {
+                    const int i = i0 + u * kWarpSize + lane;
+                    if (i < n16) v[u] = ld_stream_v4(src + i);
+                }
+                for (unsigned m = dst; m; m &= m - 1) {
+                    const int k = __ffs(m) - 1;
+                    const int ek = __shfl_sync(kFullMask, e, k);
+                    const int64_t rk = __shfl_sync(kFullMask, row, k);
+                    int4* d = reinterpret_cast<int4*>(recv_msgs + (static_cast<int64_t>(ek) * slots + rk) * msg_bytes + 16);
+#pragma unroll
+                    for (int u = 0; u < kLLUnroll; ++u) {
+                        const int i = i0 + u * kWarpSize + lane;
+                        if (i < n16) st_stream_v4(d + i, v[u]);
+                    }
+                }
+            }
+        } else {
+            for (int i0 = 0; i0 < n16; i0 += kWarpSize * kLLUnroll) {
+                int4 v[kLLUnroll];
+#pragma unroll
+                for (int u = 0; u < kLLUnroll; ++u) {
+                    const int i = i0 + u * kWarpSize + lane;
+                    v[u] = i < n16 ? ld_stream_v4(src + i) : make_int4(0, 0, 0, 0);
+                }
+                int2 q[kLLUnroll];
+                float sc[kLLUnroll];
+                int ex[kLLUnroll];
+#pragma unroll
+                for (int u = 0; u < kLLUnroll; ++u) {
+                    float f[8];
+                    unpack8(v[u], f);
+                    float amax = absmax8(f);
+#pragma unroll
+                    for (int off = 8; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, off));
+                    const Fp8Scale fs = fp8_scale(amax, round_scale);
+                    q[u] = cast8_e4m3(f, fs.mult);
+                    sc[u] = fs.scale;
+                    ex[u] = fs.exponent;
+                }
+                for (unsigned m = dst; m; m &= m - 1) {
+                    const int k = __ffs(m) - 1;
+                    const int ek = __shfl_sync(kFullMask, e, k);
+                    const int64_t rk = __shfl_sync(kFullMask, row, k);
+                    uint8_t* msg = recv_msgs + (static_cast<int64_t>(ek) * slots + rk) * msg_bytes;
+                    int2* d = reinterpret_cast<int2*>(msg + 16);
+                    uint8_t* tail = msg + 16 + H;
+#pragma unroll
+                    for (int u = 0; u < kLLUnroll; ++u) {
+                        const int i = i0 + u * kWarpSize + lane;
+                        if (i < n16) {
+                            st_stream_v2(d + i, q[u]);
+                            if ((lane & 15) == 0) {
+                                if (use_ue8m0) tail[i / 16] = static_cast<uint8_t>(ex[u] + 127);
+                                else reinterpret_cast<float*>(tail)[i / 16] = sc[u];
+                            }
+                        }
+                    }
+                }
+            }
+            if (use_ue8m0) {
+                // Bytes [G, 4G) of the scale tail are zero (G is a multiple of 4).
+                for (unsigned m = dst; m; m &= m - 1) {
+                    const int k = __ffs(m) - 1;
+                    const int ek = __shfl_sync(kFullMask, e, k);
+                    const int64_t rk = __shfl_sync(kFullMask, row, k);
+                    uint32_t* z = reinterpret_cast<uint32_t*>(recv_msgs + (static_cast<int64_t>(ek) * slots + rk) * msg_bytes +
+                                                              16 + H + G);
+                    for (int w = lane; w < (3 * G) / 4; w += kWarpSize) z[w] = 0u;
+                }
+            }
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kLLCombineThreads)
+    ll_combine_kernel(int R, int T, int maxT, int H, int K, int E, const int4* __restrict__ y,
+                      const int64_t* __restrict__ topk_idx, const float* __restrict__ topk_weights,
+                      const int32_t* __restrict__ slot, int4* __restrict__ out) {
+    constexpr int kWarps = kLLCombineThreads / kWarpSize;
+    const int lane = lane_id();
+    const int64_t n_tokens = static_cast<int64_t>(R) * T;
+    const int64_t slots = static_cast<int64_t>(R) * maxT;
+    const int n16 = H / 8;
+
+    for (int64_t g = static_cast<int64_t>(blockIdx.x) * kWarps + threadIdx.x / kWarpSize; g < n_tokens;
+         g += static_cast<int64_t>(gridDim.x) * kWarps) {
+        const int s = static_cast<int>(g / T);
+        const int t = static_cast<int>(g - static_cast<int64_t>(s) * T);
+        int64_t src_row = -1;  // flat row e * slots + row
+        float w = 0.0f;
+        if (lane < K) {
+            const int64_t v = __ldg(topk_idx + g * K + lane);
+            const int32_t r = __ldg(slot + (static_cast<int64_t>(s) * maxT + t) * K + lane);
+            if (v >= 0 && v < E && r >= 0) {
+                src_row = v * slots + r;
+                w = __ldg(topk_weights + g * K + lane);
+            }
+        }
+        const unsigned valid = __ballot_sync(kFullMask, src_row >= 0);
+
+        for (int i0 = 0; i0 < n16; i0 += kWarpSize * kLLCombineUnroll) {
+            float acc[kLLCombineUnroll][8];
+#pragma unroll
+            for (int u = 0; u < kLLCombineUnroll; ++u)
+#pragma unroll
+                for (int q = 0; q < 8; ++q) acc[u][q] = 0.0f;
+            unsigned m = valid;
+            while (m) {
+                int kk[kLLCombineFanIn];
+                int64_t sr[kLLCombineFanIn];
+                float wk[kLLCombineFanIn];
+#pragma unroll
+                for (int j = 0; j < kLLCombineFanIn; ++j) {
+                    kk[j] = m ? __ffs(m) - 1 : -1;
+                    if (m) m &= m - 1;
+                    const int srcl = kk[j] < 0 ? 0 : kk[j];
+                    sr[j] = __shfl_sync(kFullMask, src_row, srcl);
+                    wk[j] = __shfl_sync(kFullMask, w, srcl);
+                }
+                int4 v[kLLCombineFanIn][kLLCombineUnroll];
+#pragma unroll
+                for (int j = 0; j < kLLCombineFanIn; ++j)
+#pragma unroll
+                    for (int u = 0; u < kLLCombineUnroll; ++u) {
+                        const int i = i0 + u * kWarpSize + lane;
+                        if (kk[j] >= 0 && i < n16) v[j][u] = ld_stream_v4(y + sr[j] * n16 + i);
+                    }
+#pragma unroll
+                for (int j = 0; j < kLLCombineFanIn; ++j) {
+                    if (kk[j] < 0) continue;
+#pragma unroll
+                    for (int u = 0; u < kLLCombineUnroll; ++u) {
+                        float f[8];
+                        unpack8(v[j][u], f);
+#pragma unroll
+                        for (int q = 0; q < 8; ++q) acc[u][q] = __fmaf_rn(wk[j], f[q], acc[u][q]);
+                    }
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < kLLCombineUnroll; ++u) {
+                const int i = i0 + u * kWarpSize + lane;
+                if (i < n16) out[g * n16 + i] = pack8_bf16(acc[u]);
+            }
+        }
+    }
+}
+
+template <typename Kernel>
+int resident_blocks(Kernel k, int threads, int num_sms, size_t smem = 0) {
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, threads, smem) != cudaSuccess || per_sm < 1)
+        per_sm = 1;
+    return per_sm * num_sms;
+}
+
+int clamp_grid(int planned, int64_t warps_needed, int warps_per_block) {
+    const int64_t need = (warps_needed + warps_per_block - 1) / warps_per_block;
+    return static_cast<int>(need < planned ? (need > 0 ? need : 1) : planned);
+}
+
+size_t ll_count_smem(int E) { return sizeof(int32_t) * static_cast<size_t>(kLLCountWarps + 1) * E; }
+
+}  // namespace
+
+cudaError_t plan_ll(LaunchPlan* plan, int num_experts) {
+    const int n = plan->num_sms;
+    plan->ll_dispatch_blocks[0] = resident_blocks(ll_dispatch_kernel<false>, kLLDispatchThreads, n);
+    plan->ll_dispatch_blocks[1] = resident_blocks(ll_dispatch_kernel<true>, kLLDispatchThreads, n);
+    plan->ll_combine_blocks = resident_blocks(ll_combine_kernel, kLLCombineThreads, n);
+    const size_t smem = ll_count_smem(num_experts);
+    if (smem > 48 * 1024)
+        return cudaFuncSetAttribute(ll_count_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    static_cast<int>(smem));
+    return cudaSuccess;
+}
+
+cudaError_t launch_ll_dispatch(const LaunchPlan& plan, int R, int T, int maxT, int H, int K, int E,
+                               const void* x, const int64_t* topk_idx, bool use_fp8, bool round_scale,
+                               bool use_ue8m0, int32_t* slot, int32_t* cnt, void* recv_msgs,
+                               int32_t* packed_recv_count, int64_t* layout_range, int32_t* stats,
+                               int32_t* status, cudaStream_t stream) {
+    ll_count_kernel<<<R, kLLCountThreads, ll_count_smem(E), stream>>>(R, T, maxT, K, E, topk_idx, slot, cnt,
+                                                                      status);
+    cudaError_t err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+    const int fin_threads = 256;
+    ll_finish_kernel<<<(E + fin_threads - 1) / fin_threads, fin_threads, 0, stream>>>(
+        R, maxT, E, cnt, packed_recv_count, layout_range, stats, status);
+    err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+    const int64_t n_tokens = static_cast<int64_t>(R) * T;
+    if (n_tokens == 0) return cudaSuccess;
+    const int64_t msg = ep_ll_msg_bytes(H, use_fp8 ? 1 : 0);
+    const int grid = clamp_grid(plan.ll_dispatch_blocks[use_fp8 ? 1 : 0], n_tokens, kLLDispatchThreads / kWarpSize);
+    const bool rs = round_scale || use_ue8m0;
+    if (use_fp8)
+        ll_dispatch_kernel<true><<<grid, kLLDispatchThreads, 0, stream>>>(
+            R, T, maxT, H, K, E, static_cast<const int4*>(x), topk_idx, rs, use_ue8m0, slot, layout_range,
+            static_cast<uint8_t*>(recv_msgs), msg);
+    else
+        ll_dispatch_kernel<false><<<grid, kLLDispatchThreads, 0, stream>>>(
+            R, T, maxT, H, K, E, static_cast<const int4*>(x), topk_idx, rs, use_ue8m0, slot, layout_range,
+            static_cast<uint8_t*>(recv_msgs), msg);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_ll_combine(const LaunchPlan& plan, int R, int T, int maxT, int H, int K, int E,
+                              const void* y, const int64_t* topk_idx, const float* topk_weights,
+                              const int32_t* slot, void* out, cudaStream_t stream) {
+    const int64_t n_tokens = static_cast<int64_t>(R) * T;
+    if (n_tokens == 0) return cudaSuccess;
+    const int grid = clamp_grid(plan.ll_combine_blocks, n_tokens, kLLCombineThreads / kWarpSize);
+    ll_combine_kernel<<<grid, kLLCombineThreads, 0, stream>>>(R, T, maxT, H, K, E, static_cast<const int4*>(y),
+                                                              topk_idx, topk_weights, slot,
+                                                              static_cast<int4*>(out));
+    return cudaGetLastError();
+}
+
+}  // namespace ep

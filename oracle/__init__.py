@@ -192,7 +192,8 @@ def dispatch(x, send_head, capacity: int, num_experts: int, mode: int = MODE_BF1
         out.setdefault("recv_x_scales", np.zeros((R, capacity, G), np.float32))
     if topk_idx is not None:
         out.setdefault("recv_topk_idx", np.full((R, capacity, K), -2, np.int64))
-        out.setdefault("recv_topk_weights", np.full((R, capacity, K), np.nan, np.float32))
+        if topk_weights is not None:
+            out.setdefault("recv_topk_weights", np.full((R, capacity, K), np.nan, np.float32))
     xs = _c(x, np.uint8 if mode == MODE_FP8_IN else np.uint16)
     tok = _c(tokens, np.int64)
     _check(_load().oracle_dispatch(

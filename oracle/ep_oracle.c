@@ -358,7 +358,8 @@ int oracle_dispatch(int R, int T, int H, int K, int E, int64_t cap, int mode,
                 int64_t e = topk_idx ? topk_idx[(size_t)g * K + k] : -1;
                 int mine = e >= 0 && e / EL == r;
                 if (recv_topk_idx) recv_topk_idx[dst * K + k] = mine ? e % EL : -1;
-                if (recv_topk_weights) recv_topk_weights[dst * K + k] = mine ? topk_weights[(size_t)g * K + k] : 0.0f;
+                if (recv_topk_weights && topk_weights)
+                    recv_topk_weights[dst * K + k] = mine ? topk_weights[(size_t)g * K + k] : 0.0f;
             }
         }
     }

@@ -1,0 +1,272 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle, element by element.
+
+Sizes span several CTA tiles / scan rounds and ragged tails; integer, index,
+bf16 and FP8 outputs must be bit-exact; combine outputs are compared exactly
+as well (same fp32 order) and additionally against the 5e-6 relative bound.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from combine_get_dispatch_03_gb300 import ep
+from combine_get_dispatch_03_gb300 import workloads as W
+
+import _parity as P
+
+pytestmark = pytest.mark.gpu
+
+REL_TOL = 5e-6  # combine tolerance (fp32 accumulation)
+
+
+def S(name, R, T, H, E, K, routing="uniform", mask_p=0.0, C=12, A=1, seed=0, **kw):
+    return W.Shape(name, R=R, T=T, H=H, E=E, K=K, routing=routing, mask_p=mask_p, C=C, A=A,
+                   seed=90000 + seed, **kw)
+
+
+NORMAL_CASES = [
+    S("r1", 1, 37, 256, 4, 2, seed=1),
+    S("r2_ragged", 2, 1500, 512, 8, 3, mask_p=0.1, C=5, A=4, seed=2),
+    S("r3_odd", 3, 1025, 128, 12, 4, routing="zipf", mask_p=0.05, C=7, seed=3),
+    S("r8_small", 8, 256, 1024, 32, 4, seed=4),
+    S("r8_v3_like", 8, 700, 7168, 256, 8, routing="gumbel", A=128, seed=5),
+    S("r16_zipf", 16, 333, 2048, 256, 8, routing="zipf", mask_p=0.05, seed=6),
+    S("r32", 32, 65, 1024, 256, 8, seed=7),
+    S("r5_multiround", 5, 4100, 256, 20, 2, mask_p=0.3, C=12, seed=8),
+    S("r8_allmasked", 8, 40, 256, 32, 4, mask_p=1.0, seed=9),
+    S("r4_T1", 4, 1, 256, 16, 4, seed=10),
+    S("r17_nodes", 17, 50, 256, 34, 5, routing="zipf", mask_p=0.1, seed=11),
+]
+
+
+@pytest.mark.parametrize("shape", NORMAL_CASES, ids=lambda s: s.name)
+def test_layout_and_record(shape):
+    res = P.run_normal(shape, with_weights=True)
+    assert res["status"] == 0
+    P.compare_layout(res["lay"], res["ora_lay"])
+    P.compare_record(res["h"], res["ora_n"], shape.T)
+
+
+@pytest.mark.parametrize("shape", NORMAL_CASES, ids=lambda s: s.name)
+def test_dispatch_bf16_and_combine(shape):
+    res = P.run_normal(shape, with_weights=True)
+    assert res["status"] == 0 and res["combine_status"] == 0
+    P.compare_dispatch(res, shape, O.MODE_BF16)
+    np.testing.assert_array_equal(P.host(res["c"]["combined_x"]), res["ora_c"]["out"])
+    np.testing.assert_array_equal(P.host(res["c"]["combined_topk_weights"]), res["ora_c"]["combined_topk_weights"])
+
+
+@pytest.mark.parametrize("shape", NORMAL_CASES[:7], ids=lambda s: s.name)
+def test_combine_fp32_biases_fresh_outputs(shape):
+    res = P.run_normal(shape, with_weights=True, biases=True, out_fp32=True, y_seed=shape.seed + 77)
+    assert res["combine_status"] == 0
+    got = P.host(res["c"]["combined_x"])
+    want = res["ora_c"]["out"]
+    assert P.rel_err(got, want) <= REL_TOL
+    np.testing.assert_array_equal(got, want)
+
+
+@pytest.mark.parametrize("shape", NORMAL_CASES[:7], ids=lambda s: s.name)
+def test_combine_bf16_biases(shape):
+    res = P.run_normal(shape, with_weights=False, biases=True, out_fp32=False, y_seed=shape.seed + 78)
+    assert res["combine_status"] == 0
+    np.testing.assert_array_equal(P.host(res["c"]["combined_x"]), res["ora_c"]["out"])
+
+
+FP8_CASES = [c for c in NORMAL_CASES if c.H % 128 == 0]
+
+
+@pytest.mark.parametrize("shape", FP8_CASES, ids=lambda s: s.name)
+def test_dispatch_cast_fp8(shape):
+    shape = W.Shape(**{**shape.__dict__, "outlier_frac": 0.01, "outlier_scale": 50.0})
+    res = P.run_normal(shape, mode=O.MODE_CAST_FP8)
+    assert res["status"] == 0
+    P.compare_dispatch(res, shape, O.MODE_CAST_FP8)
+
+
+@pytest.mark.parametrize("shape", FP8_CASES[:5], ids=lambda s: s.name)
+def test_dispatch_fp8_input(shape):
+    res = P.run_normal(shape, mode=O.MODE_FP8_IN)
+    assert res["status"] == 0
+    P.compare_dispatch(res, shape, O.MODE_FP8_IN)
+
+
+def test_cached_dispatch_reuses_record():
+    shape = S("cached", 8, 900, 1024, 64, 6, routing="gumbel", mask_p=0.05, seed=20)
+    res = P.run_normal(shape)
+    h = res["h"]
+    x2 = W.normal_bf16((shape.R, shape.T, shape.H), 4321, "x2")
+    out = P.Guarded((shape.R, res["cap"], shape.H), torch.bfloat16)
+    ep.ep_dispatch(h, x2.to(P.DEV), cached=True, recv_x=out.t)
+    assert h.status() == 0
+    ora = O.dispatch(W.bf16_bits(x2), res["ora_n"]["send_head"], res["cap"], shape.E)
+    rows = P.valid_rows(res["ora_n"]["num_recv"], res["cap"])
+    np.testing.assert_array_equal(P.host(out.t)[rows], ora["recv_x"][rows])
+    out.check()
+    # cached FP8 cast as well
+    q = P.Guarded((shape.R, res["cap"], shape.H), torch.float8_e4m3fn)
+    s = P.Guarded((shape.R, res["cap"], shape.H // 128), torch.float32)
+    ep.ep_dispatch(h, x2.to(P.DEV), cached=True, cast_to_fp8=True, recv_x=q.t, recv_x_scales=s.t)
+    assert h.status() == 0
+    ora = O.dispatch(W.bf16_bits(x2), res["ora_n"]["send_head"], res["cap"], shape.E, mode=O.MODE_CAST_FP8)
+    np.testing.assert_array_equal(P.host(q.t)[rows], ora["recv_x"][rows])
+    np.testing.assert_array_equal(P.host(s.t)[rows], ora["recv_x_scales"][rows])
+    q.check()
+    s.check()
+
+
+def test_combine_of_dispatch_restores_x():
+    """combine(dispatch(x)) / (number of receiving ranks) == x exactly (fp32 out)."""
+    shape = S("roundtrip", 8, 300, 1024, 32, 4, mask_p=0.1, seed=21)
+    res = P.run_normal(shape, out_fp32=True)
+    got = P.host(res["c"]["combined_x"])
+    n = res["ora_lay"]["is_token_in_rank"].sum(axis=2).astype(np.float32)
+    x = (res["x"].astype(np.uint32) << 16).view(np.float32)
+    hit = n > 0
+    np.testing.assert_array_equal((got / np.where(hit, n, 1)[..., None])[hit], x[hit])
+    assert (got[~hit] == 0).all()
+
+
+def test_capacity_overflow_is_reported_and_bounded():
+    shape = S("cap", 4, 200, 256, 16, 4, seed=22)
+    idx, _ = W.routing(shape)
+    need = P.needed_capacity(idx, shape.E)
+    res = P.run_normal(shape, cap=need - 5)
+    assert res["status"] == 2  # EP_ERR_CAPACITY
+    P.compare_dispatch(res, shape, O.MODE_BF16)  # rows that fit are exact; guards intact
+
+
+def test_bad_expert_is_reported():
+    shape = S("bad", 2, 64, 128, 8, 2, seed=23)
+    h = ep.Handle(P.config_of(shape, 256))
+    idx, _ = W.routing(shape)
+    idx[1, 5, 1] = 8  # == E
+    ep.ep_get_dispatch_layout(h, torch.from_numpy(idx).to(P.DEV))
+    assert h.status() == 7
+
+
+def test_inconsistent_counts_are_reported():
+    shape = S("inc", 4, 64, 128, 16, 2, seed=24)
+    idx, w = W.routing(shape)
+    h = ep.Handle(P.config_of(shape, 512))
+    lay = ep.ep_get_dispatch_layout(h, torch.from_numpy(idx).to(P.DEV))
+    tpr = lay["num_tokens_per_rank"].clone()
+    tpr[1, 2] += 1
+    ep.ep_dispatch(h, W.tokens_x(shape).to(P.DEV), topk_idx=torch.from_numpy(idx).to(P.DEV),
+                   num_tokens_per_rank=tpr, is_token_in_rank=lay["is_token_in_rank"],
+                   num_tokens_per_expert=lay["num_tokens_per_expert"])
+    assert h.status() == 6
+
+
+def test_zero_tokens():
+    shape = S("empty", 4, 0, 256, 16, 4, seed=25)
+    h = ep.Handle(ep.Config(4, 8, 256, 16, 4, 12, 4, 8))
+    idx = torch.zeros((4, 0, 4), dtype=torch.int64, device=P.DEV)
+    lay = ep.ep_get_dispatch_layout(h, idx)
+    x = torch.zeros((4, 0, 256), dtype=torch.bfloat16, device=P.DEV)
+    d = ep.ep_dispatch(h, x, topk_idx=idx, topk_weights=torch.zeros((4, 0, 4), device=P.DEV),
+                       num_tokens_per_rank=lay["num_tokens_per_rank"], is_token_in_rank=lay["is_token_in_rank"],
+                       num_tokens_per_expert=lay["num_tokens_per_expert"])
+    c = ep.ep_combine(h, d["recv_x"])
+    assert h.status() == 0
+    assert (P.host(lay["num_tokens_per_rank"]) == 0).all()
+    assert (P.host(h.export("rank_prefix_matrix")) == 0).all()
+    assert (P.host(d["num_recv_tokens_per_expert"]) == 0).all()
+    assert c["combined_x"].shape == (4, 0, 256)
+
+
+def test_host_side_validation():
+    h = ep.Handle(ep.Config(4, 8, 256, 16, 4, 12, 1, 8))
+    x = torch.zeros((4, 9, 256), dtype=torch.bfloat16, device=P.DEV)  # T > num_max_tokens
+    idx = torch.zeros((4, 9, 4), dtype=torch.int64, device=P.DEV)
+    with pytest.raises(ep.EPError):
+        ep.ep_get_dispatch_layout(h, idx)
+    with pytest.raises(ep.EPError):
+        ep.ep_combine(h, torch.zeros((4, 8, 256), dtype=torch.bfloat16, device=P.DEV))  # no dispatch yet
+    with pytest.raises(ep.EPError):
+        ep.ep_dispatch(h, x[:, :8].contiguous(), cached=True)  # no fresh dispatch yet
+
+
+# ----------------------------------------------------------------------------- low latency
+
+LL_CASES = [
+    S("ll_r2", 2, 5, 512, 8, 3, mask_p=0.1, seed=30, max_tokens=7),
+    S("ll_r4", 4, 33, 1024, 16, 4, seed=31, max_tokens=40),
+    S("ll_r8_zipf", 8, 64, 2048, 64, 8, routing="zipf", mask_p=0.05, seed=32, max_tokens=64),
+    S("ll_r32", 32, 12, 7168, 256, 8, seed=33, max_tokens=16),
+    S("ll_r3_full", 3, 100, 512, 6, 2, seed=34, max_tokens=100),
+]
+LL_FORMATS = ["bf16", "fp8", "fp8_round", "fp8_ue8m0"]
+
+
+def run_ll(shape, fmt):
+    use_fp8 = fmt != "bf16"
+    idx, w = W.routing(shape)
+    x = W.tokens_x(shape)
+    maxT = shape.max_tokens
+    cfg = P.config_of(shape, 0)
+    h = ep.Handle(cfg)
+    msg = ep.ep_ll_msg_bytes(shape.H, use_fp8)
+    msgs = P.Guarded((shape.R, shape.EL, shape.R * maxT, msg), torch.uint8)
+    stats = torch.full((shape.R, shape.EL), 3, dtype=torch.int32, device=P.DEV)
+    out = ep.ep_ll_dispatch(h, x.to(P.DEV), torch.from_numpy(idx).to(P.DEV), use_fp8=use_fp8,
+                            round_scale=fmt == "fp8_round", use_ue8m0=fmt == "fp8_ue8m0", recv_msgs=msgs.t,
+                            cumulative_local_expert_recv_stats=stats)
+    status = h.status()
+    ora = O.ll_dispatch(W.bf16_bits(x), idx, maxT, shape.E, use_fp8=use_fp8, round_scale=fmt == "fp8_round",
+                        use_ue8m0=fmt == "fp8_ue8m0")
+    return dict(h=h, idx=idx, w=w, x=x, out=out, ora=ora, msgs=msgs, stats=stats, status=status, msg=msg)
+
+
+@pytest.mark.parametrize("fmt", LL_FORMATS)
+@pytest.mark.parametrize("shape", LL_CASES, ids=lambda s: s.name)
+def test_ll_dispatch(shape, fmt):
+    r = run_ll(shape, fmt)
+    assert r["status"] == 0
+    ora, out, idx = r["ora"], r["out"], r["idx"]
+    np.testing.assert_array_equal(P.host(out["packed_recv_count"]), ora["packed_recv_count"])
+    np.testing.assert_array_equal(P.host(out["packed_recv_layout_range"]), ora["packed_recv_layout_range"])
+    np.testing.assert_array_equal(P.host(r["stats"]), ora["packed_recv_count"] + 3)
+    slot = P.host(r["h"].export("ll_slot_row"))[:, :shape.T]
+    np.testing.assert_array_equal(slot, ora["slot_row"])
+    msgs = P.host(out["recv_msgs"])
+    EL = shape.EL
+    s_, t_, k_ = np.nonzero(idx >= 0)
+    e = idx[s_, t_, k_]
+    rows = ora["slot_row"][s_, t_, k_]
+    np.testing.assert_array_equal(msgs[e // EL, e % EL, rows], ora["msgs_by_slot"][s_, t_, k_])
+    # rows past packed_recv_count are untouched
+    cnt = ora["packed_recv_count"]
+    untouched = np.arange(shape.R * shape.max_tokens)[None, None, :] >= cnt[:, :, None]
+    assert (msgs[untouched] == P.CANARY).all()
+    r["msgs"].check()
+
+
+@pytest.mark.parametrize("shape", LL_CASES, ids=lambda s: s.name)
+def test_ll_combine(shape):
+    r = run_ll(shape, "fp8_ue8m0")
+    idx, w = r["idx"], r["w"]
+    maxT = shape.max_tokens
+    y_host = np.zeros((shape.R, shape.EL, shape.R * maxT, shape.H), np.uint16)
+    cnt = r["ora"]["packed_recv_count"]
+    fresh = W.bf16_bits(W.normal_bf16((int(cnt.sum()), shape.H), shape.seed, "lly"))
+    mask = np.arange(shape.R * maxT)[None, None, :] < cnt[:, :, None]
+    y_host[mask] = fresh
+    y_dev = P.dev_bf16(y_host)
+    got = ep.ep_ll_combine(r["h"], y_dev, torch.from_numpy(idx).to(P.DEV), torch.from_numpy(w).to(P.DEV))
+    assert r["h"].status() == 0
+    want = O.ll_combine(y_host, idx, w, r["ora"]["slot_row"], maxT, shape.E)
+    np.testing.assert_array_equal(P.host(got), want)
+
+
+def test_ll_views():
+    shape = LL_CASES[1]
+    r = run_ll(shape, "fp8")
+    px, sc, src = ep.ll_views(r["out"]["recv_msgs"], shape.H, True)
+    idx = r["idx"]
+    s_, t_, k_ = np.nonzero(idx >= 0)
+    e = idx[s_, t_, k_]
+    rows = r["ora"]["slot_row"][s_, t_, k_]
+    np.testing.assert_array_equal(P.host(src)[e // shape.EL, e % shape.EL, rows], t_)
+    q = P.host(px.contiguous())[e // shape.EL, e % shape.EL, rows]
+    np.testing.assert_array_equal(q, r["ora"]["msgs_by_slot"][s_, t_, k_, 16:16 + shape.H])
