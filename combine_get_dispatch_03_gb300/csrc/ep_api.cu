@@ -117,6 +117,11 @@ ep_status check_tokens(const ep_handle* h, int32_t num_tokens) {
 
 }  // namespace
 
+namespace ep {
+// Lets other translation units of the library set the thread's ep_last_error() text.
+void record_error(const char* message) { g_last_error = message ? message : ""; }
+}  // namespace ep
+
 extern "C" {
 
 const char* ep_status_string(ep_status s) {

@@ -43,7 +43,7 @@ _lib = None
 EXPORTS = ("ep_handle_create", "ep_handle_destroy", "ep_handle_status", "ep_handle_num_recv",
            "ep_handle_field_bytes", "ep_handle_export", "ep_status_string", "ep_last_error",
            "ep_get_dispatch_layout", "ep_dispatch", "ep_combine", "ep_ll_msg_bytes", "ep_ll_dispatch",
-           "ep_ll_combine")
+           "ep_ll_combine", "ep_ll_dispatch_noalloc")
 
 
 def library_path() -> str:
@@ -78,8 +78,11 @@ def lib():
         L.ep_ll_msg_bytes.restype = I64
         L.ep_ll_dispatch.argtypes = [P, I32, P, P, I32, I32, I32, P, P, P, P, P]
         L.ep_ll_combine.argtypes = [P, P, P, P, P, P]
+        L.ep_ll_dispatch_noalloc.argtypes = [I32, I32, I32, I32, I32, I32, P, P, I32, I32, I32, P, P, P, P, P, P,
+                                             P]
         for name in ("ep_handle_create", "ep_handle_status", "ep_handle_num_recv", "ep_handle_export",
-                     "ep_get_dispatch_layout", "ep_dispatch", "ep_combine", "ep_ll_dispatch", "ep_ll_combine"):
+                     "ep_get_dispatch_layout", "ep_dispatch", "ep_combine", "ep_ll_dispatch", "ep_ll_combine",
+                     "ep_ll_dispatch_noalloc"):
             getattr(L, name).restype = S
         _lib = L
     return _lib

@@ -243,6 +243,42 @@ ep_status ep_ll_dispatch(ep_handle* h, int32_t num_tokens, const void* x, const 
 ep_status ep_ll_combine(ep_handle* h, const void* x, const int64_t* topk_idx,
                         const float* topk_weights, void* combined_x, ep_stream_t stream);
 
+/* ------------------------------------- low-latency dispatch, no allocation */
+
+/* Capacity of the fixed count scratch of ep_ll_dispatch_noalloc(): int32
+ * entries, one per (source rank, expert) pair, so num_ranks * num_experts
+ * may not exceed it.  64 KiB of device memory per GPU that loads the library. */
+#define EP_LL_NOALLOC_MAX_COUNTS 16384
+
+/* No counterpart on the pages: this is an addition of this library for
+ * callers that must not allocate device memory -- an engine plugin whose
+ * enqueue path may not allocate, a server that reserves all device memory at
+ * start-up, or a latency-critical loop that cannot take the synchronisation
+ * cudaMalloc/cudaFree may cause.  It computes exactly what ep_ll_dispatch()
+ * computes, without a handle: every buffer is the caller's, including the
+ * slot map slot_row (int32 [R][maxT][K], row of each valid slot in its
+ * expert's packed rows, -1 otherwise; ep_ll_dispatch() keeps it in the
+ * handle) and the status word `status` (one device int32 that the kernels
+ * set to the first error code and never clear; the caller zeroes it).
+ * The per-(source, expert) counts the kernels pass between them live in a
+ * file-scope __device__ array of EP_LL_NOALLOC_MAX_COUNTS entries, so
+ * num_ranks * num_experts beyond that is rejected with EP_ERR_UNSUPPORTED
+ * before anything is enqueued.  The function calls no cudaMalloc, cudaFree
+ * or other allocating routine.  Its first call on a device looks up the
+ * array's device address and the launch shapes for that device; make that
+ * first call before any stream capture.  Every call on a device shares the
+ * array (it keeps the last call's counts, and nothing in it needs clearing),
+ * so calls whose kernels may overlap on the GPU -- on different streams
+ * without an ordering between them -- race and must not be issued.
+ * Other sizes, layouts and errors as for ep_ll_dispatch(). */
+ep_status ep_ll_dispatch_noalloc(int32_t num_ranks, int32_t num_tokens, int32_t num_max_tokens,
+                                 int32_t hidden, int32_t num_experts, int32_t num_topk, const void* x,
+                                 const int64_t* topk_idx, int32_t use_fp8, int32_t round_scale,
+                                 int32_t use_ue8m0, void* recv_msgs, int32_t* packed_recv_count,
+                                 int64_t* packed_recv_layout_range,
+                                 int32_t* cumulative_local_expert_recv_stats, int32_t* slot_row,
+                                 int32_t* status, ep_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
