@@ -227,6 +227,8 @@ def run_ours(args):
     torch.cuda.set_device(dev)
     stream = torch.cuda.current_stream(dev)
     shape = W.WORKLOADS[HEADLINE]
+    if args.tokens:
+        shape = shape.scaled(T=args.tokens)
     R, T, H, E, K = shape.R, shape.T, shape.H, shape.E, shape.K
     st = prepare_normal(ep, shape, dev)
     h, cap, hits = st["h"], st["cap"], st["hits"]
@@ -339,13 +341,14 @@ def run_ours(args):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
-        cpu = cpu_baseline(shape, tokens=max(64, T // args.cpu_fraction), reps=1)
+        cpu = cpu_baseline(W.WORKLOADS[HEADLINE], tokens=max(64, W.WORKLOADS[HEADLINE].T // args.cpu_fraction),
+                           reps=2)
 
     result = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(step_ms, 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded routing and N(0,1) bf16 tokens)",
-        "config": {"workload": f"{HEADLINE}: R=8 T=4096 H=7168 E=256 K=8 Gumbel routing A=128 C=12; step = "
+        "config": {"workload": f"{HEADLINE}: R=8 T={T} H=7168 E=256 K=8 Gumbel routing A=128 C=12; step = "
                                "get_dispatch_layout + dispatch (fresh record) + combine (received rows, "
                                "top-k weight reduction)",
                    "l2": "no flush; inputs larger than L2 (x 470 MB, receive buffer %.2f GB vs 129 MB L2)"
@@ -496,53 +499,70 @@ def measure_other_ops(ep, dev, peak, reps=20):
 
 # ----------------------------------------------------------------------------- CPU oracle
 
-def cpu_baseline(shape, tokens: int, reps: int = 1):
-    """The CPU oracle, as it stands, on the first `tokens` tokens of every rank of the workload."""
-    import oracle as O
+def cpu_sample(shape, tokens: int):
+    """Inputs of the oracle sample: the first `tokens` tokens of every rank of the workload."""
     sub = W.Shape(**{**shape.__dict__, "T": tokens})
     idx, w = W.routing(shape)
     idx, w = np.ascontiguousarray(idx[:, :tokens]), np.ascontiguousarray(w[:, :tokens])
     x = W.bf16_bits(W.tokens_x(shape, device="cuda" if torch.cuda.is_available() else "cpu")[:, :tokens])
-    best = None
+    return sub, idx, w, x
+
+
+def cpu_step(sub, idx, w, x):
+    """One oracle pass (layout + notify + dispatch + combine); returns (seconds, hits)."""
+    import oracle as O
+    t0 = time.perf_counter()
+    lay = O.get_dispatch_layout(idx, sub.E, with_rdma=sub.R > 8)
+    cap = int(lay["num_tokens_per_rank"].sum(axis=0).max())
+    n = O.dispatch_notify(lay["num_tokens_per_rank"], lay["is_token_in_rank"], lay["num_tokens_per_expert"],
+                          sub.C, sub.A, cap)
+    d = O.dispatch(x, n["send_head"], cap, sub.E, topk_idx=idx, topk_weights=w)
+    O.combine(d["recv_x"], n["send_head"], recv_topk_weights=d["recv_topk_weights"])
+    return time.perf_counter() - t0, int(lay["num_tokens_per_rank"].sum())
+
+
+def cpu_describe(shape, tokens):
+    return (f"{HEADLINE} restricted to the first {tokens} of {shape.T} tokens of each of the {shape.R} ranks: "
+            "layout + notify + dispatch + combine, single-threaded C oracle")
+
+
+def cpu_baseline(shape, tokens: int, reps: int = 1):
+    """The CPU oracle, as it stands, timed on a bounded sample of the workload (best of reps)."""
+    sub, idx, w, x = cpu_sample(shape, tokens)
+    best, hits = None, 0
     for _ in range(reps):
-        t0 = time.perf_counter()
-        lay = O.get_dispatch_layout(idx, sub.E, with_rdma=sub.R > 8)
-        cap = int(lay["num_tokens_per_rank"].sum(axis=0).max())
-        n = O.dispatch_notify(lay["num_tokens_per_rank"], lay["is_token_in_rank"], lay["num_tokens_per_expert"],
-                              sub.C, sub.A, cap)
-        d = O.dispatch(x, n["send_head"], cap, sub.E, topk_idx=idx, topk_weights=w)
-        O.combine(d["recv_x"], n["send_head"], recv_topk_weights=d["recv_topk_weights"])
-        dt = time.perf_counter() - t0
+        dt, hits = cpu_step(sub, idx, w, x)
         best = dt if best is None else min(best, dt)
-    hits = int(lay["num_tokens_per_rank"].sum())
     b = normal_bytes(sub.R, tokens, sub.H, sub.K, hits)
     payload = b["dispatch"]["payload"] + b["combine"]["payload"]
     return {"value": round(payload / best / 1e9, 3), "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": f"{HEADLINE} restricted to the first {tokens} of {shape.T} tokens of each of the "
-                      f"{shape.R} ranks: layout + notify + dispatch + combine, single-threaded C",
-            "seconds": round(best, 3), "tokens_per_s": round(sub.R * tokens / best, 1)}
+            "sample": cpu_describe(shape, tokens), "seconds": round(best, 3),
+            "tokens_per_s": round(sub.R * tokens / best, 1)}
 
 
 def run_reference(args):
+    """The reference arm: the CPU oracle on the host cores, W warm-up and K timed sample steps."""
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
     shape = W.WORKLOADS[HEADLINE]
     tokens = max(64, shape.T // args.cpu_fraction)
-    # warm-up steps and timed steps, each one bounded sample of the workload
+    sub, idx, w, x = cpu_sample(shape, tokens)
     for _ in range(args.warmup):
-        pass
-    per = []
+        cpu_step(sub, idx, w, x)
+    secs, hits = [], 0
     for _ in range(args.steps):
-        per.append(cpu_baseline(shape, tokens=tokens, reps=1))
-    secs = [p["seconds"] for p in per]
-    value = statistics.median(p["value"] for p in per)
+        dt, hits = cpu_step(sub, idx, w, x)
+        secs.append(dt)
+    b = normal_bytes(sub.R, tokens, sub.H, sub.K, hits)
+    payload = b["dispatch"]["payload"] + b["combine"]["payload"]
+    value = round(payload * len(secs) / sum(secs) / 1e9, 4)
+    desc = cpu_describe(shape, tokens)
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": 1,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * statistics.median(secs), 2),
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * sum(secs) / len(secs), 2),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-            "data": "synthetic", "config": {"workload": per[0]["sample"]},
-            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
-                             "sample": per[0]["sample"]},
+            "data": "synthetic", "config": {"workload": desc},
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": desc},
             "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -558,6 +578,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-ops", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--tokens", type=int, default=0,
+                    help="tokens per rank of the headline workload (0 = its full 4096; smaller only for profiling)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
