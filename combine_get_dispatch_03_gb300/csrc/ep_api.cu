@@ -14,7 +14,7 @@
 #include "ep_kernels.h"
 
 namespace ep {
-cudaError_t plan_dispatch_combine(LaunchPlan* plan);
+cudaError_t plan_dispatch_combine(LaunchPlan* plan, int hidden);
 cudaError_t plan_ll(LaunchPlan* plan, int num_experts);
 }  // namespace ep
 
@@ -161,7 +161,7 @@ ep_status ep_handle_create(const ep_config* cfg, ep_handle** out) {
         return cuda_fail(err, "cudaGetDevice");
     }
     err = cudaDeviceGetAttribute(&h->plan.num_sms, cudaDevAttrMultiProcessorCount, h->device);
-    if (err == cudaSuccess) err = ep::plan_dispatch_combine(&h->plan);
+    if (err == cudaSuccess) err = ep::plan_dispatch_combine(&h->plan, cfg->hidden);
     if (err == cudaSuccess) err = ep::plan_ll(&h->plan, cfg->num_experts);
     if (err != cudaSuccess) {
         delete h;
@@ -361,7 +361,7 @@ ep_status ep_dispatch(ep_handle* h, int32_t num_tokens, const void* x, ep_dtype 
     err = ep::launch_dispatch(h->plan, mode, c.num_ranks, num_tokens, c.hidden, c.num_topk,
                               c.num_experts / c.num_ranks, c.recv_capacity, x, x_scales,
                               cached ? nullptr : topk_idx, cached ? nullptr : topk_weights, h->send_head, recv_x,
-                              recv_x_scales, recv_topk_idx, recv_topk_weights, stream);
+                              recv_x_scales, recv_topk_idx, recv_topk_weights, h->status, stream);
     if (err != cudaSuccess) return cuda_fail(err, "dispatch launch");
     return EP_OK;
 }

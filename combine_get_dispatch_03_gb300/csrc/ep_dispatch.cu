@@ -26,6 +26,7 @@ namespace {
 constexpr int kDispatchUnroll = 4;  // 16-byte vectors in flight per lane (payload read)
 constexpr int kCombineUnroll = 2;   // 16-byte columns per lane per pass
 constexpr int kCombineFanIn = 4;    // source rows loaded together before accumulation
+constexpr bool kUseBulkDispatch = true;  // bulk-copy (TMA 1D) dispatch where the rows fit in shared memory
 
 // Row of rank `lane` for token g, or -1 (not sent / past capacity).
 __device__ __forceinline__ int32_t dest_row(const int32_t* send_head, int64_t g, int R, int64_t cap, int lane) {
@@ -152,6 +153,165 @@ __global__ void __launch_bounds__(kDispatchThreads)
     }
 }
 
+// Bulk-copy dispatch: each CTA walks its tokens (blockIdx.x + j * gridDim.x)
+// through `stages` shared-memory row buffers.  Warp 0 lane 0 loads a row with
+// one bulk copy (completion counted on the stage's mbarrier) stages-1 tokens
+// ahead, and writes it to every destination row with one bulk store each; the
+// stores of token j form one bulk group, and a stage is refilled only after
+// the group that read it has finished reading.  In cast mode all warps of the
+// CTA turn the staged bf16 row into e4m3 codes + fp32 scales in a second
+// buffer first.  A wait that reaches its iteration cap reports
+// EP_ERR_TIMEOUT, lets the loads already issued land, and leaves.
+struct BulkSmem {
+    uint32_t in_stride, out_stride, meta_bytes, total;
+};
+
+__host__ __device__ __forceinline__ uint32_t align128(uint32_t v) { return (v + 127u) & ~127u; }
+
+__host__ __device__ __forceinline__ BulkSmem bulk_smem(int mode, int H, int stages) {
+    BulkSmem b;
+    const uint32_t in_bytes = mode == kModeFp8In ? H : 2 * H;
+    b.in_stride = align128(in_bytes);
+    b.out_stride = mode == kModeCastFp8 ? align128(H + 4 * (H / kFp8Group)) : 0;
+    b.meta_bytes = align128(64 + stages * (32 * 4 + 32 * 8 + 32 * 4) + 16);
+    b.total = b.meta_bytes + stages * (b.in_stride + b.out_stride);
+    return b;
+}
+
+template <int kMode>
+__global__ void dispatch_bulk_kernel(int R, int T, int H, int K, int EL, int64_t cap, int stages, bool scales_bulk,
+                                     const uint8_t* __restrict__ x, const float* __restrict__ x_scales,
+                                     const int64_t* __restrict__ topk_idx, const float* __restrict__ topk_weights,
+                                     const int32_t* __restrict__ send_head, uint8_t* __restrict__ recv_x,
+                                     float* __restrict__ recv_x_scales, int64_t* __restrict__ recv_topk_idx,
+                                     float* __restrict__ recv_topk_weights, int32_t* status) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int S = stages;
+    const int tid = threadIdx.x;
+    const int lane = lane_id();
+    const bool warp0 = tid < kWarpSize;
+    const int G = H / kFp8Group;
+    const uint32_t in_bytes = kMode == kModeFp8In ? H : 2 * H;
+    const uint32_t out_bytes = kMode == kModeBf16 ? 2 * H : H;  // payload bytes of one destination row
+    const BulkSmem lay = bulk_smem(kMode, H, S);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem);                       // [S], S <= 8
+    int32_t* s_row = reinterpret_cast<int32_t*>(smem + 64);                   // [S][32]
+    int64_t* s_idx = reinterpret_cast<int64_t*>(smem + 64 + S * 128);         // [S][32]
+    float* s_w = reinterpret_cast<float*>(smem + 64 + S * 384);               // [S][32]
+    int32_t* s_flag = reinterpret_cast<int32_t*>(smem + 64 + S * 512);
+    uint8_t* in_base = smem + lay.meta_bytes;
+    uint8_t* out_base = in_base + S * lay.in_stride;
+
+    const int64_t n_tokens = static_cast<int64_t>(R) * T;
+    const int64_t first = blockIdx.x, stride = gridDim.x;
+    const int64_t n_local = first < n_tokens ? (n_tokens - 1 - first) / stride + 1 : 0;
+    if (n_local == 0) return;
+    if (tid == 0) {
+        // one arrival with the row's transaction bytes + one per warp-0 lane for its metadata copies
+        for (int s = 0; s < S; ++s) mbar_init(&bars[s], 1 + kWarpSize);
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    // Warp 0: start the copies of the token's destination rows, top-k slots and row;
+    // all of them complete on the stage's barrier, so nothing here waits.
+    auto produce = [&](int64_t j) {
+        const int s = static_cast<int>(j % S);
+        const int64_t g = first + j * stride;
+        if (lane < R) cp_async_4(&s_row[s * 32 + lane], send_head + g * R + lane);
+        if (topk_idx != nullptr && lane < K) {
+            cp_async_8(&s_idx[s * 32 + lane], topk_idx + g * K + lane);
+            if (topk_weights != nullptr) cp_async_4(&s_w[s * 32 + lane], topk_weights + g * K + lane);
+        }
+        cp_async_arrive(&bars[s]);
+        if (lane == 0) {
+            mbar_arrive_expect_tx(&bars[s], in_bytes);
+            bulk_load(in_base + s * lay.in_stride, x + g * in_bytes, in_bytes, &bars[s]);
+        }
+    };
+
+    if (warp0) {
+        const int64_t pro = n_local < S - 1 ? n_local : S - 1;
+        for (int64_t j = 0; j < pro; ++j) produce(j);
+    }
+    int64_t j = 0;
+    for (; j < n_local; ++j) {
+        const int s = static_cast<int>(j % S);
+        if (tid == 0) *s_flag = mbar_wait_bounded(&bars[s], static_cast<uint32_t>((j / S) & 1)) ? 1 : 0;
+        __syncthreads();
+        if (*s_flag == 0) break;
+        const uint8_t* payload = in_base + s * lay.in_stride;
+        if constexpr (kMode == kModeCastFp8) {
+            const int4* xin = reinterpret_cast<const int4*>(payload);
+            uint8_t* qo = out_base + s * lay.out_stride;
+            float* so = reinterpret_cast<float*>(qo + H);
+            const int n16 = H / 8;
+            for (int i0 = (tid / kWarpSize) * kWarpSize; i0 < n16; i0 += blockDim.x) {
+                const int i = i0 + lane;
+                float f[8];
+                unpack8(i < n16 ? xin[i] : make_int4(0, 0, 0, 0), f);
+                float amax = absmax8(f);
+#pragma unroll
+                for (int off = 8; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, off));
+                const Fp8Scale fs = fp8_scale(amax, false);
+                if (i < n16) {
+                    reinterpret_cast<int2*>(qo)[i] = cast8_e4m3(f, fs.mult);
+                    if ((lane & 15) == 0) so[i / 16] = fs.scale;
+                }
+            }
+            fence_async_smem();
+            __syncthreads();
+            payload = qo;
+        }
+        if (warp0) {
+            int32_t row = lane < R ? s_row[s * 32 + lane] : -1;
+            if (row >= cap) row = -1;
+            const unsigned dst = __ballot_sync(kFullMask, row >= 0);
+            if (lane == 0) {
+                for (unsigned m = dst; m; m &= m - 1) {
+                    const int r = __ffs(m) - 1;
+                    const int64_t drow = static_cast<int64_t>(r) * cap + s_row[s * 32 + r];
+                    bulk_store(recv_x + drow * out_bytes, payload, out_bytes);
+                    if (kMode == kModeCastFp8 && scales_bulk)
+                        bulk_store(recv_x_scales + drow * G, payload + H, 4 * G);
+                }
+                bulk_commit();
+            }
+            const int64_t g = first + j * stride;
+            for (unsigned m = dst; m; m &= m - 1) {
+                const int r = __ffs(m) - 1;
+                const int64_t drow = static_cast<int64_t>(r) * cap + s_row[s * 32 + r];
+                if ((recv_topk_idx != nullptr || recv_topk_weights != nullptr) && lane < K) {
+                    const int64_t e = s_idx[s * 32 + lane];
+                    const bool mine = e >= 0 && static_cast<int>(e) / EL == r;
+                    if (recv_topk_idx != nullptr) recv_topk_idx[drow * K + lane] = mine ? e % EL : -1;
+                    if (recv_topk_weights != nullptr)
+                        recv_topk_weights[drow * K + lane] = (mine && topk_weights != nullptr) ? s_w[s * 32 + lane] : 0.0f;
+                }
+                if (kMode == kModeFp8In)
+                    for (int i = lane; i < G; i += kWarpSize) recv_x_scales[drow * G + i] = __ldg(x_scales + g * G + i);
+                if (kMode == kModeCastFp8 && !scales_bulk) {
+                    const float* so = reinterpret_cast<const float*>(payload + H);
+                    for (int i = lane; i < G; i += kWarpSize) recv_x_scales[drow * G + i] = so[i];
+                }
+            }
+            // Refill the stage that token j-1 used once its stores have read it.
+            if (j + S - 1 < n_local) {
+                if (lane == 0) bulk_wait_read<1>();
+                __syncwarp();
+                produce(j + S - 1);
+            }
+        }
+    }
+    if (j < n_local && tid == 0) {
+        report(status, EP_ERR_TIMEOUT);
+        // Let the row loads already issued land before this CTA's shared memory is released.
+        const int64_t issued = (j + S - 1 < n_local) ? j + S - 1 : n_local;
+        for (int64_t k = j + 1; k < issued; ++k) mbar_wait_bounded(&bars[k % S], static_cast<uint32_t>((k / S) & 1));
+    }
+    if (tid == 0) bulk_wait_all();
+}
+
 template <bool kOutF32>
 __global__ void __launch_bounds__(kCombineThreads)
     combine_kernel(int R, int T, int H, int K, int64_t cap, const int32_t* __restrict__ send_head,
@@ -254,8 +414,40 @@ int clamp_grid(int planned, int64_t warps_needed, int warps_per_block) {
 
 }  // namespace
 
-cudaError_t plan_dispatch_combine(LaunchPlan* plan) {
+int bulk_stages(int mode, int H) {
+    // about 64 KB of row buffers per CTA, between 2 and 8 stages
+    const uint32_t per = bulk_smem(mode, H, 1).in_stride + bulk_smem(mode, H, 1).out_stride;
+    int s = static_cast<int>(65536u / per);
+    return s < 2 ? 2 : (s > 8 ? 8 : s);
+}
+
+int bulk_threads(int mode) { return mode == kModeCastFp8 ? 4 * kWarpSize : kWarpSize; }
+
+template <int kMode>
+cudaError_t plan_bulk(LaunchPlan* plan, int H) {
+    const int S = bulk_stages(kMode, H);
+    const uint32_t smem = bulk_smem(kMode, H, S).total;
+    plan->bulk_stages[kMode] = 0;
+    if (smem > 200u * 1024u) return cudaSuccess;  // rows too long to stage: the register kernel is used
+    cudaError_t err = cudaFuncSetAttribute(dispatch_bulk_kernel<kMode>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           static_cast<int>(smem));
+    if (err != cudaSuccess) return err;
+    int per_sm = 0;
+    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, dispatch_bulk_kernel<kMode>, bulk_threads(kMode), smem);
+    if (err != cudaSuccess) return err;
+    if (per_sm < 1) return cudaSuccess;
+    plan->bulk_stages[kMode] = S;
+    plan->bulk_smem[kMode] = smem;
+    plan->bulk_blocks[kMode] = per_sm * plan->num_sms;
+    return cudaSuccess;
+}
+
+cudaError_t plan_dispatch_combine(LaunchPlan* plan, int H) {
     const int n = plan->num_sms;
+    cudaError_t err = plan_bulk<kModeBf16>(plan, H);
+    if (err == cudaSuccess && H % kFp8Group == 0) err = plan_bulk<kModeCastFp8>(plan, H);
+    if (err == cudaSuccess && H % kFp8Group == 0) err = plan_bulk<kModeFp8In>(plan, H);
+    if (err != cudaSuccess) return err;
     plan->dispatch_blocks[kModeBf16] = resident_blocks(dispatch_kernel<kModeBf16>, kDispatchThreads, n);
     plan->dispatch_blocks[kModeCastFp8] = resident_blocks(dispatch_kernel<kModeCastFp8>, kDispatchThreads, n);
     plan->dispatch_blocks[kModeFp8In] = resident_blocks(dispatch_kernel<kModeFp8In>, kDispatchThreads, n);
@@ -268,9 +460,37 @@ cudaError_t launch_dispatch(const LaunchPlan& plan, int mode, int R, int T, int 
                             const void* x, const float* x_scales, const int64_t* topk_idx,
                             const float* topk_weights, const int32_t* send_head, void* recv_x,
                             float* recv_x_scales, int64_t* recv_topk_idx, float* recv_topk_weights,
-                            cudaStream_t stream) {
+                            int32_t* status, cudaStream_t stream) {
     const int64_t n_tokens = static_cast<int64_t>(R) * T;
     if (n_tokens == 0) return cudaSuccess;
+    if (kUseBulkDispatch && plan.bulk_stages[mode] > 0) {
+        const int grid = clamp_grid(plan.bulk_blocks[mode], n_tokens, 1);
+        const int S = plan.bulk_stages[mode];
+        const uint32_t smem = plan.bulk_smem[mode];
+        const int threads = bulk_threads(mode);
+        const int G = H / kFp8Group;
+        const bool scales_bulk = (G % 4 == 0) && ((reinterpret_cast<uintptr_t>(recv_x_scales) & 15u) == 0);
+        const uint8_t* xb = static_cast<const uint8_t*>(x);
+        uint8_t* rb = static_cast<uint8_t*>(recv_x);
+        switch (mode) {
+            case kModeBf16:
+                dispatch_bulk_kernel<kModeBf16><<<grid, threads, smem, stream>>>(
+                    R, T, H, K, EL, cap, S, scales_bulk, xb, x_scales, topk_idx, topk_weights, send_head, rb,
+                    recv_x_scales, recv_topk_idx, recv_topk_weights, status);
+                break;
+            case kModeCastFp8:
+                dispatch_bulk_kernel<kModeCastFp8><<<grid, threads, smem, stream>>>(
+                    R, T, H, K, EL, cap, S, scales_bulk, xb, x_scales, topk_idx, topk_weights, send_head, rb,
+                    recv_x_scales, recv_topk_idx, recv_topk_weights, status);
+                break;
+            default:
+                dispatch_bulk_kernel<kModeFp8In><<<grid, threads, smem, stream>>>(
+                    R, T, H, K, EL, cap, S, scales_bulk, xb, x_scales, topk_idx, topk_weights, send_head, rb,
+                    recv_x_scales, recv_topk_idx, recv_topk_weights, status);
+                break;
+        }
+        return cudaGetLastError();
+    }
     const int grid = clamp_grid(plan.dispatch_blocks[mode], n_tokens, kDispatchThreads / kWarpSize);
     switch (mode) {
         case kModeBf16:

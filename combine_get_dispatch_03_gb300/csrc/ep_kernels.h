@@ -15,12 +15,15 @@ struct LaunchPlan {
     int combine_blocks[2] = {0, 0};      // bf16 out, fp32 out
     int ll_dispatch_blocks[2] = {0, 0};  // bf16, fp8
     int ll_combine_blocks = 0;
+    int bulk_stages[3] = {0, 0, 0};      // bulk-copy dispatch: stages per CTA (0 = not usable)
+    unsigned bulk_smem[3] = {0, 0, 0};   // its dynamic shared memory
+    int bulk_blocks[3] = {0, 0, 0};      // its resident grid
 };
 
 constexpr int kLayoutThreads = 1024;
 constexpr int kNotifyThreads = 1024;
 constexpr int kDispatchThreads = 512;
-constexpr int kCombineThreads = 512;
+constexpr int kCombineThreads = 256;
 constexpr int kLLCountThreads = 512;
 constexpr int kLLDispatchThreads = 512;
 constexpr int kLLCombineThreads = 512;
@@ -43,7 +46,7 @@ cudaError_t launch_dispatch(const LaunchPlan& plan, int mode, int R, int T, int 
                             const void* x, const float* x_scales, const int64_t* topk_idx,
                             const float* topk_weights, const int32_t* send_head, void* recv_x,
                             float* recv_x_scales, int64_t* recv_topk_idx, float* recv_topk_weights,
-                            cudaStream_t stream);
+                            int32_t* status, cudaStream_t stream);
 
 cudaError_t launch_combine(const LaunchPlan& plan, bool out_fp32, int R, int T, int H, int K, int64_t cap,
                            const int32_t* send_head, const void* y, const float* recv_topk_weights,

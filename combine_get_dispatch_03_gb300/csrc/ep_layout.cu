@@ -7,23 +7,25 @@
 // row, ordered by source rank then token, with channel prefix matrices at
 // the boundaries of C contiguous token ranges.
 //
-// Both kernels run one CTA per source rank: the per-rank work is a few
-// hundred KB of routing data, so a single CTA with every load of a round in
-// flight reads it in a couple of microseconds, and keeping a source rank in
-// one CTA makes its token scan a block-local scan (no cross-CTA waiting and
-// no scratch memory).  A second grid slot (blockIdx.x == R) of the notify
-// kernel folds the R x R and R x E summaries.
+// Both kernels give each source rank one thread-block cluster of kClusterCtas
+// CTAs; CTA q of the cluster owns the q-th contiguous slice of that rank's
+// tokens.  Partial counts are exchanged through distributed shared memory
+// after a cluster barrier, so a kernel is one launch with no global scratch,
+// no atomics on global memory and no waiting on other launches.
+#include <cooperative_groups.h>
+
 #include "ep_common.cuh"
 #include "ep_kernels.h"
+
+namespace cg = cooperative_groups;
 
 namespace ep {
 
 namespace {
 
-constexpr int kLayoutRound = 4096;  // tokens per round of the layout kernel (mask staging in smem)
-constexpr int kLayoutUnroll = 8;    // top-k entries in flight per thread
-constexpr int kNotifyTPT = 4;       // tokens per thread per notify round
-constexpr int kNotifyRound = kNotifyThreads * kNotifyTPT;
+constexpr int kClusterCtas = 8;      // CTAs per source rank (portable cluster size)
+constexpr int kLayoutRound = 2048;   // tokens of one round of the layout kernel (mask staging in smem)
+constexpr int kLayoutUnroll = 8;     // top-k entries in flight per thread
 constexpr int kNotifyWarps = kNotifyThreads / kWarpSize;
 
 // Mask of destination ranks of one token from its R-byte is_token_in_rank row.
@@ -58,6 +60,14 @@ __device__ __forceinline__ void store_rank_mask(uint8_t* row, int R, uint32_t m)
     }
 }
 
+// Token slice [lo, hi) of CTA q of a cluster over T tokens.
+__device__ __forceinline__ void cluster_slice(int T, int q, int& lo, int& hi) {
+    const int per = (T + kClusterCtas - 1) / kClusterCtas;
+    lo = min(T, q * per);
+    hi = min(T, lo + per);
+}
+
+// grid (kClusterCtas, R), cluster (kClusterCtas, 1, 1).
 __global__ void __launch_bounds__(kLayoutThreads)
     get_dispatch_layout_kernel(const int64_t* __restrict__ topk_idx, int R, int T, int K, int E, int EL,
                                int32_t* __restrict__ tpr, int32_t* __restrict__ tprdma,
@@ -67,7 +77,9 @@ __global__ void __launch_bounds__(kLayoutThreads)
     __shared__ int32_t s_rank[kMaxRanks];
     __shared__ int32_t s_node[kMaxRanks / 8];
 
-    const int s = blockIdx.x;
+    cg::cluster_group cluster = cg::this_cluster();
+    const int q = static_cast<int>(cluster.block_rank());
+    const int s = blockIdx.y;
     const int tid = threadIdx.x;
     const int lane = lane_id();
     const int NN = (R + 7) / 8;
@@ -75,15 +87,16 @@ __global__ void __launch_bounds__(kLayoutThreads)
     if (tid < kMaxRanks) s_rank[tid] = 0;
     if (tid < kMaxRanks / 8) s_node[tid] = 0;
 
+    int lo, hi;
+    cluster_slice(T, q, lo, hi);
     const int64_t* idx_s = topk_idx + static_cast<int64_t>(s) * T * K;
     uint8_t* itr_s = itr + static_cast<int64_t>(s) * T * R;
 
-    for (int round = 0; round < T; round += kLayoutRound) {
-        const int len = min(kLayoutRound, T - round);
+    for (int round = lo; round < hi; round += kLayoutRound) {
+        const int len = min(kLayoutRound, hi - round);
         for (int i = tid; i < len; i += kLayoutThreads) s_mask[i] = 0;
         __syncthreads();
-
-        // Phase A: flat walk over this round's top-k entries (coalesced 8-byte loads).
+        // Flat walk over this round's top-k entries (coalesced 8-byte loads, several in flight).
         const int64_t e_begin = static_cast<int64_t>(round) * K;
         const int64_t e_end = static_cast<int64_t>(round + len) * K;
         for (int64_t i0 = e_begin + tid; i0 < e_end; i0 += kLayoutUnroll * kLayoutThreads) {
@@ -107,8 +120,7 @@ __global__ void __launch_bounds__(kLayoutThreads)
             }
         }
         __syncthreads();
-
-        // Phase B: per token, the mask row and the per-rank / per-node counts.
+        // Per token: the mask row and the per-rank / per-node counts.
         for (int tl0 = 0; tl0 < len; tl0 += kLayoutThreads) {
             const int tl = tl0 + tid;
             const uint32_t m = tl < len ? s_mask[tl] : 0u;
@@ -125,14 +137,29 @@ __global__ void __launch_bounds__(kLayoutThreads)
         __syncthreads();
     }
 
-    for (int i = tid; i < E; i += kLayoutThreads) tpe[static_cast<int64_t>(s) * E + i] = s_expert[i];
-    if (tid < R) tpr[s * R + tid] = s_rank[tid];
-    if (tprdma != nullptr && tid < NN) tprdma[s * NN + tid] = s_node[tid];
+    // Sum the cluster's partial counts: CTA q writes the entries i with i % kClusterCtas == q.
+    cluster.sync();
+    for (int e = q + kClusterCtas * tid; e < E; e += kClusterCtas * kLayoutThreads) {
+        int32_t sum = 0;
+        for (int p = 0; p < kClusterCtas; ++p) sum += cluster.map_shared_rank(s_expert, p)[e];
+        tpe[static_cast<int64_t>(s) * E + e] = sum;
+    }
+    if (q == 0 && tid < R) {
+        int32_t sum = 0;
+        for (int p = 0; p < kClusterCtas; ++p) sum += cluster.map_shared_rank(s_rank, p)[tid];
+        tpr[s * R + tid] = sum;
+    }
+    if (q == 1 && tprdma != nullptr && tid < NN) {
+        int32_t sum = 0;
+        for (int p = 0; p < kClusterCtas; ++p) sum += cluster.map_shared_rank(s_node, p)[tid];
+        tprdma[s * NN + tid] = sum;
+    }
+    cluster.sync();  // keep every CTA's shared memory alive until the sums are read
 }
 
-// One CTA per source rank s (blockIdx.x < R): block-local scan of the R hit
-// columns over the tokens of s.  blockIdx.x == R: rank_prefix_matrix, num_recv
-// and the aligned per-expert receive counts.
+// grid (kClusterCtas, R + 1), cluster (kClusterCtas, 1, 1).  Cluster s < R: the
+// rows of source s.  Cluster R: rank_prefix_matrix, num_recv and the aligned
+// per-expert receive counts.
 __global__ void __launch_bounds__(kNotifyThreads)
     dispatch_notify_kernel(int R, int T, int E, int C, int A, int64_t cap, const int32_t* __restrict__ tpr,
                            const uint8_t* __restrict__ itr, const int32_t* __restrict__ tpe,
@@ -140,11 +167,23 @@ __global__ void __launch_bounds__(kNotifyThreads)
                            int32_t* __restrict__ recv_channel_prefix, int32_t* __restrict__ num_recv,
                            int32_t* __restrict__ send_head, int32_t* __restrict__ recv_src_idx,
                            int32_t* __restrict__ num_recv_per_expert, int32_t* status) {
+    __shared__ int32_t s_cnt[kMaxRanks];                 // hits of this CTA's slice, per rank
+    __shared__ int32_t s_base[kMaxRanks];                // rows taken by earlier sources
+    __shared__ int32_t s_before[kMaxRanks];              // hits of this source before the current round
+    __shared__ int32_t s_warp[kMaxRanks][kNotifyWarps];  // per-warp counts -> exclusive prefixes
+    __shared__ int32_t s_total[kMaxRanks];               // hits of the current round
+    static_assert(kNotifyWarps == kWarpSize, "the column scan gives one lane per warp");
+
+    cg::cluster_group cluster = cg::this_cluster();
+    const int q = static_cast<int>(cluster.block_rank());
+    const int s = blockIdx.y;
     const int tid = threadIdx.x;
-    const int s = blockIdx.x;
+    const int lane = lane_id();
+    const int warp = tid / kWarpSize;
 
     if (s == R) {
-        for (int r = tid; r < R; r += kNotifyThreads) {
+        const int per = kNotifyThreads * kClusterCtas;
+        for (int r = q * kNotifyThreads + tid; r < R; r += per) {
             int32_t acc = 0;
             for (int sp = 0; sp < R; ++sp) {
                 acc += __ldg(tpr + sp * R + r);
@@ -153,7 +192,7 @@ __global__ void __launch_bounds__(kNotifyThreads)
             num_recv[r] = acc;
             if (acc > cap) report(status, EP_ERR_CAPACITY);
         }
-        for (int e = tid; e < E; e += kNotifyThreads) {
+        for (int e = q * kNotifyThreads + tid; e < E; e += per) {
             int64_t sum = 0;
             for (int sp = 0; sp < R; ++sp) sum += __ldg(tpe + static_cast<int64_t>(sp) * E + e);
             num_recv_per_expert[e] = static_cast<int32_t>(((sum + A - 1) / A) * A);
@@ -161,98 +200,107 @@ __global__ void __launch_bounds__(kNotifyThreads)
         return;
     }
 
-    __shared__ int32_t s_base[kMaxRanks];  // rows of rank r taken by sources < s
-    __shared__ int32_t s_run[kMaxRanks];   // hits of (s -> r) in earlier rounds
-    __shared__ int32_t s_cnt[kMaxRanks][kNotifyTPT * kNotifyWarps + 1];
-
-    const int lane = lane_id();
-    const int warp = tid / kWarpSize;
-    if (tid < R) {
-        int32_t acc = 0;
-        for (int sp = 0; sp < s; ++sp) acc += __ldg(tpr + sp * R + tid);
-        s_base[tid] = acc;
-        s_run[tid] = 0;
-    }
-    const int chunk = max(1, (T + C - 1) / C);
+    int lo, hi;
+    cluster_slice(T, q, lo, hi);
     const uint8_t* itr_s = itr + static_cast<int64_t>(s) * T * R;
     int32_t* head_s = send_head + static_cast<int64_t>(s) * T * R;
+    if (tid < kMaxRanks) s_cnt[tid] = 0;
     __syncthreads();
 
-    for (int round = 0; round < T; round += kNotifyRound) {
-        uint32_t mask[kNotifyTPT];
-#pragma unroll
-        for (int j = 0; j < kNotifyTPT; ++j) {
-            const int t = round + j * kNotifyThreads + tid;
-            mask[j] = t < T ? load_rank_mask(itr_s + static_cast<int64_t>(t) * R, R) : 0u;
+    // Pass 1: hits of this slice per destination rank.
+    for (int t0 = lo; t0 < hi; t0 += kNotifyThreads) {
+        const int t = t0 + tid;
+        const uint32_t m = t < hi ? load_rank_mask(itr_s + static_cast<int64_t>(t) * R, R) : 0u;
+        for (int r = 0; r < R; ++r) {
+            const unsigned b = __ballot_sync(kFullMask, (m >> r) & 1u);
+            if (lane == 0 && b) atomicAdd(&s_cnt[r], __popc(b));
         }
-        // Per-warp hit counts of every (slot j, warp) group of 32 consecutive tokens.
-#pragma unroll
-        for (int j = 0; j < kNotifyTPT; ++j)
-            for (int r = 0; r < R; ++r) {
-                const unsigned b = __ballot_sync(kFullMask, (mask[j] >> r) & 1u);
-                if (lane == 0) s_cnt[r][j * kNotifyWarps + warp] = __popc(b);
-            }
+    }
+    cluster.sync();
+    // Rows before this slice: earlier sources (from the counts) and earlier slices of this source.
+    if (tid < R) {
+        int32_t base = 0;
+        for (int sp = 0; sp < s; ++sp) base += __ldg(tpr + sp * R + tid);
+        int32_t before = 0;
+        for (int p = 0; p < q; ++p) before += cluster.map_shared_rank(s_cnt, p)[tid];
+        s_base[tid] = base;
+        s_before[tid] = before;
+        if (q == kClusterCtas - 1) {
+            // this slice ends the source: the per-source total must match the counts
+            const int32_t total = before + s_cnt[tid];
+            if (total != __ldg(tpr + s * R + tid)) report(status, EP_ERR_INCONSISTENT);
+        }
+    }
+    cluster.sync();  // peers are done reading this CTA's s_cnt
+
+    const int chunk = max(1, (T + C - 1) / C);
+    const unsigned lt = lanemask_lt();
+    for (int t0 = lo; t0 < hi; t0 += kNotifyThreads) {
+        const int t = t0 + tid;
+        const bool live = t < hi;
+        const uint32_t m = live ? load_rank_mask(itr_s + static_cast<int64_t>(t) * R, R) : 0u;
+        for (int r = 0; r < R; ++r) {
+            const unsigned b = __ballot_sync(kFullMask, (m >> r) & 1u);
+            if (lane == 0) s_warp[r][warp] = __popc(b);
+        }
         __syncthreads();
-        // Warp r turns column r into exclusive prefixes (plus the earlier rounds' hits).
-        if (warp < R) {
-            constexpr int kPer = kNotifyTPT * kNotifyWarps / kWarpSize;
-            int32_t v[kPer];
-            int32_t local = 0;
-#pragma unroll
-            for (int i = 0; i < kPer; ++i) {
-                v[i] = s_cnt[warp][lane * kPer + i];
-                local += v[i];
-            }
-            int32_t incl = local;
+        if (warp < R) {  // warp r: exclusive prefix over the warps of this round, column r
+            const int32_t v = s_warp[warp][lane];
+            int32_t incl = v;
 #pragma unroll
             for (int off = 1; off < kWarpSize; off <<= 1) {
                 const int32_t o = __shfl_up_sync(kFullMask, incl, off);
                 if (lane >= off) incl += o;
             }
-            const int32_t before = s_run[warp];
-            int32_t run = before + incl - local;
-#pragma unroll
-            for (int i = 0; i < kPer; ++i) {
-                s_cnt[warp][lane * kPer + i] = run;
-                run += v[i];
-            }
-            __syncwarp();
-            if (lane == kWarpSize - 1) s_run[warp] = before + incl;
+            s_warp[warp][lane] = s_before[warp] + incl - v;
+            if (lane == kWarpSize - 1) s_total[warp] = incl;
         }
         __syncthreads();
-        // Rows, recv_src_idx and the channel boundaries.
-        const unsigned lt = lanemask_lt();
+        int32_t rows[kMaxRanks];
 #pragma unroll
-        for (int j = 0; j < kNotifyTPT; ++j) {
-            const int t = round + j * kNotifyThreads + tid;
-            const bool live = t < T;
-            const bool boundary = live && (t % chunk) == 0;
-            const int c = t / chunk;
-            for (int r = 0; r < R; ++r) {
-                const bool bit = (mask[j] >> r) & 1u;
-                const unsigned b = __ballot_sync(kFullMask, bit);
-                const int32_t excl = s_cnt[r][j * kNotifyWarps + warp] + __popc(b & lt);
-                if (!live) continue;
-                int32_t row = -1;
-                if (bit) {
-                    row = s_base[r] + excl;
-                    if (row < cap) recv_src_idx[static_cast<int64_t>(r) * cap + row] = t;
-                }
-                head_s[static_cast<int64_t>(t) * R + r] = row;
-                if (boundary) {
-                    recv_channel_prefix[(static_cast<int64_t>(r) * R + s) * C + c] = s_base[r] + excl;
-                    if (c > 0) channel_prefix[(static_cast<int64_t>(s) * R + r) * C + c - 1] = excl;
-                }
+        for (int r = 0; r < kMaxRanks; ++r) {
+            if (r >= R) break;
+            const bool bit = (m >> r) & 1u;
+            const unsigned b = __ballot_sync(kFullMask, bit);
+            const int32_t excl = s_warp[r][warp] + __popc(b & lt);  // hits of (s -> r) before t
+            rows[r] = bit ? s_base[r] + excl : -1;
+            if (live && (t % chunk) == 0) {
+                const int c = t / chunk;
+                recv_channel_prefix[(static_cast<int64_t>(r) * R + s) * C + c] = s_base[r] + excl;
+                if (c > 0) channel_prefix[(static_cast<int64_t>(s) * R + r) * C + c - 1] = excl;
             }
         }
+        if (live) {
+            int32_t* dst = head_s + static_cast<int64_t>(t) * R;
+            if ((R & 3) == 0) {
+#pragma unroll
+                for (int r = 0; r < kMaxRanks; r += 4) {
+                    if (r >= R) break;
+                    reinterpret_cast<int4*>(dst)[r / 4] = make_int4(rows[r], rows[r + 1], rows[r + 2], rows[r + 3]);
+                }
+            } else {
+#pragma unroll
+                for (int r = 0; r < kMaxRanks; ++r) {
+                    if (r >= R) break;
+                    dst[r] = rows[r];
+                }
+            }
+#pragma unroll
+            for (int r = 0; r < kMaxRanks; ++r) {
+                if (r >= R) break;
+                if (rows[r] >= 0 && rows[r] < cap) recv_src_idx[static_cast<int64_t>(r) * cap + rows[r]] = t;
+            }
+        }
+        // the next round starts after this round's hits
+        __syncthreads();
+        if (tid < R) s_before[tid] += s_total[tid];
         __syncthreads();
     }
 
-    // Channels that end at T (or hold no token) and the consistency check.
-    if (tid < R) {
+    // Channels that end at T (or hold no token): written by the last slice of the source.
+    if (q == kClusterCtas - 1 && tid < R) {
         const int r = tid;
-        const int32_t total = s_run[r];
-        if (total != __ldg(tpr + s * R + r)) report(status, EP_ERR_INCONSISTENT);
+        const int32_t total = __ldg(tpr + s * R + r);
         for (int c = 0; c < C; ++c) {
             const int64_t start = min(static_cast<int64_t>(T), static_cast<int64_t>(c) * chunk);
             const int64_t end = min(static_cast<int64_t>(T), static_cast<int64_t>(c + 1) * chunk);
@@ -267,10 +315,20 @@ __global__ void __launch_bounds__(kNotifyThreads)
 cudaError_t launch_get_dispatch_layout(const int64_t* topk_idx, int R, int T, int K, int E, int32_t* tpr,
                                        int32_t* tprdma, int32_t* tpe, uint8_t* itr, int32_t* status,
                                        cudaStream_t stream) {
-    const size_t smem = sizeof(int32_t) * static_cast<size_t>(E);
-    get_dispatch_layout_kernel<<<R, kLayoutThreads, smem, stream>>>(topk_idx, R, T, K, E, E / R, tpr, tprdma,
-                                                                     tpe, itr, status);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(kClusterCtas, R, 1);
+    cfg.blockDim = dim3(kLayoutThreads, 1, 1);
+    cfg.dynamicSmemBytes = sizeof(int32_t) * static_cast<size_t>(E);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = kClusterCtas;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, get_dispatch_layout_kernel, topk_idx, R, T, K, E, E / R, tpr, tprdma, tpe, itr,
+                              status);
 }
 
 cudaError_t launch_dispatch_notify(int R, int T, int E, int C, int A, int64_t cap, const int32_t* tpr,
@@ -278,11 +336,21 @@ cudaError_t launch_dispatch_notify(int R, int T, int E, int C, int A, int64_t ca
                                    int32_t* channel_prefix, int32_t* recv_channel_prefix, int32_t* num_recv,
                                    int32_t* send_head, int32_t* recv_src_idx, int32_t* num_recv_per_expert,
                                    int32_t* status, cudaStream_t stream) {
-    dispatch_notify_kernel<<<R + 1, kNotifyThreads, 0, stream>>>(R, T, E, C, A, cap, tpr, itr, tpe, rank_prefix,
-                                                                 channel_prefix, recv_channel_prefix, num_recv,
-                                                                 send_head, recv_src_idx, num_recv_per_expert,
-                                                                 status);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(kClusterCtas, R + 1, 1);
+    cfg.blockDim = dim3(kNotifyThreads, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = kClusterCtas;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, dispatch_notify_kernel, R, T, E, C, A, cap, tpr, itr, tpe, rank_prefix,
+                              channel_prefix, recv_channel_prefix, num_recv, send_head, recv_src_idx,
+                              num_recv_per_expert, status);
 }
 
 }  // namespace ep
