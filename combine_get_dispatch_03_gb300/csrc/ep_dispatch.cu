@@ -263,6 +263,36 @@ __global__ void dispatch_bulk_kernel(int R, int T, int H, int K, int EL, int64_t
             __syncthreads();
             payload = qo;
         }
+        // Top-k metadata and FP8 scales of every destination: warp 1 when the CTA has
+        // several warps (it then runs beside warp 0's stores and refill), else warp 0.
+        const int meta_warp = blockDim.x > kWarpSize ? 1 : 0;
+        if (tid / kWarpSize == meta_warp) {
+            int32_t row = lane < R ? s_row[s * 32 + lane] : -1;
+            if (row >= cap) row = -1;
+            const unsigned dst = __ballot_sync(kFullMask, row >= 0);
+            const int64_t g = first + j * stride;
+            int e = -1;
+            float w = 0.0f;
+            if (lane < K && topk_idx != nullptr) {
+                e = static_cast<int>(s_idx[s * 32 + lane]);
+                if (topk_weights != nullptr) w = s_w[s * 32 + lane];
+            }
+            for (unsigned m = dst; m; m &= m - 1) {
+                const int r = __ffs(m) - 1;
+                const int64_t drow = static_cast<int64_t>(r) * cap + s_row[s * 32 + r];
+                if ((recv_topk_idx != nullptr || recv_topk_weights != nullptr) && lane < K) {
+                    const bool mine = e >= 0 && e / EL == r;
+                    if (recv_topk_idx != nullptr) recv_topk_idx[drow * K + lane] = mine ? e % EL : -1;
+                    if (recv_topk_weights != nullptr) recv_topk_weights[drow * K + lane] = mine ? w : 0.0f;
+                }
+                if (kMode == kModeFp8In)
+                    for (int i = lane; i < G; i += kWarpSize) recv_x_scales[drow * G + i] = __ldg(x_scales + g * G + i);
+                if (kMode == kModeCastFp8 && !scales_bulk) {
+                    const float* so = reinterpret_cast<const float*>(payload + H);
+                    for (int i = lane; i < G; i += kWarpSize) recv_x_scales[drow * G + i] = so[i];
+                }
+            }
+        }
         if (warp0) {
             int32_t row = lane < R ? s_row[s * 32 + lane] : -1;
             if (row >= cap) row = -1;
@@ -276,24 +306,6 @@ __global__ void dispatch_bulk_kernel(int R, int T, int H, int K, int EL, int64_t
                         bulk_store(recv_x_scales + drow * G, payload + H, 4 * G);
                 }
                 bulk_commit();
-            }
-            const int64_t g = first + j * stride;
-            for (unsigned m = dst; m; m &= m - 1) {
-                const int r = __ffs(m) - 1;
-                const int64_t drow = static_cast<int64_t>(r) * cap + s_row[s * 32 + r];
-                if ((recv_topk_idx != nullptr || recv_topk_weights != nullptr) && lane < K) {
-                    const int64_t e = s_idx[s * 32 + lane];
-                    const bool mine = e >= 0 && static_cast<int>(e) / EL == r;
-                    if (recv_topk_idx != nullptr) recv_topk_idx[drow * K + lane] = mine ? e % EL : -1;
-                    if (recv_topk_weights != nullptr)
-                        recv_topk_weights[drow * K + lane] = (mine && topk_weights != nullptr) ? s_w[s * 32 + lane] : 0.0f;
-                }
-                if (kMode == kModeFp8In)
-                    for (int i = lane; i < G; i += kWarpSize) recv_x_scales[drow * G + i] = __ldg(x_scales + g * G + i);
-                if (kMode == kModeCastFp8 && !scales_bulk) {
-                    const float* so = reinterpret_cast<const float*>(payload + H);
-                    for (int i = lane; i < G; i += kWarpSize) recv_x_scales[drow * G + i] = so[i];
-                }
             }
             // Refill the stage that token j-1 used once its stores have read it.
             if (j + S - 1 < n_local) {

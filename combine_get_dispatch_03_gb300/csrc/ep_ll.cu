@@ -74,22 +74,34 @@ __global__ void __launch_bounds__(kLLCountThreads)
     for (int e = tid; e < E; e += kLLCountThreads) cnt[static_cast<int64_t>(s) * E + e] = s_run[e];
 }
 
+// One warp per expert e: lane s holds the count of source s, a warp scan gives
+// each source block's begin.  R <= 32.
 __global__ void ll_finish_kernel(int R, int maxT, int E, const int32_t* __restrict__ cnt,
                                  int32_t* __restrict__ packed_recv_count, int64_t* __restrict__ layout_range,
                                  int32_t* __restrict__ stats, int32_t* status) {
     const int64_t slots = static_cast<int64_t>(R) * maxT;
-    for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < E; e += gridDim.x * blockDim.x) {
-        int64_t begin = 0;
-        for (int s = 0; s < R; ++s) {
-            const int32_t c = __ldg(cnt + static_cast<int64_t>(s) * E + e);
-            layout_range[static_cast<int64_t>(e) * R + s] =
-                static_cast<int64_t>((static_cast<uint64_t>(c) << 32) | static_cast<uint32_t>(begin));
-            begin += c;
+    const int lane = lane_id();
+    const int warps = blockDim.x / kWarpSize;
+    for (int e = blockIdx.x * warps + threadIdx.x / kWarpSize; e < E; e += gridDim.x * warps) {
+        const int32_t c = lane < R ? __ldg(cnt + static_cast<int64_t>(lane) * E + e) : 0;
+        int32_t incl = c;
+#pragma unroll
+        for (int off = 1; off < kWarpSize; off <<= 1) {
+            const int32_t o = __shfl_up_sync(kFullMask, incl, off);
+            if (lane >= off) incl += o;
         }
-        if (begin > slots) report(status, EP_ERR_CAPACITY);
-        const int32_t n = static_cast<int32_t>(begin < slots ? begin : slots);
-        packed_recv_count[e] = n;
-        if (stats != nullptr) stats[e] += n;
+        const int32_t begin = incl - c;
+        if (lane < R)
+            layout_range[static_cast<int64_t>(e) * R + lane] =
+                static_cast<int64_t>((static_cast<uint64_t>(static_cast<uint32_t>(c)) << 32) |
+                                     static_cast<uint32_t>(begin));
+        const int32_t total = __shfl_sync(kFullMask, incl, kWarpSize - 1);
+        if (lane == 0) {
+            if (total > slots) report(status, EP_ERR_CAPACITY);
+            const int32_t n = static_cast<int32_t>(total < slots ? total : slots);
+            packed_recv_count[e] = n;
+            if (stats != nullptr) stats[e] += n;
+        }
     }
 }
 
@@ -329,8 +341,8 @@ cudaError_t launch_ll_dispatch(const LaunchPlan& plan, int R, int T, int maxT, i
                                                                       status);
     cudaError_t err = cudaGetLastError();
     if (err != cudaSuccess) return err;
-    const int fin_threads = 256;
-    ll_finish_kernel<<<(E + fin_threads - 1) / fin_threads, fin_threads, 0, stream>>>(
+    const int fin_warps = 8;
+    ll_finish_kernel<<<(E + fin_warps - 1) / fin_warps, fin_warps * kWarpSize, 0, stream>>>(
         R, maxT, E, cnt, packed_recv_count, layout_range, stats, status);
     err = cudaGetLastError();
     if (err != cudaSuccess) return err;
