@@ -92,7 +92,7 @@ def source_digest():
 
 def recorded_traffic(kernel):
     """DRAM bytes per launch from a committed ncu summary, if taken on the current kernel sources."""
-    path = os.path.join(ROOT, "profiles", "traffic.json")
+    path = os.path.join(ROOT, "profiles", "traffic_per_launch.txt")
     if not os.path.exists(path):
         return None
     with open(path) as f:
@@ -245,38 +245,41 @@ def run_ours(args):
     out = torch.empty((R, T, H), dtype=torch.bfloat16, device=dev)
     out_w = torch.empty((R, T, K), dtype=torch.float32, device=dev)
 
+    # The dispatch runs as its two parts, notify (the record) and the prepared data movement,
+    # so that the data kernel has its own pair of events.
     def step(idx_in, w_in, x_in, ev=None, base=0):
         if ev: ev.rec(base, stream)
         ep.ep_get_dispatch_layout(h, idx_in, **lay)
         if ev: ev.rec(base + 1, stream)
-        ep.ep_dispatch(h, x_in, topk_idx=idx_in, topk_weights=w_in,
-                       num_tokens_per_rank=lay["num_tokens_per_rank"], is_token_in_rank=lay["is_token_in_rank"],
-                       num_tokens_per_expert=lay["num_tokens_per_expert"], recv_x=recv_x, recv_topk_idx=recv_i,
-                       recv_topk_weights=recv_w, num_recv_tokens_per_expert=nrpe)
+        ep.ep_notify_dispatch(h, lay["num_tokens_per_rank"], lay["is_token_in_rank"], lay["num_tokens_per_expert"],
+                              num_recv_tokens_per_expert=nrpe)
         if ev: ev.rec(base + 2, stream)
-        ep.ep_combine(h, recv_x, topk_weights=recv_w, combined_x=out, combined_topk_weights=out_w)
+        ep.ep_dispatch(h, x_in, topk_idx=idx_in, topk_weights=w_in, recv_x=recv_x, recv_topk_idx=recv_i,
+                       recv_topk_weights=recv_w, prepared=True)
         if ev: ev.rec(base + 3, stream)
+        ep.ep_combine(h, recv_x, topk_weights=recv_w, combined_x=out, combined_topk_weights=out_w)
+        if ev: ev.rec(base + 4, stream)
 
     for _ in range(args.warmup):
         step(idx_d, w_d, x_d)
     torch.cuda.synchronize(dev)
     h.check()
 
-    ev = Events(4 * args.steps + 1)
+    ev = Events(5 * args.steps + 1)
     barrier(world)
     with ClockSampler(dev.index) as clocks:
         torch.cuda.synchronize(dev)
         t0 = time.perf_counter()
         for i in range(args.steps):
-            step(idx_d, w_d, x_d, ev, 4 * i)
-        ev.rec(4 * args.steps, stream)
+            step(idx_d, w_d, x_d, ev, 5 * i)
+        ev.rec(5 * args.steps, stream)
         torch.cuda.synchronize(dev)
         wall = time.perf_counter() - t0
     barrier(world)
     h.check()
-    step_ms = ev.ms(0, 4 * args.steps) / args.steps
-    op_ms = {name: statistics.mean(ev.ms(4 * i + j, 4 * i + j + 1) for i in range(args.steps))
-             for j, name in enumerate(("layout", "dispatch", "combine"))}
+    step_ms = ev.ms(0, 5 * args.steps) / args.steps
+    op_ms = {name: statistics.mean(ev.ms(5 * i + j, 5 * i + j + 1) for i in range(args.steps))
+             for j, name in enumerate(("layout", "notify", "dispatch", "combine"))}
 
     bm = normal_bytes(R, T, H, K, hits)
     payload = bm["dispatch"]["payload"] + bm["combine"]["payload"]
@@ -287,9 +290,9 @@ def run_ours(args):
 
     # dominant operation of the step and its roofline
     dom = max(("dispatch", "combine"), key=lambda k: op_ms[k])
-    dom_bytes = total(bm[dom]) + (total(bm["notify"]) if dom == "dispatch" else 0)
+    dom_bytes = total(bm[dom])
     achieved = dom_bytes / (op_ms[dom] / 1e3) / 1e9
-    kernel_name = "dispatch_notify_kernel + dispatch_kernel<0>" if dom == "dispatch" else "combine_kernel<false>"
+    kernel_name = "dispatch_bulk_kernel<0>" if dom == "dispatch" else "combine_kernel<false>"
     traffic = recorded_traffic(kernel_name)
 
     # end to end: pinned host inputs in, the step's result out, every step
@@ -349,8 +352,8 @@ def run_ours(args):
         "warmup": args.warmup, "ms_per_step": round(step_ms, 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded routing and N(0,1) bf16 tokens)",
         "config": {"workload": f"{HEADLINE}: R=8 T={T} H=7168 E=256 K=8 Gumbel routing A=128 C=12; step = "
-                               "get_dispatch_layout + dispatch (fresh record) + combine (received rows, "
-                               "top-k weight reduction)",
+                               "get_dispatch_layout + notify_dispatch + dispatch (bf16, top-k metadata) + "
+                               "combine (received rows, top-k weight reduction)",
                    "l2": "no flush; inputs larger than L2 (x 470 MB, receive buffer %.2f GB vs 129 MB L2)"
                          % (R * cap * H * 2 / 1e9),
                    "parallelism": "replicas" if world > 1 else "single GPU, R=8 virtual ranks"},
@@ -361,28 +364,31 @@ def run_ours(args):
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "traffic": traffic, "algorithmic_bytes": dom_bytes},
         "cpu_baseline": cpu, "clocks": clocks.summary(), "e2e": e2e,
-        "gpu_launches": 4 * args.steps, "wall_s_timed": round(wall, 3), "ops": ops,
+        "gpu_launches": 4 * args.steps,  # layout, notify, dispatch, combine "wall_s_timed": round(wall, 3), "ops": ops,
     }
     if rank == 0:
         print(json.dumps(result), flush=True)
 
 
-def timed(fn, reps, stream, warmup=3):
+def timed(fn, reps, stream, warmup=3, batches=5):
+    """Steady-state time of one call: `reps` calls queued back to back between two events
+    (host launch overhead hidden behind the GPU work), median over `batches` such runs."""
     for _ in range(warmup):
         fn()
     torch.cuda.synchronize()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     times = []
-    for _ in range(reps):
+    for _ in range(batches):
         a.record(stream)
-        fn()
+        for _ in range(reps):
+            fn()
         b.record(stream)
         b.synchronize()
-        times.append(a.elapsed_time(b))
+        times.append(a.elapsed_time(b) / reps)
     return statistics.median(times)
 
 
-def measure_other_ops(ep, dev, peak, reps=20):
+def measure_other_ops(ep, dev, peak, reps=10):
     """Per-op times of the other workloads (median of reps, after warm-up)."""
     stream = torch.cuda.current_stream(dev)
     res = {}
@@ -426,7 +432,7 @@ def measure_other_ops(ep, dev, peak, reps=20):
     d = ep.ep_dispatch(h, st["x_d"], topk_idx=st["idx_d"], topk_weights=st["w_d"],
                        num_tokens_per_rank=lay["num_tokens_per_rank"], is_token_in_rank=lay["is_token_in_rank"],
                        num_tokens_per_expert=lay["num_tokens_per_expert"])
-    ms_disp = timed(lambda: ep.ep_dispatch(h, st["x_d"], cached=True, recv_x=d["recv_x"]), 5, stream)
+    ms_disp = timed(lambda: ep.ep_dispatch(h, st["x_d"], cached=True, recv_x=d["recv_x"]), reps, stream)
     b0, b1 = W.biases(shape, device=dev)
     ys = [W.expert_outputs(shape, shape.R * st["cap"], i, device=dev).view(shape.R, st["cap"], shape.H)
           for i in range(2)]
@@ -492,7 +498,7 @@ def measure_other_ops(ep, dev, peak, reps=20):
     b = normal_bytes(shape.R, shape.T, shape.H, shape.K, st["hits"])
     step_b = {"payload": b["dispatch"]["payload"] + b["combine"]["payload"],
               "meta": sum(v["meta"] for v in b.values())}
-    report("normal_small.step", ms, step_b, {"note": "L2-resident, includes torch output allocation"})
+    report("normal_small.step", ms, step_b, {"note": "L2-resident; outputs allocated by torch in each call"})
     h.destroy()
     return res
 

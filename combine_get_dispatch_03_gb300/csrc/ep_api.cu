@@ -33,7 +33,8 @@ struct ep_handle {
     int32_t* send_head = nullptr;            // [R][maxT][R]
     int32_t* ll_slot = nullptr;              // [R][maxT][K]
     int32_t* ll_cnt = nullptr;               // [R][E]
-    int normal_tokens = -1;                  // T of the last fresh dispatch, -1 = none
+    int normal_tokens = -1;                  // T of the current dispatch record, -1 = none
+    bool prepared = false;                   // record built by ep_notify_dispatch, not yet used
     int ll_tokens = -1;                      // T of the last LL dispatch, -1 = none
 };
 
@@ -323,7 +324,21 @@ ep_status ep_dispatch(ep_handle* h, int32_t num_tokens, const void* x, ep_dtype 
     EP_CHECK_ARG(num_tokens == 0 || (x != nullptr && aligned16(x)), "x must be a 16-byte aligned device pointer");
     EP_CHECK_ARG(recv_x != nullptr && aligned16(recv_x), "recv_x must be a 16-byte aligned device pointer");
 
-    if (cached) {
+    EP_CHECK_ARG(cached == EP_DISPATCH_FRESH || cached == EP_DISPATCH_CACHED || cached == EP_DISPATCH_PREPARED,
+                 "unknown dispatch mode %d", cached);
+    if (cached == EP_DISPATCH_PREPARED) {
+        EP_CHECK_ARG(num_tokens_per_rank == nullptr && is_token_in_rank == nullptr && num_tokens_per_expert == nullptr &&
+                         num_recv_tokens_per_expert == nullptr,
+                     "prepared dispatch takes no layout arguments (ep_notify_dispatch had them)");
+        if (!h->prepared || h->normal_tokens != num_tokens)
+            return fail(EP_ERR_STATE, "prepared dispatch without an ep_notify_dispatch for %d tokens", num_tokens);
+        EP_CHECK_ARG((recv_topk_idx == nullptr && recv_topk_weights == nullptr) || topk_idx != nullptr,
+                     "recv_topk_* outputs need topk_idx");
+        EP_CHECK_ARG(recv_topk_weights == nullptr || topk_weights != nullptr, "recv_topk_weights needs topk_weights");
+        EP_CHECK_ARG(aligned8(topk_idx) && aligned4(topk_weights) && aligned8(recv_topk_idx) &&
+                         aligned4(recv_topk_weights),
+                     "misaligned top-k pointer");
+    } else if (cached == EP_DISPATCH_CACHED) {
         EP_CHECK_ARG(topk_idx == nullptr && topk_weights == nullptr && num_tokens_per_rank == nullptr &&
                          is_token_in_rank == nullptr && num_tokens_per_expert == nullptr &&
                          recv_topk_idx == nullptr && recv_topk_weights == nullptr &&
@@ -349,7 +364,7 @@ ep_status ep_dispatch(ep_handle* h, int32_t num_tokens, const void* x, ep_dtype 
 
     DeviceGuard guard(h->device);
     cudaError_t err;
-    if (!cached) {
+    if (cached == EP_DISPATCH_FRESH) {
         err = ep::launch_dispatch_notify(c.num_ranks, num_tokens, c.num_experts, c.num_channels, c.expert_alignment,
                                          c.recv_capacity, num_tokens_per_rank, is_token_in_rank,
                                          num_tokens_per_expert, h->rank_prefix, h->channel_prefix,
@@ -358,11 +373,38 @@ ep_status ep_dispatch(ep_handle* h, int32_t num_tokens, const void* x, ep_dtype 
         if (err != cudaSuccess) return cuda_fail(err, "dispatch_notify launch");
         h->normal_tokens = num_tokens;
     }
+    h->prepared = false;
+    const bool with_topk = cached != EP_DISPATCH_CACHED;
     err = ep::launch_dispatch(h->plan, mode, c.num_ranks, num_tokens, c.hidden, c.num_topk,
                               c.num_experts / c.num_ranks, c.recv_capacity, x, x_scales,
-                              cached ? nullptr : topk_idx, cached ? nullptr : topk_weights, h->send_head, recv_x,
-                              recv_x_scales, recv_topk_idx, recv_topk_weights, h->status, stream);
+                              with_topk ? topk_idx : nullptr, with_topk ? topk_weights : nullptr, h->send_head,
+                              recv_x, recv_x_scales, recv_topk_idx, recv_topk_weights, h->status, stream);
     if (err != cudaSuccess) return cuda_fail(err, "dispatch launch");
+    return EP_OK;
+}
+
+ep_status ep_notify_dispatch(ep_handle* h, int32_t num_tokens, const int32_t* num_tokens_per_rank,
+                             const uint8_t* is_token_in_rank, const int32_t* num_tokens_per_expert,
+                             int32_t* num_recv_tokens_per_expert, ep_stream_t stream) {
+    if (h == nullptr) return fail(EP_ERR_INVALID_ARG, "handle is NULL");
+    ep_status st = check_tokens(h, num_tokens);
+    if (st != EP_OK) return st;
+    const ep_config& c = h->cfg;
+    EP_CHECK_ARG(c.recv_capacity > 0, "handle was created with recv_capacity 0 (normal mode disabled)");
+    EP_CHECK_ARG(num_tokens_per_rank && is_token_in_rank && num_tokens_per_expert && num_recv_tokens_per_expert,
+                 "the layout inputs and num_recv_tokens_per_expert are required");
+    EP_CHECK_ARG(aligned4(num_tokens_per_rank) && aligned16(is_token_in_rank) && aligned4(num_tokens_per_expert) &&
+                     aligned4(num_recv_tokens_per_expert),
+                 "misaligned layout pointer");
+    DeviceGuard guard(h->device);
+    cudaError_t err = ep::launch_dispatch_notify(
+        c.num_ranks, num_tokens, c.num_experts, c.num_channels, c.expert_alignment, c.recv_capacity,
+        num_tokens_per_rank, is_token_in_rank, num_tokens_per_expert, h->rank_prefix, h->channel_prefix,
+        h->recv_channel_prefix, h->num_recv, h->send_head, h->recv_src_idx, num_recv_tokens_per_expert, h->status,
+        stream);
+    if (err != cudaSuccess) return cuda_fail(err, "dispatch_notify launch");
+    h->normal_tokens = num_tokens;
+    h->prepared = true;
     return EP_OK;
 }
 

@@ -45,6 +45,7 @@ __global__ void __launch_bounds__(kDispatchThreads)
                     const float* __restrict__ topk_weights, const int32_t* __restrict__ send_head,
                     void* __restrict__ recv_x, float* __restrict__ recv_x_scales,
                     int64_t* __restrict__ recv_topk_idx, float* __restrict__ recv_topk_weights) {
+    pdl_enter();
     constexpr int kWarps = kDispatchThreads / kWarpSize;
     const int lane = lane_id();
     const int64_t n_tokens = static_cast<int64_t>(R) * T;
@@ -185,6 +186,7 @@ __global__ void dispatch_bulk_kernel(int R, int T, int H, int K, int EL, int64_t
                                      const int32_t* __restrict__ send_head, uint8_t* __restrict__ recv_x,
                                      float* __restrict__ recv_x_scales, int64_t* __restrict__ recv_topk_idx,
                                      float* __restrict__ recv_topk_weights, int32_t* status) {
+    pdl_enter();
     extern __shared__ __align__(128) uint8_t smem[];
     const int S = stages;
     const int tid = threadIdx.x;
@@ -329,6 +331,7 @@ __global__ void __launch_bounds__(kCombineThreads)
     combine_kernel(int R, int T, int H, int K, int64_t cap, const int32_t* __restrict__ send_head,
                    const int4* __restrict__ y, const float* __restrict__ recv_w, const int4* __restrict__ bias0,
                    const int4* __restrict__ bias1, void* __restrict__ out, float* __restrict__ cw) {
+    pdl_enter();
     constexpr int kWarps = kCombineThreads / kWarpSize;
     const int lane = lane_id();
     const int64_t n_tokens = static_cast<int64_t>(R) * T;
@@ -473,6 +476,7 @@ cudaError_t launch_dispatch(const LaunchPlan& plan, int mode, int R, int T, int 
                             const float* topk_weights, const int32_t* send_head, void* recv_x,
                             float* recv_x_scales, int64_t* recv_topk_idx, float* recv_topk_weights,
                             int32_t* status, cudaStream_t stream) {
+    cudaError_t err = cudaSuccess;
     const int64_t n_tokens = static_cast<int64_t>(R) * T;
     if (n_tokens == 0) return cudaSuccess;
     if (kUseBulkDispatch && plan.bulk_stages[mode] > 0) {
@@ -486,48 +490,55 @@ cudaError_t launch_dispatch(const LaunchPlan& plan, int mode, int R, int T, int 
         uint8_t* rb = static_cast<uint8_t*>(recv_x);
         switch (mode) {
             case kModeBf16:
-                dispatch_bulk_kernel<kModeBf16><<<grid, threads, smem, stream>>>(
+                err = launch_kernel(dispatch_bulk_kernel<kModeBf16>, dim3(grid), dim3(threads), smem, stream, 1,
+            
                     R, T, H, K, EL, cap, S, scales_bulk, xb, x_scales, topk_idx, topk_weights, send_head, rb,
                     recv_x_scales, recv_topk_idx, recv_topk_weights, status);
                 break;
             case kModeCastFp8:
-                dispatch_bulk_kernel<kModeCastFp8><<<grid, threads, smem, stream>>>(
+                err = launch_kernel(dispatch_bulk_kernel<kModeCastFp8>, dim3(grid), dim3(threads), smem, stream, 1,
+            
                     R, T, H, K, EL, cap, S, scales_bulk, xb, x_scales, topk_idx, topk_weights, send_head, rb,
                     recv_x_scales, recv_topk_idx, recv_topk_weights, status);
                 break;
             default:
-                dispatch_bulk_kernel<kModeFp8In><<<grid, threads, smem, stream>>>(
+                err = launch_kernel(dispatch_bulk_kernel<kModeFp8In>, dim3(grid), dim3(threads), smem, stream, 1,
+            
                     R, T, H, K, EL, cap, S, scales_bulk, xb, x_scales, topk_idx, topk_weights, send_head, rb,
                     recv_x_scales, recv_topk_idx, recv_topk_weights, status);
                 break;
         }
-        return cudaGetLastError();
+        return err;
     }
     const int grid = clamp_grid(plan.dispatch_blocks[mode], n_tokens, kDispatchThreads / kWarpSize);
     switch (mode) {
         case kModeBf16:
-            dispatch_kernel<kModeBf16><<<grid, kDispatchThreads, 0, stream>>>(
+            err = launch_kernel(dispatch_kernel<kModeBf16>, dim3(grid), dim3(kDispatchThreads), 0, stream, 1,
+            
                 R, T, H, K, EL, cap, x, x_scales, topk_idx, topk_weights, send_head, recv_x, recv_x_scales,
                 recv_topk_idx, recv_topk_weights);
             break;
         case kModeCastFp8:
-            dispatch_kernel<kModeCastFp8><<<grid, kDispatchThreads, 0, stream>>>(
+            err = launch_kernel(dispatch_kernel<kModeCastFp8>, dim3(grid), dim3(kDispatchThreads), 0, stream, 1,
+            
                 R, T, H, K, EL, cap, x, x_scales, topk_idx, topk_weights, send_head, recv_x, recv_x_scales,
                 recv_topk_idx, recv_topk_weights);
             break;
         default:
-            dispatch_kernel<kModeFp8In><<<grid, kDispatchThreads, 0, stream>>>(
+            err = launch_kernel(dispatch_kernel<kModeFp8In>, dim3(grid), dim3(kDispatchThreads), 0, stream, 1,
+            
                 R, T, H, K, EL, cap, x, x_scales, topk_idx, topk_weights, send_head, recv_x, recv_x_scales,
                 recv_topk_idx, recv_topk_weights);
             break;
     }
-    return cudaGetLastError();
+    return err;
 }
 
 cudaError_t launch_combine(const LaunchPlan& plan, bool out_fp32, int R, int T, int H, int K, int64_t cap,
                            const int32_t* send_head, const void* y, const float* recv_topk_weights,
                            const void* bias0, const void* bias1, void* out, float* combined_topk_weights,
                            cudaStream_t stream) {
+    cudaError_t err = cudaSuccess;
     const int64_t n_tokens = static_cast<int64_t>(R) * T;
     if (n_tokens == 0) return cudaSuccess;
     const int grid = clamp_grid(plan.combine_blocks[out_fp32 ? 1 : 0], n_tokens, kCombineThreads / kWarpSize);
@@ -535,13 +546,15 @@ cudaError_t launch_combine(const LaunchPlan& plan, bool out_fp32, int R, int T, 
     const int4* b0 = static_cast<const int4*>(bias0);
     const int4* b1 = static_cast<const int4*>(bias1);
     if (out_fp32)
-        combine_kernel<true><<<grid, kCombineThreads, 0, stream>>>(R, T, H, K, cap, send_head, yv, recv_topk_weights,
+        err = launch_kernel(combine_kernel<true>, dim3(grid), dim3(kCombineThreads), 0, stream, 1,
+            R, T, H, K, cap, send_head, yv, recv_topk_weights,
                                                                   b0, b1, out, combined_topk_weights);
     else
-        combine_kernel<false><<<grid, kCombineThreads, 0, stream>>>(R, T, H, K, cap, send_head, yv,
+        err = launch_kernel(combine_kernel<false>, dim3(grid), dim3(kCombineThreads), 0, stream, 1,
+            R, T, H, K, cap, send_head, yv,
                                                                    recv_topk_weights, b0, b1, out,
                                                                    combined_topk_weights);
-    return cudaGetLastError();
+    return err;
 }
 
 }  // namespace ep

@@ -26,7 +26,7 @@ constexpr int kDispatchThreads = 512;
 constexpr int kCombineThreads = 256;
 constexpr int kLLCountThreads = 512;
 constexpr int kLLDispatchThreads = 512;
-constexpr int kLLCombineThreads = 512;
+constexpr int kLLCombineThreads = 256;
 
 enum DispatchMode { kModeBf16 = 0, kModeCastFp8 = 1, kModeFp8In = 2 };
 

@@ -72,6 +72,7 @@ __global__ void __launch_bounds__(kLayoutThreads)
     get_dispatch_layout_kernel(const int64_t* __restrict__ topk_idx, int R, int T, int K, int E, int EL,
                                int32_t* __restrict__ tpr, int32_t* __restrict__ tprdma,
                                int32_t* __restrict__ tpe, uint8_t* __restrict__ itr, int32_t* status) {
+    pdl_enter();
     extern __shared__ int32_t s_expert[];  // [E]
     __shared__ uint32_t s_mask[kLayoutRound];
     __shared__ int32_t s_rank[kMaxRanks];
@@ -167,6 +168,7 @@ __global__ void __launch_bounds__(kNotifyThreads)
                            int32_t* __restrict__ recv_channel_prefix, int32_t* __restrict__ num_recv,
                            int32_t* __restrict__ send_head, int32_t* __restrict__ recv_src_idx,
                            int32_t* __restrict__ num_recv_per_expert, int32_t* status) {
+    pdl_enter();
     __shared__ int32_t s_cnt[kMaxRanks];                 // hits of this CTA's slice, per rank
     __shared__ int32_t s_base[kMaxRanks];                // rows taken by earlier sources
     __shared__ int32_t s_before[kMaxRanks];              // hits of this source before the current round
@@ -315,20 +317,9 @@ __global__ void __launch_bounds__(kNotifyThreads)
 cudaError_t launch_get_dispatch_layout(const int64_t* topk_idx, int R, int T, int K, int E, int32_t* tpr,
                                        int32_t* tprdma, int32_t* tpe, uint8_t* itr, int32_t* status,
                                        cudaStream_t stream) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(kClusterCtas, R, 1);
-    cfg.blockDim = dim3(kLayoutThreads, 1, 1);
-    cfg.dynamicSmemBytes = sizeof(int32_t) * static_cast<size_t>(E);
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = kClusterCtas;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, get_dispatch_layout_kernel, topk_idx, R, T, K, E, E / R, tpr, tprdma, tpe, itr,
-                              status);
+    return launch_kernel(get_dispatch_layout_kernel, dim3(kClusterCtas, R, 1), dim3(kLayoutThreads, 1, 1),
+                         sizeof(int32_t) * static_cast<size_t>(E), stream, kClusterCtas, topk_idx, R, T, K, E, E / R,
+                         tpr, tprdma, tpe, itr, status);
 }
 
 cudaError_t launch_dispatch_notify(int R, int T, int E, int C, int A, int64_t cap, const int32_t* tpr,
@@ -336,21 +327,9 @@ cudaError_t launch_dispatch_notify(int R, int T, int E, int C, int A, int64_t ca
                                    int32_t* channel_prefix, int32_t* recv_channel_prefix, int32_t* num_recv,
                                    int32_t* send_head, int32_t* recv_src_idx, int32_t* num_recv_per_expert,
                                    int32_t* status, cudaStream_t stream) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(kClusterCtas, R + 1, 1);
-    cfg.blockDim = dim3(kNotifyThreads, 1, 1);
-    cfg.dynamicSmemBytes = 0;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = kClusterCtas;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, dispatch_notify_kernel, R, T, E, C, A, cap, tpr, itr, tpe, rank_prefix,
-                              channel_prefix, recv_channel_prefix, num_recv, send_head, recv_src_idx,
-                              num_recv_per_expert, status);
+    return launch_kernel(dispatch_notify_kernel, dim3(kClusterCtas, R + 1, 1), dim3(kNotifyThreads, 1, 1), 0, stream,
+                         kClusterCtas, R, T, E, C, A, cap, tpr, itr, tpe, rank_prefix, channel_prefix,
+                         recv_channel_prefix, num_recv, send_head, recv_src_idx, num_recv_per_expert, status);
 }
 
 }  // namespace ep

@@ -10,11 +10,13 @@
 // timing; here the rows are fixed beforehand so the layout is deterministic:
 //   1. ll_count (one CTA per source rank): stable rank of each slot among the
 //      slots of the same (source, expert), in (token, k) order, and the count;
-//   2. ll_finish (E threads): begin of each source block = prefix over
-//      sources; packed_recv_count, packed_recv_layout_range, receive stats;
-//   3. ll_dispatch (one warp per token): read + cast the row once, write the
-//      message to each of its K destinations; the final row of every slot
-//      stays in the handle for the combine.
+//   2. ll_finish: begin of each source block = prefix over sources (one warp
+//      per expert); packed_recv_count, packed_recv_layout_range, receive
+//      stats; and the final row of every slot, which stays in the handle for
+//      the combine;
+//   3. ll_dispatch: read + cast the row once into a complete message in
+//      shared memory, then one bulk store per destination slot (a register
+//      kernel, one warp per token, serves messages too long to stage).
 // LL combine (§4.3): one warp per token gathers its K expert outputs and
 // accumulates w_k * y in fp32 with fused multiply-adds in slot order.
 #include "ep_common.cuh"
@@ -32,6 +34,7 @@ constexpr int kLLCombineFanIn = 4;
 __global__ void __launch_bounds__(kLLCountThreads)
     ll_count_kernel(int R, int T, int maxT, int K, int E, const int64_t* __restrict__ topk_idx,
                     int32_t* __restrict__ slot, int32_t* __restrict__ cnt, int32_t* status) {
+    pdl_enter();
     extern __shared__ int32_t smem[];
     int32_t* s_warp = smem;                   // [kLLCountWarps][E]: per-warp count -> exclusive prefix
     int32_t* s_run = smem + kLLCountWarps * E;  // [E]: slots of this source seen so far
@@ -74,15 +77,21 @@ __global__ void __launch_bounds__(kLLCountThreads)
     for (int e = tid; e < E; e += kLLCountThreads) cnt[static_cast<int64_t>(s) * E + e] = s_run[e];
 }
 
-// One warp per expert e: lane s holds the count of source s, a warp scan gives
-// each source block's begin.  R <= 32.
-__global__ void ll_finish_kernel(int R, int maxT, int E, const int32_t* __restrict__ cnt,
-                                 int32_t* __restrict__ packed_recv_count, int64_t* __restrict__ layout_range,
-                                 int32_t* __restrict__ stats, int32_t* status) {
+// Blocks [0, expert_blocks): one warp per expert e; lane s holds the count of
+// source s, a warp scan gives each source block's begin (R <= 32).  The other
+// blocks: one thread per top-k slot turns its position within (source, expert)
+// into the final row, begin(e, s) + position, or -1 past the R * maxT capacity.
+__global__ void ll_finish_kernel(int R, int T, int maxT, int K, int E, int expert_blocks,
+                                 const int64_t* __restrict__ topk_idx, const int32_t* __restrict__ cnt,
+                                 int32_t* __restrict__ slot, int32_t* __restrict__ packed_recv_count,
+                                 int64_t* __restrict__ layout_range, int32_t* __restrict__ stats, int32_t* status) {
+    pdl_enter();
     const int64_t slots = static_cast<int64_t>(R) * maxT;
-    const int lane = lane_id();
-    const int warps = blockDim.x / kWarpSize;
-    for (int e = blockIdx.x * warps + threadIdx.x / kWarpSize; e < E; e += gridDim.x * warps) {
+    if (static_cast<int>(blockIdx.x) < expert_blocks) {
+        const int lane = lane_id();
+        const int warps = blockDim.x / kWarpSize;
+        const int e = blockIdx.x * warps + threadIdx.x / kWarpSize;
+        if (e >= E) return;
         const int32_t c = lane < R ? __ldg(cnt + static_cast<int64_t>(lane) * E + e) : 0;
         int32_t incl = c;
 #pragma unroll
@@ -102,7 +111,161 @@ __global__ void ll_finish_kernel(int R, int maxT, int E, const int32_t* __restri
             packed_recv_count[e] = n;
             if (stats != nullptr) stats[e] += n;
         }
+        return;
     }
+    const int64_t i = static_cast<int64_t>(blockIdx.x - expert_blocks) * blockDim.x + threadIdx.x;
+    if (i >= static_cast<int64_t>(R) * T * K) return;
+    const int s = static_cast<int>(i / (static_cast<int64_t>(T) * K));
+    const int64_t tk = i - static_cast<int64_t>(s) * T * K;
+    const int64_t v = __ldg(topk_idx + i);
+    int32_t* sp = slot + static_cast<int64_t>(s) * maxT * K + tk;
+    const int32_t pos = *sp;
+    int32_t row = -1;
+    if (v >= 0 && v < E && pos >= 0) {
+        int64_t begin = 0;
+        for (int sp2 = 0; sp2 < s; ++sp2) begin += __ldg(cnt + static_cast<int64_t>(sp2) * E + v);
+        if (begin + pos < slots) row = static_cast<int32_t>(begin + pos);
+    }
+    *sp = row;
+}
+
+// Bulk-copy low-latency dispatch: each CTA walks tokens blockIdx.x + j * gridDim.x
+// through `stages` shared-memory buffers.  A stage holds one complete message
+// (header, payload, FP8 scales) -- for bf16 the row is loaded straight into the
+// payload position -- and warp 0 lane 0 writes it to every valid slot's row with
+// one bulk store each.  In FP8 mode the CTA's warps first cast the staged bf16
+// row into the message.  Slot rows and expert ids arrive by cp.async on the
+// stage's barrier.  Bounded waits as in the normal bulk dispatch.
+__host__ __device__ __forceinline__ uint32_t ll_align128(uint32_t v) { return (v + 127u) & ~127u; }
+
+struct LLBulkSmem {
+    uint32_t in_stride, msg_stride, meta_bytes, total;
+};
+
+__host__ __device__ __forceinline__ LLBulkSmem ll_bulk_smem(bool fp8, int H, int64_t msg_bytes, int stages) {
+    LLBulkSmem b;
+    b.in_stride = fp8 ? ll_align128(2 * H) : 0;
+    b.msg_stride = ll_align128(static_cast<uint32_t>(msg_bytes));
+    b.meta_bytes = ll_align128(64 + stages * (32 * 4 + 32 * 8) + 16);
+    b.total = b.meta_bytes + stages * (b.in_stride + b.msg_stride);
+    return b;
+}
+
+template <bool kFp8>
+__global__ void ll_dispatch_bulk_kernel(int R, int T, int maxT, int H, int K, int E, int stages,
+                                        const uint8_t* __restrict__ x, const int64_t* __restrict__ topk_idx,
+                                        bool round_scale, bool use_ue8m0, const int32_t* __restrict__ slot,
+                                        uint8_t* __restrict__ recv_msgs, int64_t msg_bytes, int32_t* status) {
+    pdl_enter();
+    extern __shared__ __align__(128) uint8_t bulk_smem_raw[];
+    uint8_t* smem = bulk_smem_raw;
+    const int S = stages;
+    const int tid = threadIdx.x;
+    const int lane = lane_id();
+    const bool warp0 = tid < kWarpSize;
+    const int G = H / kFp8Group;
+    const uint32_t row_bytes = 2 * H;
+    const LLBulkSmem lay = ll_bulk_smem(kFp8, H, msg_bytes, S);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
+    int32_t* s_row = reinterpret_cast<int32_t*>(smem + 64);            // [S][32]
+    int64_t* s_idx = reinterpret_cast<int64_t*>(smem + 64 + S * 128);  // [S][32]
+    int32_t* s_flag = reinterpret_cast<int32_t*>(smem + 64 + S * 384);
+    uint8_t* msg_base = smem + lay.meta_bytes;
+    uint8_t* in_base = msg_base + S * lay.msg_stride;
+    const int64_t slots = static_cast<int64_t>(R) * maxT;
+    const int64_t n_tokens = static_cast<int64_t>(R) * T;
+    const int64_t first = blockIdx.x, stride = gridDim.x;
+    const int64_t n_local = first < n_tokens ? (n_tokens - 1 - first) / stride + 1 : 0;
+    if (n_local == 0) return;
+    if (tid == 0) {
+        for (int s = 0; s < S; ++s) mbar_init(&bars[s], 1 + kWarpSize);
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    auto produce = [&](int64_t j) {
+        const int st = static_cast<int>(j % S);
+        const int64_t g = first + j * stride;
+        const int64_t s = g / T;
+        const int64_t t = g - s * T;
+        if (lane < K) {
+            cp_async_4(&s_row[st * 32 + lane], slot + (s * maxT + t) * K + lane);
+            cp_async_8(&s_idx[st * 32 + lane], topk_idx + g * K + lane);
+        }
+        cp_async_arrive(&bars[st]);
+        if (lane == 0) {
+            mbar_arrive_expect_tx(&bars[st], row_bytes);
+            uint8_t* dst = kFp8 ? in_base + st * lay.in_stride : msg_base + st * lay.msg_stride + 16;
+            bulk_load(dst, x + g * row_bytes, row_bytes, &bars[st]);
+        }
+    };
+
+    if (warp0) {
+        const int64_t pro = n_local < S - 1 ? n_local : S - 1;
+        for (int64_t j = 0; j < pro; ++j) produce(j);
+    }
+    int64_t j = 0;
+    for (; j < n_local; ++j) {
+        const int st = static_cast<int>(j % S);
+        if (tid == 0) *s_flag = mbar_wait_bounded(&bars[st], static_cast<uint32_t>((j / S) & 1)) ? 1 : 0;
+        __syncthreads();
+        if (*s_flag == 0) break;
+        uint8_t* msg = msg_base + st * lay.msg_stride;
+        const int64_t g = first + j * stride;
+        if constexpr (kFp8) {
+            const int4* xin = reinterpret_cast<const int4*>(in_base + st * lay.in_stride);
+            int2* q = reinterpret_cast<int2*>(msg + 16);
+            uint8_t* tail = msg + 16 + H;
+            const int n16 = H / 8;
+            for (int i0 = (tid / kWarpSize) * kWarpSize; i0 < n16; i0 += blockDim.x) {
+                const int i = i0 + lane;
+                float f[8];
+                unpack8(i < n16 ? xin[i] : make_int4(0, 0, 0, 0), f);
+                float amax = absmax8(f);
+#pragma unroll
+                for (int off = 8; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, off));
+                const Fp8Scale fs = fp8_scale(amax, round_scale);
+                if (i < n16) {
+                    q[i] = cast8_e4m3(f, fs.mult);
+                    if ((lane & 15) == 0) {
+                        if (use_ue8m0) tail[i / 16] = static_cast<uint8_t>(fs.exponent + 127);
+                        else reinterpret_cast<float*>(tail)[i / 16] = fs.scale;
+                    }
+                }
+            }
+            if (use_ue8m0)
+                for (int w = tid; w < (3 * G) / 4; w += blockDim.x) reinterpret_cast<uint32_t*>(tail + G)[w] = 0u;
+        }
+        if (tid == 0) *reinterpret_cast<int4*>(msg) = make_int4(static_cast<int>(g % T), 0, 0, 0);
+        fence_async_smem();
+        __syncthreads();
+        if (warp0) {
+            int64_t dst_row = -1;
+            if (lane < K) {
+                const int64_t e = s_idx[st * 32 + lane];
+                const int32_t row = s_row[st * 32 + lane];
+                if (e >= 0 && e < E && row >= 0 && row < slots) dst_row = e * slots + row;
+            }
+            const unsigned dst = __ballot_sync(kFullMask, dst_row >= 0);
+            for (unsigned m = dst; m; m &= m - 1) {
+                const int k = __ffs(m) - 1;
+                const int64_t r = __shfl_sync(kFullMask, dst_row, k);
+                if (lane == 0) bulk_store(recv_msgs + r * msg_bytes, msg, static_cast<uint32_t>(msg_bytes));
+            }
+            if (lane == 0) bulk_commit();
+            if (j + S - 1 < n_local) {
+                if (lane == 0) bulk_wait_read<1>();
+                __syncwarp();
+                produce(j + S - 1);
+            }
+        }
+    }
+    if (j < n_local && tid == 0) {
+        report(status, EP_ERR_TIMEOUT);
+        const int64_t issued = (j + S - 1 < n_local) ? j + S - 1 : n_local;
+        for (int64_t k = j + 1; k < issued; ++k) mbar_wait_bounded(&bars[k % S], static_cast<uint32_t>((k / S) & 1));
+    }
+    if (tid == 0) bulk_wait_all();
 }
 
 // One warp per source token.  kFp8: e4m3 payload + scales (fp32, or UE8M0 bytes).
@@ -110,8 +273,8 @@ template <bool kFp8>
 __global__ void __launch_bounds__(kLLDispatchThreads)
     ll_dispatch_kernel(int R, int T, int maxT, int H, int K, int E, const int4* __restrict__ x,
                        const int64_t* __restrict__ topk_idx, bool round_scale, bool use_ue8m0,
-                       int32_t* __restrict__ slot, const int64_t* __restrict__ layout_range,
-                       uint8_t* __restrict__ recv_msgs, int64_t msg_bytes) {
+                       const int32_t* __restrict__ slot, uint8_t* __restrict__ recv_msgs, int64_t msg_bytes) {
+    pdl_enter();
     constexpr int kWarps = kLLDispatchThreads / kWarpSize;
     const int lane = lane_id();
     const int64_t n_tokens = static_cast<int64_t>(R) * T;
@@ -128,14 +291,11 @@ __global__ void __launch_bounds__(kLLDispatchThreads)
         int64_t row = -1;
         if (lane < K) {
             const int64_t v = __ldg(topk_idx + g * K + lane);
-            int32_t* sp = slot + (static_cast<int64_t>(s) * maxT + t) * K + lane;
-            const int32_t pos = *sp;
-            if (v >= 0 && v < E && pos >= 0) {
+            const int32_t r = __ldg(slot + (static_cast<int64_t>(s) * maxT + t) * K + lane);
+            if (v >= 0 && v < E && r >= 0 && r < slots) {
                 e = static_cast<int>(v);
-                row = (__ldg(layout_range + static_cast<int64_t>(e) * R + s) & 0xffffffffLL) + pos;
-                if (row >= slots) row = -1;
+                row = r;
             }
-            *sp = row >= 0 ? static_cast<int32_t>(row) : -1;
         }
         const unsigned dst = __ballot_sync(kFullMask, row >= 0);
         if (dst == 0u) continue;
@@ -233,6 +393,7 @@ __global__ void __launch_bounds__(kLLCombineThreads)
     ll_combine_kernel(int R, int T, int maxT, int H, int K, int E, const int4* __restrict__ y,
                       const int64_t* __restrict__ topk_idx, const float* __restrict__ topk_weights,
                       const int32_t* __restrict__ slot, int4* __restrict__ out) {
+    pdl_enter();
     constexpr int kWarps = kLLCombineThreads / kWarpSize;
     const int lane = lane_id();
     const int64_t n_tokens = static_cast<int64_t>(R) * T;
@@ -320,11 +481,19 @@ size_t ll_count_smem(int E) { return sizeof(int32_t) * static_cast<size_t>(kLLCo
 
 }  // namespace
 
+constexpr uint32_t kLLBulkMaxSmem = 200u * 1024u;  // larger messages use the register kernel
+
 cudaError_t plan_ll(LaunchPlan* plan, int num_experts) {
     const int n = plan->num_sms;
     plan->ll_dispatch_blocks[0] = resident_blocks(ll_dispatch_kernel<false>, kLLDispatchThreads, n);
     plan->ll_dispatch_blocks[1] = resident_blocks(ll_dispatch_kernel<true>, kLLDispatchThreads, n);
     plan->ll_combine_blocks = resident_blocks(ll_combine_kernel, kLLCombineThreads, n);
+    cudaError_t err = cudaFuncSetAttribute(ll_dispatch_bulk_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           static_cast<int>(kLLBulkMaxSmem));
+    if (err == cudaSuccess)
+        err = cudaFuncSetAttribute(ll_dispatch_bulk_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   static_cast<int>(kLLBulkMaxSmem));
+    if (err != cudaSuccess) return err;
     const size_t smem = ll_count_smem(num_experts);
     if (smem > 48 * 1024)
         return cudaFuncSetAttribute(ll_count_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -337,41 +506,72 @@ cudaError_t launch_ll_dispatch(const LaunchPlan& plan, int R, int T, int maxT, i
                                bool use_ue8m0, int32_t* slot, int32_t* cnt, void* recv_msgs,
                                int32_t* packed_recv_count, int64_t* layout_range, int32_t* stats,
                                int32_t* status, cudaStream_t stream) {
-    ll_count_kernel<<<R, kLLCountThreads, ll_count_smem(E), stream>>>(R, T, maxT, K, E, topk_idx, slot, cnt,
+    cudaError_t err = launch_kernel(ll_count_kernel, dim3(R), dim3(kLLCountThreads), ll_count_smem(E), stream, 1,
+            R, T, maxT, K, E, topk_idx, slot, cnt,
                                                                       status);
-    cudaError_t err = cudaGetLastError();
     if (err != cudaSuccess) return err;
-    const int fin_warps = 8;
-    ll_finish_kernel<<<(E + fin_warps - 1) / fin_warps, fin_warps * kWarpSize, 0, stream>>>(
-        R, maxT, E, cnt, packed_recv_count, layout_range, stats, status);
-    err = cudaGetLastError();
+    const int fin_threads = 256;
+    const int expert_blocks = (E + fin_threads / kWarpSize - 1) / (fin_threads / kWarpSize);
+    const int64_t n_slots = static_cast<int64_t>(R) * T * K;
+    const int slot_blocks = static_cast<int>((n_slots + fin_threads - 1) / fin_threads);
+    err = launch_kernel(ll_finish_kernel, dim3(expert_blocks + slot_blocks), dim3(fin_threads), 0, stream, 1,
+            
+        R, T, maxT, K, E, expert_blocks, topk_idx, cnt, slot, packed_recv_count, layout_range, stats, status);
     if (err != cudaSuccess) return err;
     const int64_t n_tokens = static_cast<int64_t>(R) * T;
     if (n_tokens == 0) return cudaSuccess;
     const int64_t msg = ep_ll_msg_bytes(H, use_fp8 ? 1 : 0);
-    const int grid = clamp_grid(plan.ll_dispatch_blocks[use_fp8 ? 1 : 0], n_tokens, kLLDispatchThreads / kWarpSize);
     const bool rs = round_scale || use_ue8m0;
+    // Bulk-copy kernel: about 64 KB of stages per CTA, 2..8 stages.
+    const uint32_t per_stage = ll_bulk_smem(use_fp8, H, msg, 1).total - ll_bulk_smem(use_fp8, H, msg, 0).total;
+    int S = static_cast<int>(65536u / per_stage);
+    S = S < 2 ? 2 : (S > 8 ? 8 : S);
+    const uint32_t smem = ll_bulk_smem(use_fp8, H, msg, S).total;
+    if (smem <= kLLBulkMaxSmem) {
+        // resident CTAs per SM from the shared memory (227 KB per SM, 1 KB reserved per CTA); a larger
+        // grid would only queue, since no CTA waits for another
+        int per_sm = static_cast<int>((227u * 1024u) / (smem + 1024u));
+        per_sm = per_sm < 1 ? 1 : (per_sm > 8 ? 8 : per_sm);
+        const int64_t want = static_cast<int64_t>(per_sm) * plan.num_sms;
+        const int grid = static_cast<int>(want < n_tokens ? want : n_tokens);
+        const uint8_t* xb = static_cast<const uint8_t*>(x);
+        uint8_t* mb = static_cast<uint8_t*>(recv_msgs);
+        if (use_fp8)
+            err = launch_kernel(ll_dispatch_bulk_kernel<true>, dim3(grid), dim3(4 * kWarpSize), smem, stream, 1,
+            R, T, maxT, H, K, E, S, xb, topk_idx,
+                                                                              rs, use_ue8m0, slot, mb, msg, status);
+        else
+            err = launch_kernel(ll_dispatch_bulk_kernel<false>, dim3(grid), dim3(kWarpSize), smem, stream, 1,
+            R, T, maxT, H, K, E, S, xb, topk_idx, rs,
+                                                                            use_ue8m0, slot, mb, msg, status);
+        return err;
+    }
+    const int grid = clamp_grid(plan.ll_dispatch_blocks[use_fp8 ? 1 : 0], n_tokens, kLLDispatchThreads / kWarpSize);
     if (use_fp8)
-        ll_dispatch_kernel<true><<<grid, kLLDispatchThreads, 0, stream>>>(
-            R, T, maxT, H, K, E, static_cast<const int4*>(x), topk_idx, rs, use_ue8m0, slot, layout_range,
+        err = launch_kernel(ll_dispatch_kernel<true>, dim3(grid), dim3(kLLDispatchThreads), 0, stream, 1,
+            
+            R, T, maxT, H, K, E, static_cast<const int4*>(x), topk_idx, rs, use_ue8m0, slot,
             static_cast<uint8_t*>(recv_msgs), msg);
     else
-        ll_dispatch_kernel<false><<<grid, kLLDispatchThreads, 0, stream>>>(
-            R, T, maxT, H, K, E, static_cast<const int4*>(x), topk_idx, rs, use_ue8m0, slot, layout_range,
+        err = launch_kernel(ll_dispatch_kernel<false>, dim3(grid), dim3(kLLDispatchThreads), 0, stream, 1,
+            
+            R, T, maxT, H, K, E, static_cast<const int4*>(x), topk_idx, rs, use_ue8m0, slot,
             static_cast<uint8_t*>(recv_msgs), msg);
-    return cudaGetLastError();
+    return err;
 }
 
 cudaError_t launch_ll_combine(const LaunchPlan& plan, int R, int T, int maxT, int H, int K, int E,
                               const void* y, const int64_t* topk_idx, const float* topk_weights,
                               const int32_t* slot, void* out, cudaStream_t stream) {
+    cudaError_t err = cudaSuccess;
     const int64_t n_tokens = static_cast<int64_t>(R) * T;
     if (n_tokens == 0) return cudaSuccess;
     const int grid = clamp_grid(plan.ll_combine_blocks, n_tokens, kLLCombineThreads / kWarpSize);
-    ll_combine_kernel<<<grid, kLLCombineThreads, 0, stream>>>(R, T, maxT, H, K, E, static_cast<const int4*>(y),
+    err = launch_kernel(ll_combine_kernel, dim3(grid), dim3(kLLCombineThreads), 0, stream, 1,
+            R, T, maxT, H, K, E, static_cast<const int4*>(y),
                                                               topk_idx, topk_weights, slot,
                                                               static_cast<int4*>(out));
-    return cudaGetLastError();
+    return err;
 }
 
 }  // namespace ep

@@ -22,6 +22,7 @@ STATUS_NAMES = {0: "EP_OK", 1: "EP_ERR_INVALID_ARG", 2: "EP_ERR_CAPACITY", 3: "E
                 4: "EP_ERR_CUDA", 5: "EP_ERR_UNSUPPORTED", 6: "EP_ERR_INCONSISTENT",
                 7: "EP_ERR_BAD_EXPERT", 8: "EP_ERR_STATE"}
 EP_BF16, EP_FP8_E4M3, EP_FP32 = 0, 1, 2
+EP_DISPATCH_FRESH, EP_DISPATCH_CACHED, EP_DISPATCH_PREPARED = 0, 1, 2
 FIELDS = {"rank_prefix_matrix": 0, "channel_prefix_matrix": 1, "recv_channel_prefix_matrix": 2,
           "recv_src_idx": 3, "send_head": 4, "num_recv": 5, "ll_slot_row": 6}
 
@@ -43,7 +44,7 @@ _lib = None
 EXPORTS = ("ep_handle_create", "ep_handle_destroy", "ep_handle_status", "ep_handle_num_recv",
            "ep_handle_field_bytes", "ep_handle_export", "ep_status_string", "ep_last_error",
            "ep_get_dispatch_layout", "ep_dispatch", "ep_combine", "ep_ll_msg_bytes", "ep_ll_dispatch",
-           "ep_ll_combine", "ep_ll_dispatch_noalloc")
+           "ep_ll_combine", "ep_ll_dispatch_noalloc", "ep_notify_dispatch")
 
 
 def library_path() -> str:
@@ -78,11 +79,12 @@ def lib():
         L.ep_ll_msg_bytes.restype = I64
         L.ep_ll_dispatch.argtypes = [P, I32, P, P, I32, I32, I32, P, P, P, P, P]
         L.ep_ll_combine.argtypes = [P, P, P, P, P, P]
+        L.ep_notify_dispatch.argtypes = [P, I32, P, P, P, P, P]
         L.ep_ll_dispatch_noalloc.argtypes = [I32, I32, I32, I32, I32, I32, P, P, I32, I32, I32, P, P, P, P, P, P,
                                              P]
         for name in ("ep_handle_create", "ep_handle_status", "ep_handle_num_recv", "ep_handle_export",
                      "ep_get_dispatch_layout", "ep_dispatch", "ep_combine", "ep_ll_dispatch", "ep_ll_combine",
-                     "ep_ll_dispatch_noalloc"):
+                     "ep_ll_dispatch_noalloc", "ep_notify_dispatch"):
             getattr(L, name).restype = S
         _lib = L
     return _lib
@@ -257,11 +259,31 @@ def ep_get_dispatch_layout(h: Handle, topk_idx: torch.Tensor, num_tokens_per_ran
                 is_token_in_rank=itr)
 
 
+def ep_notify_dispatch(h: Handle, num_tokens_per_rank, is_token_in_rank, num_tokens_per_expert,
+                       num_recv_tokens_per_expert=None, stream=None):
+    """Build the dispatch record (notify step); follow with ep_dispatch(..., prepared=True)."""
+    c, d = h.cfg, h.device
+    R = c.num_ranks
+    T = is_token_in_rank.shape[1]
+    if is_token_in_rank.dtype not in (torch.bool, torch.uint8):
+        raise TypeError("is_token_in_rank must be bool or uint8")
+    if num_recv_tokens_per_expert is None:
+        num_recv_tokens_per_expert = _empty((R, c.num_local_experts), torch.int32, d)
+    _raise(lib().ep_notify_dispatch(
+        h.ptr, T, _ptr(num_tokens_per_rank, "num_tokens_per_rank", torch.int32, (R, R), d),
+        _ptr(is_token_in_rank, "is_token_in_rank", None, (R, T, R), d),
+        _ptr(num_tokens_per_expert, "num_tokens_per_expert", torch.int32, (R, c.num_experts), d),
+        _ptr(num_recv_tokens_per_expert, "num_recv_tokens_per_expert", torch.int32, (R, c.num_local_experts), d),
+        _stream(stream)))
+    h.normal_tokens = T
+    return num_recv_tokens_per_expert
+
+
 def ep_dispatch(h: Handle, x: torch.Tensor, topk_idx=None, topk_weights=None, num_tokens_per_rank=None,
                 is_token_in_rank=None, num_tokens_per_expert=None, x_scales=None, cast_to_fp8: bool = False,
                 cached: bool = False, recv_x=None, recv_x_scales=None, recv_topk_idx=None, recv_topk_weights=None,
-                num_recv_tokens_per_expert=None, with_topk: bool = True, stream=None):
-    """Normal-mode dispatch into [R][cap][...] receive buffers (fresh or cached record)."""
+                num_recv_tokens_per_expert=None, with_topk: bool = True, prepared: bool = False, stream=None):
+    """Normal-mode dispatch into [R][cap][...] receive buffers (fresh, cached or prepared record)."""
     c, d = h.cfg, h.device
     R, H, K, cap = c.num_ranks, c.hidden, c.num_topk, c.recv_capacity
     T = x.shape[1]
@@ -276,13 +298,14 @@ def ep_dispatch(h: Handle, x: torch.Tensor, topk_idx=None, topk_weights=None, nu
         recv_x = _empty((R, cap, H), torch.float8_e4m3fn if fp8_out else torch.bfloat16, d)
     if fp8_out and recv_x_scales is None:
         recv_x_scales = _empty((R, cap, G), torch.float32, d)
+    mode = EP_DISPATCH_CACHED if cached else (EP_DISPATCH_PREPARED if prepared else EP_DISPATCH_FRESH)
     if not cached:
         if with_topk and topk_idx is not None:
             if recv_topk_idx is None:
                 recv_topk_idx = _empty((R, cap, K), torch.int64, d)
             if topk_weights is not None and recv_topk_weights is None:
                 recv_topk_weights = _empty((R, cap, K), torch.float32, d)
-        if num_recv_tokens_per_expert is None:
+        if num_recv_tokens_per_expert is None and not prepared:
             num_recv_tokens_per_expert = _empty((R, c.num_local_experts), torch.int32, d)
     itr_ptr = None
     if is_token_in_rank is not None:
@@ -301,8 +324,8 @@ def ep_dispatch(h: Handle, x: torch.Tensor, topk_idx=None, topk_weights=None, nu
         _ptr(recv_topk_idx, "recv_topk_idx", torch.int64, (R, cap, K), d),
         _ptr(recv_topk_weights, "recv_topk_weights", torch.float32, (R, cap, K), d),
         _ptr(num_recv_tokens_per_expert, "num_recv_tokens_per_expert", torch.int32, (R, c.num_local_experts), d),
-        int(bool(cached)), _stream(stream)))
-    if not cached:
+        mode, _stream(stream)))
+    if mode == EP_DISPATCH_FRESH:
         h.normal_tokens = T
     return dict(recv_x=recv_x, recv_x_scales=recv_x_scales, recv_topk_idx=recv_topk_idx,
                 recv_topk_weights=recv_topk_weights, num_recv_tokens_per_expert=num_recv_tokens_per_expert)

@@ -140,11 +140,33 @@ ep_status ep_get_dispatch_layout(ep_handle* h, int32_t num_tokens, const int64_t
 
 /* -------------------------------------------------------- normal dispatch */
 
+/* How ep_dispatch() obtains the dispatch record. */
+typedef enum ep_dispatch_mode {
+    EP_DISPATCH_FRESH = 0,    /* build the record from the layout inputs, then move the rows          */
+    EP_DISPATCH_CACHED = 1,   /* reuse the record of an earlier dispatch; no top-k inputs or outputs  */
+    EP_DISPATCH_PREPARED = 2  /* use the record that ep_notify_dispatch() just built for this call;
+                                 top-k inputs and outputs as in fresh mode, layout inputs NULL        */
+} ep_dispatch_mode;
+
+/* The notify step of a dispatch ([P1] notify_dispatch; [P3] §4.1 the
+ * prefix matrices, recv_src_idx, send_head and num_recv_tokens_per_expert):
+ * builds the handle's dispatch record for num_tokens tokens per rank from
+ * num_tokens_per_rank [R][R], is_token_in_rank [R][T][R] and
+ * num_tokens_per_expert [R][E], and writes num_recv_tokens_per_expert
+ * [R][EL] (aligned).  Exactly what the fresh mode of ep_dispatch() does
+ * first; call it on its own to read the receive counts
+ * (ep_handle_num_recv) before moving any row, then ep_dispatch() in
+ * EP_DISPATCH_PREPARED mode with the same num_tokens. */
+ep_status ep_notify_dispatch(ep_handle* h, int32_t num_tokens, const int32_t* num_tokens_per_rank,
+                             const uint8_t* is_token_in_rank, const int32_t* num_tokens_per_expert,
+                             int32_t* num_recv_tokens_per_expert, ep_stream_t stream);
+
 /* Normal-mode dispatch ([P3] §4.1 intranode_dispatch).
  *
- * Fresh mode (cached == 0): first builds the dispatch record in the handle
- * from num_tokens_per_rank [R][R], is_token_in_rank [R][T][R] and
- * num_tokens_per_expert [R][E] (the layout outputs):
+ * `cached` takes an ep_dispatch_mode.  Fresh mode (EP_DISPATCH_FRESH): first
+ * builds the dispatch record in the handle from num_tokens_per_rank [R][R],
+ * is_token_in_rank [R][T][R] and num_tokens_per_expert [R][E] (the layout
+ * outputs), as ep_notify_dispatch() does:
  *   rank_prefix_matrix[s][r] = sum_{s'<=s} num_tokens_per_rank[s'][r]
  *   receive rows: inside rank r, tokens arrive ordered by source rank, then
  *     token index; send_head[s][t][r] = that row, or -1 if not sent
@@ -154,10 +176,13 @@ ep_status ep_get_dispatch_layout(ep_handle* h, int32_t num_tokens, const int64_t
  *   recv_channel_prefix_matrix[r][s][c] = first row of that channel in r
  *   num_recv_tokens_per_expert[r][j] (int32 [R][EL], output) = received
  *     top-k slots of local expert j, rounded up to expert_alignment
- * Cached mode (cached != 0): reuses the record of the last fresh dispatch on
- * this handle with the same num_tokens; topk_idx, topk_weights, the three
- * layout inputs, recv_topk_* and num_recv_tokens_per_expert must be NULL
- * ([P3] §4.1: a cached handle takes no top-k inputs).
+ * Cached mode (EP_DISPATCH_CACHED): reuses the record of the last fresh or
+ * prepared dispatch on this handle with the same num_tokens; topk_idx,
+ * topk_weights, the three layout inputs, recv_topk_* and
+ * num_recv_tokens_per_expert must be NULL ([P3] §4.1: a cached handle takes
+ * no top-k inputs).  Prepared mode (EP_DISPATCH_PREPARED): the record of the
+ * ep_notify_dispatch() call just made with the same num_tokens; the layout
+ * inputs and num_recv_tokens_per_expert must be NULL, top-k as in fresh mode.
  *
  * Payload (both modes), for every (s,t) and every rank r it is sent to:
  *   x_dtype == EP_BF16, cast_to_fp8 == 0: recv_x[r][row] = x[s][t] (bf16 [.][.][H])

@@ -115,6 +115,29 @@ def test_cached_dispatch_reuses_record():
     s.check()
 
 
+def test_notify_then_prepared_dispatch_equals_fresh():
+    """ep_notify_dispatch + the prepared mode give the fresh dispatch's record and rows."""
+    shape = S("prepared", 8, 700, 1024, 64, 6, routing="zipf", mask_p=0.05, A=4, seed=26)
+    res = P.run_normal(shape)
+    h2 = ep.Handle(P.config_of(shape, res["cap"]))
+    idx_d = torch.from_numpy(res["idx"]).to(P.DEV)
+    w_d = torch.from_numpy(res["w"]).to(P.DEV)
+    lay = ep.ep_get_dispatch_layout(h2, idx_d)
+    nrpe = ep.ep_notify_dispatch(h2, lay["num_tokens_per_rank"], lay["is_token_in_rank"], lay["num_tokens_per_expert"])
+    assert (h2.num_recv().numpy() == res["ora_n"]["num_recv"]).all()  # counts readable before any row moves
+    d = ep.ep_dispatch(h2, P.dev_bf16(res["x"]), topk_idx=idx_d, topk_weights=w_d, prepared=True)
+    assert h2.status() == 0
+    np.testing.assert_array_equal(P.host(nrpe), res["ora_n"]["num_recv_tokens_per_expert"])
+    P.compare_record(h2, res["ora_n"], shape.T)
+    rows = P.valid_rows(res["ora_n"]["num_recv"], res["cap"])
+    np.testing.assert_array_equal(P.host(d["recv_x"])[rows], res["ora_d"]["recv_x"][rows])
+    np.testing.assert_array_equal(P.host(d["recv_topk_idx"])[rows], res["ora_d"]["recv_topk_idx"][rows])
+    np.testing.assert_array_equal(P.host(d["recv_topk_weights"])[rows], res["ora_d"]["recv_topk_weights"][rows])
+    # the record is consumed: a second prepared dispatch needs a new notify
+    with pytest.raises(ep.EPError):
+        ep.ep_dispatch(h2, P.dev_bf16(res["x"]), topk_idx=idx_d, prepared=True)
+
+
 def test_combine_of_dispatch_restores_x():
     """combine(dispatch(x)) / (number of receiving ranks) == x exactly (fp32 out)."""
     shape = S("roundtrip", 8, 300, 1024, 32, 4, mask_p=0.1, seed=21)
