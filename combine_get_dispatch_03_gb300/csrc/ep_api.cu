@@ -33,6 +33,7 @@ struct ep_handle {
     int32_t* send_head = nullptr;            // [R][maxT][R]
     int32_t* ll_slot = nullptr;              // [R][maxT][K]
     int32_t* ll_cnt = nullptr;               // [R][E]
+    int32_t* rank_mask = nullptr;            // [R], nonzero = masked
     int normal_tokens = -1;                  // T of the current dispatch record, -1 = none
     bool prepared = false;                   // record built by ep_notify_dispatch, not yet used
     int ll_tokens = -1;                      // T of the last LL dispatch, -1 = none
@@ -171,10 +172,10 @@ ep_status ep_handle_create(const ep_config* cfg, ep_handle** out) {
 
     const size_t R = cfg->num_ranks, C = cfg->num_channels, T = cfg->num_max_tokens, K = cfg->num_topk;
     const size_t E = cfg->num_experts, cap = static_cast<size_t>(cfg->recv_capacity);
-    const size_t sizes[] = {1, R * R, R * R * C, R * R * C, R, R * cap, R * T * R, R * T * K, R * E};
+    const size_t sizes[] = {1, R * R, R * R * C, R * R * C, R, R * cap, R * T * R, R * T * K, R * E, R};
     int32_t** slots[] = {&h->status,   &h->rank_prefix,  &h->channel_prefix, &h->recv_channel_prefix,
                          &h->num_recv, &h->recv_src_idx, &h->send_head,      &h->ll_slot,
-                         &h->ll_cnt};
+                         &h->ll_cnt,   &h->rank_mask};
     size_t total = 0;
     for (size_t s : sizes) total += align_up(s * sizeof(int32_t), 256);
     err = cudaMalloc(&h->dmem, total);
@@ -451,7 +452,7 @@ ep_status ep_ll_dispatch(ep_handle* h, int32_t num_tokens, const void* x, const 
     DeviceGuard guard(h->device);
     cudaError_t err = ep::launch_ll_dispatch(h->plan, c.num_ranks, num_tokens, c.num_max_tokens, c.hidden, c.num_topk,
                                              c.num_experts, x, topk_idx, use_fp8 != 0, round_scale != 0,
-                                             use_ue8m0 != 0, h->ll_slot, h->ll_cnt, recv_msgs, packed_recv_count,
+                                             use_ue8m0 != 0, h->rank_mask, h->ll_slot, h->ll_cnt, recv_msgs, packed_recv_count,
                                              packed_recv_layout_range, cumulative_local_expert_recv_stats, h->status,
                                              stream);
     if (err != cudaSuccess) return cuda_fail(err, "low-latency dispatch launch");
@@ -473,6 +474,44 @@ ep_status ep_ll_combine(ep_handle* h, const void* x, const int64_t* topk_idx, co
     cudaError_t err = ep::launch_ll_combine(h->plan, c.num_ranks, T, c.num_max_tokens, c.hidden, c.num_topk,
                                             c.num_experts, x, topk_idx, topk_weights, h->ll_slot, combined_x, stream);
     if (err != cudaSuccess) return cuda_fail(err, "low-latency combine launch");
+    return EP_OK;
+}
+
+ep_status ep_update_mask_buffer(ep_handle* h, int32_t rank, int32_t masked, ep_stream_t stream) {
+    if (h == nullptr) return fail(EP_ERR_INVALID_ARG, "handle is NULL");
+    EP_CHECK_ARG(rank >= 0 && rank < h->cfg.num_ranks, "rank %d outside [0, %d)", rank, h->cfg.num_ranks);
+    DeviceGuard guard(h->device);
+    cudaError_t err = cudaMemsetAsync(h->rank_mask + rank, 0, sizeof(int32_t), stream);
+    if (err == cudaSuccess && masked) err = cudaMemsetAsync(h->rank_mask + rank, 1, 1, stream);
+    if (err != cudaSuccess) return cuda_fail(err, "updating the mask buffer");
+    return EP_OK;
+}
+
+ep_status ep_query_mask_buffer(ep_handle* h, int32_t* host_mask, ep_stream_t stream) {
+    if (h == nullptr || host_mask == nullptr) return fail(EP_ERR_INVALID_ARG, "NULL argument");
+    DeviceGuard guard(h->device);
+    cudaError_t err = cudaMemcpyAsync(host_mask, h->rank_mask, sizeof(int32_t) * h->cfg.num_ranks, cudaMemcpyDefault,
+                                      stream);
+    if (err == cudaSuccess) err = cudaStreamSynchronize(stream);
+    if (err != cudaSuccess) return cuda_fail(err, "reading the mask buffer");
+    return EP_OK;
+}
+
+ep_status ep_clean_mask_buffer(ep_handle* h, ep_stream_t stream) {
+    if (h == nullptr) return fail(EP_ERR_INVALID_ARG, "handle is NULL");
+    DeviceGuard guard(h->device);
+    cudaError_t err = cudaMemsetAsync(h->rank_mask, 0, sizeof(int32_t) * h->cfg.num_ranks, stream);
+    if (err != cudaSuccess) return cuda_fail(err, "clearing the mask buffer");
+    return EP_OK;
+}
+
+ep_status ep_selftest_bounded_wait(ep_handle* h, uint32_t max_iterations, int32_t rank, ep_stream_t stream) {
+    if (h == nullptr) return fail(EP_ERR_INVALID_ARG, "handle is NULL");
+    EP_CHECK_ARG(rank >= 0 && rank < h->cfg.num_ranks, "rank %d outside [0, %d)", rank, h->cfg.num_ranks);
+    EP_CHECK_ARG(max_iterations >= 1 && max_iterations <= (1u << 20), "max_iterations must lie in [1, 2^20]");
+    DeviceGuard guard(h->device);
+    cudaError_t err = ep::launch_bounded_wait_selftest(max_iterations, rank, h->rank_mask, h->status, stream);
+    if (err != cudaSuccess) return cuda_fail(err, "self-test launch");
     return EP_OK;
 }
 

@@ -170,8 +170,9 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Bounded wait for the phase with the given parity; false if the cap was reached.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
-    for (uint32_t it = 0; it < kMaxWaitIterations; ++it)
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
+                                                  uint32_t max_iterations = kMaxWaitIterations) {
+    for (uint32_t it = 0; it < max_iterations; ++it)
         if (mbar_try_wait(bar, parity)) return true;
     return false;
 }

@@ -55,9 +55,12 @@ cudaError_t launch_combine(const LaunchPlan& plan, bool out_fp32, int R, int T, 
 
 cudaError_t launch_ll_dispatch(const LaunchPlan& plan, int R, int T, int maxT, int H, int K, int E,
                                const void* x, const int64_t* topk_idx, bool use_fp8, bool round_scale,
-                               bool use_ue8m0, int32_t* slot, int32_t* cnt, void* recv_msgs,
-                               int32_t* packed_recv_count, int64_t* layout_range, int32_t* stats,
-                               int32_t* status, cudaStream_t stream);
+                               bool use_ue8m0, const int32_t* rank_mask, int32_t* slot, int32_t* cnt,
+                               void* recv_msgs, int32_t* packed_recv_count, int64_t* layout_range,
+                               int32_t* stats, int32_t* status, cudaStream_t stream);
+
+cudaError_t launch_bounded_wait_selftest(uint32_t max_iterations, int rank, int32_t* rank_mask, int32_t* status,
+                                         cudaStream_t stream);
 
 cudaError_t launch_ll_combine(const LaunchPlan& plan, int R, int T, int maxT, int H, int K, int E,
                               const void* y, const int64_t* topk_idx, const float* topk_weights,

@@ -33,7 +33,8 @@ constexpr int kLLCombineFanIn = 4;
 
 __global__ void __launch_bounds__(kLLCountThreads)
     ll_count_kernel(int R, int T, int maxT, int K, int E, const int64_t* __restrict__ topk_idx,
-                    int32_t* __restrict__ slot, int32_t* __restrict__ cnt, int32_t* status) {
+                    const int32_t* __restrict__ rank_mask, int32_t* __restrict__ slot, int32_t* __restrict__ cnt,
+                    int32_t* status) {
     pdl_enter();
     extern __shared__ int32_t smem[];
     int32_t* s_warp = smem;                   // [kLLCountWarps][E]: per-warp count -> exclusive prefix
@@ -56,6 +57,9 @@ __global__ void __launch_bounds__(kLLCountThreads)
             const int64_t v = __ldg(idx_s + i);
             if (v >= 0 && v < E) e = static_cast<int>(v);
             else if (v != -1) report(status, EP_ERR_BAD_EXPERT);
+            // a masked rank neither sends nor receives
+            if (e >= 0 && rank_mask != nullptr && (__ldg(rank_mask + s) != 0 || __ldg(rank_mask + e / (E / R)) != 0))
+                e = -1;
         }
         const unsigned peers = __match_any_sync(kFullMask, e);
         const int before = __popc(peers & lanemask_lt());
@@ -464,6 +468,23 @@ __global__ void __launch_bounds__(kLLCombineThreads)
     }
 }
 
+// Self-test of the bounded waits: one thread waits, with a small iteration cap, on
+// an mbarrier whose phase nothing completes.  The wait must give up, record
+// EP_ERR_TIMEOUT and mark `rank` in the mask buffer -- what a receiver does
+// with a source rank that never delivers ([P1] low-latency receive excerpt).
+__global__ void bounded_wait_selftest_kernel(uint32_t max_iterations, int rank, int32_t* rank_mask,
+                                             int32_t* status) {
+    pdl_enter();
+    __shared__ uint64_t bar;
+    if (threadIdx.x != 0) return;
+    mbar_init(&bar, 1);
+    fence_barrier_init();
+    if (!mbar_wait_bounded(&bar, 0, max_iterations)) {
+        report(status, EP_ERR_TIMEOUT);
+        if (rank_mask != nullptr) atomicExch(rank_mask + rank, 1);
+    }
+}
+
 template <typename Kernel>
 int resident_blocks(Kernel k, int threads, int num_sms, size_t smem = 0) {
     int per_sm = 0;
@@ -503,11 +524,11 @@ cudaError_t plan_ll(LaunchPlan* plan, int num_experts) {
 
 cudaError_t launch_ll_dispatch(const LaunchPlan& plan, int R, int T, int maxT, int H, int K, int E,
                                const void* x, const int64_t* topk_idx, bool use_fp8, bool round_scale,
-                               bool use_ue8m0, int32_t* slot, int32_t* cnt, void* recv_msgs,
-                               int32_t* packed_recv_count, int64_t* layout_range, int32_t* stats,
-                               int32_t* status, cudaStream_t stream) {
+                               bool use_ue8m0, const int32_t* rank_mask, int32_t* slot, int32_t* cnt,
+                               void* recv_msgs, int32_t* packed_recv_count, int64_t* layout_range,
+                               int32_t* stats, int32_t* status, cudaStream_t stream) {
     cudaError_t err = launch_kernel(ll_count_kernel, dim3(R), dim3(kLLCountThreads), ll_count_smem(E), stream, 1,
-            R, T, maxT, K, E, topk_idx, slot, cnt,
+            R, T, maxT, K, E, topk_idx, rank_mask, slot, cnt,
                                                                       status);
     if (err != cudaSuccess) return err;
     const int fin_threads = 256;
@@ -572,6 +593,12 @@ cudaError_t launch_ll_combine(const LaunchPlan& plan, int R, int T, int maxT, in
                                                               topk_idx, topk_weights, slot,
                                                               static_cast<int4*>(out));
     return err;
+}
+
+cudaError_t launch_bounded_wait_selftest(uint32_t max_iterations, int rank, int32_t* rank_mask, int32_t* status,
+                                         cudaStream_t stream) {
+    return launch_kernel(bounded_wait_selftest_kernel, dim3(1), dim3(kWarpSize), 0, stream, 1, max_iterations, rank,
+                         rank_mask, status);
 }
 
 }  // namespace ep

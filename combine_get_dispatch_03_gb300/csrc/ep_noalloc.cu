@@ -107,7 +107,8 @@ extern "C" ep_status ep_ll_dispatch_noalloc(int32_t num_ranks, int32_t num_token
     ep_status st = setup_device(device, &s);
     if (st != EP_OK) return st;
     cudaError_t err = ep::launch_ll_dispatch(s->plan, R, T, maxT, H, K, E, x, topk_idx, use_fp8 != 0,
-                                             round_scale != 0, use_ue8m0 != 0, slot_row, s->scratch, recv_msgs,
+                                             round_scale != 0, use_ue8m0 != 0, nullptr, slot_row, s->scratch,
+                                             recv_msgs,
                                              packed_recv_count, packed_recv_layout_range,
                                              cumulative_local_expert_recv_stats, status, stream);
     if (err != cudaSuccess) return reject(EP_ERR_CUDA, cudaGetErrorString(err));

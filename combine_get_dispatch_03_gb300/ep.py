@@ -44,7 +44,8 @@ _lib = None
 EXPORTS = ("ep_handle_create", "ep_handle_destroy", "ep_handle_status", "ep_handle_num_recv",
            "ep_handle_field_bytes", "ep_handle_export", "ep_status_string", "ep_last_error",
            "ep_get_dispatch_layout", "ep_dispatch", "ep_combine", "ep_ll_msg_bytes", "ep_ll_dispatch",
-           "ep_ll_combine", "ep_ll_dispatch_noalloc", "ep_notify_dispatch")
+           "ep_ll_combine", "ep_ll_dispatch_noalloc", "ep_notify_dispatch", "ep_update_mask_buffer",
+           "ep_query_mask_buffer", "ep_clean_mask_buffer", "ep_selftest_bounded_wait")
 
 
 def library_path() -> str:
@@ -80,11 +81,16 @@ def lib():
         L.ep_ll_dispatch.argtypes = [P, I32, P, P, I32, I32, I32, P, P, P, P, P]
         L.ep_ll_combine.argtypes = [P, P, P, P, P, P]
         L.ep_notify_dispatch.argtypes = [P, I32, P, P, P, P, P]
+        L.ep_update_mask_buffer.argtypes = [P, I32, I32, P]
+        L.ep_query_mask_buffer.argtypes = [P, P, P]
+        L.ep_clean_mask_buffer.argtypes = [P, P]
+        L.ep_selftest_bounded_wait.argtypes = [P, ctypes.c_uint32, I32, P]
         L.ep_ll_dispatch_noalloc.argtypes = [I32, I32, I32, I32, I32, I32, P, P, I32, I32, I32, P, P, P, P, P, P,
                                              P]
         for name in ("ep_handle_create", "ep_handle_status", "ep_handle_num_recv", "ep_handle_export",
                      "ep_get_dispatch_layout", "ep_dispatch", "ep_combine", "ep_ll_dispatch", "ep_ll_combine",
-                     "ep_ll_dispatch_noalloc", "ep_notify_dispatch"):
+                     "ep_ll_dispatch_noalloc", "ep_notify_dispatch", "ep_update_mask_buffer",
+                     "ep_query_mask_buffer", "ep_clean_mask_buffer", "ep_selftest_bounded_wait"):
             getattr(L, name).restype = S
         _lib = L
     return _lib
@@ -215,6 +221,24 @@ class Handle:
             T = self.normal_tokens or 0
             out = out.view(-1)[:c.num_ranks * T * c.num_ranks].view(c.num_ranks, T, c.num_ranks)
         return out
+
+
+def ep_update_mask_buffer(h: Handle, rank: int, masked: bool = True, stream=None):
+    _raise(lib().ep_update_mask_buffer(h.ptr, rank, int(bool(masked)), _stream(stream)))
+
+
+def ep_query_mask_buffer(h: Handle, stream=None) -> torch.Tensor:
+    out = torch.zeros(h.cfg.num_ranks, dtype=torch.int32)
+    _raise(lib().ep_query_mask_buffer(h.ptr, ctypes.c_void_p(out.data_ptr()), _stream(stream)))
+    return out
+
+
+def ep_clean_mask_buffer(h: Handle, stream=None):
+    _raise(lib().ep_clean_mask_buffer(h.ptr, _stream(stream)))
+
+
+def ep_selftest_bounded_wait(h: Handle, max_iterations: int, rank: int, stream=None):
+    _raise(lib().ep_selftest_bounded_wait(h.ptr, max_iterations, rank, _stream(stream)))
 
 
 def ep_handle_create(cfg: Config, device=None) -> Handle:

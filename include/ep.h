@@ -268,6 +268,29 @@ ep_status ep_ll_dispatch(ep_handle* h, int32_t num_tokens, const void* x, const 
 ep_status ep_ll_combine(ep_handle* h, const void* x, const int64_t* topk_idx,
                         const float* topk_weights, void* combined_x, ep_stream_t stream);
 
+/* ------------------------------------------------------- rank masking */
+
+/* The handle's mask buffer ([P1] low-latency: mask_buffer, is_rank_masked,
+ * query / update / clean_mask_buffer): one int32 per rank, all zero after
+ * ep_handle_create().  ep_ll_dispatch() treats every slot whose source or
+ * destination rank is masked as a masked slot (no message, not counted, no
+ * contribution in ep_ll_combine()): a masked rank neither sends nor
+ * receives.  The normal-mode path ignores the mask.
+ *   update: asynchronously set (masked != 0) or clear one rank's entry;
+ *   query:  synchronise `stream` and copy the R entries to host_mask[R];
+ *   clean:  asynchronously clear every entry. */
+ep_status ep_update_mask_buffer(ep_handle* h, int32_t rank, int32_t masked, ep_stream_t stream);
+ep_status ep_query_mask_buffer(ep_handle* h, int32_t* host_mask, ep_stream_t stream);
+ep_status ep_clean_mask_buffer(ep_handle* h, ep_stream_t stream);
+
+/* Self-test of the bounded device waits (no counterpart on the pages): one
+ * kernel waits, at most max_iterations (1..2^20) polls, on an mbarrier phase
+ * that nothing completes.  The wait gives up, records EP_ERR_TIMEOUT in the
+ * status word and masks `rank` -- what the pages' receiver does with a
+ * source rank that never delivers -- and the kernel returns.  Nothing hangs
+ * or traps; read the outcome with ep_handle_status() / ep_query_mask_buffer(). */
+ep_status ep_selftest_bounded_wait(ep_handle* h, uint32_t max_iterations, int32_t rank, ep_stream_t stream);
+
 /* ------------------------------------- low-latency dispatch, no allocation */
 
 /* Capacity of the fixed count scratch of ep_ll_dispatch_noalloc(): int32

@@ -41,36 +41,57 @@ def build(force: bool = False) -> str:
     return _LIB_PATH
 
 
+def _bind(lib):
+    P = ctypes.c_void_p
+    I = ctypes.c_int
+    L = ctypes.c_int64
+    lib.oracle_bf16_to_f32.argtypes = [ctypes.c_uint16]
+    lib.oracle_bf16_to_f32.restype = ctypes.c_float
+    lib.oracle_f32_to_bf16.argtypes = [ctypes.c_float]
+    lib.oracle_f32_to_bf16.restype = ctypes.c_uint16
+    lib.oracle_f32_to_e4m3.argtypes = [ctypes.c_float]
+    lib.oracle_f32_to_e4m3.restype = ctypes.c_uint8
+    lib.oracle_e4m3_to_f32.argtypes = [ctypes.c_uint8]
+    lib.oracle_e4m3_to_f32.restype = ctypes.c_float
+    lib.oracle_fp8_quantize_group.argtypes = [P, I, I, P, P, P]
+    lib.oracle_fp8_quantize_group.restype = None
+    lib.oracle_get_dispatch_layout.argtypes = [I, I, I, I, P, P, P, P, P]
+    lib.oracle_dispatch_notify.argtypes = [I, I, I, I, I, L, P, P, P, P, P, P, P, P, P, P]
+    lib.oracle_dispatch.argtypes = [I, I, I, I, I, L, I, P, P, P, P, P, P, L, P, P, P, P]
+    lib.oracle_combine.argtypes = [I, I, I, I, L, P, P, P, P, P, I, P, L, P, P]
+    lib.oracle_ll_msg_bytes.argtypes = [I, I]
+    lib.oracle_ll_msg_bytes.restype = L
+    lib.oracle_ll_dispatch.argtypes = [I, I, I, I, I, I, P, P, P, I, I, I, P, P, P, P]
+    lib.oracle_ll_combine.argtypes = [I, I, I, I, I, I, P, P, P, P, P, L, P]
+    for name in ("oracle_get_dispatch_layout", "oracle_dispatch_notify", "oracle_dispatch",
+                 "oracle_combine", "oracle_ll_dispatch", "oracle_ll_combine"):
+        getattr(lib, name).restype = I
+    return lib
+
+
+class use_library:
+    """Run the wrappers against another build of the oracle source (the mutation tests plant a
+    mistake in a copy of ep_oracle.c and check that the pins catch it)."""
+
+    def __init__(self, path):
+        self.lib = _bind(ctypes.CDLL(path))
+
+    def __enter__(self):
+        global _lib
+        self.saved = _load()
+        _lib = self.lib
+        return self
+
+    def __exit__(self, *exc):
+        global _lib
+        _lib = self.saved
+
+
 def _load():
     global _lib
     if _lib is None:
         build()
-        lib = ctypes.CDLL(_LIB_PATH)
-        P = ctypes.c_void_p
-        I = ctypes.c_int
-        L = ctypes.c_int64
-        lib.oracle_bf16_to_f32.argtypes = [ctypes.c_uint16]
-        lib.oracle_bf16_to_f32.restype = ctypes.c_float
-        lib.oracle_f32_to_bf16.argtypes = [ctypes.c_float]
-        lib.oracle_f32_to_bf16.restype = ctypes.c_uint16
-        lib.oracle_f32_to_e4m3.argtypes = [ctypes.c_float]
-        lib.oracle_f32_to_e4m3.restype = ctypes.c_uint8
-        lib.oracle_e4m3_to_f32.argtypes = [ctypes.c_uint8]
-        lib.oracle_e4m3_to_f32.restype = ctypes.c_float
-        lib.oracle_fp8_quantize_group.argtypes = [P, I, I, P, P, P]
-        lib.oracle_fp8_quantize_group.restype = None
-        lib.oracle_get_dispatch_layout.argtypes = [I, I, I, I, P, P, P, P, P]
-        lib.oracle_dispatch_notify.argtypes = [I, I, I, I, I, L, P, P, P, P, P, P, P, P, P, P]
-        lib.oracle_dispatch.argtypes = [I, I, I, I, I, L, I, P, P, P, P, P, P, L, P, P, P, P]
-        lib.oracle_combine.argtypes = [I, I, I, I, L, P, P, P, P, P, I, P, L, P, P]
-        lib.oracle_ll_msg_bytes.argtypes = [I, I]
-        lib.oracle_ll_msg_bytes.restype = L
-        lib.oracle_ll_dispatch.argtypes = [I, I, I, I, I, I, P, P, I, I, I, P, P, P, P]
-        lib.oracle_ll_combine.argtypes = [I, I, I, I, I, I, P, P, P, P, P, L, P]
-        for name in ("oracle_get_dispatch_layout", "oracle_dispatch_notify", "oracle_dispatch",
-                     "oracle_combine", "oracle_ll_dispatch", "oracle_ll_combine"):
-            getattr(lib, name).restype = I
-        _lib = lib
+        _lib = _bind(ctypes.CDLL(_LIB_PATH))
     return _lib
 
 
@@ -226,8 +247,9 @@ def ll_msg_bytes(hidden: int, use_fp8: bool) -> int:
 
 
 def ll_dispatch(x, topk_idx, num_max_tokens: int, num_experts: int, use_fp8=True,
-                round_scale=False, use_ue8m0=False):
-    """Low-latency dispatch: one message per valid (token, slot), packed per local expert."""
+                round_scale=False, use_ue8m0=False, rank_mask=None):
+    """Low-latency dispatch: one message per valid (token, slot), packed per local expert.
+    rank_mask: optional [R] ints, nonzero = the rank neither sends nor receives."""
     R, T, H = x.shape
     K = topk_idx.shape[2]
     EL = num_experts // R
@@ -240,7 +262,8 @@ def ll_dispatch(x, topk_idx, num_max_tokens: int, num_experts: int, use_fp8=True
     )
     rc = _check(_load().oracle_ll_dispatch(
         R, T, num_max_tokens, H, K, num_experts, _p(_c(x, np.uint16)), _p(_c(topk_idx, np.int64)),
-        int(use_fp8), int(round_scale), int(use_ue8m0), _p(out["msgs_by_slot"]), _p(out["slot_row"]),
+        _p(_c(rank_mask, np.int32)), int(use_fp8), int(round_scale), int(use_ue8m0), _p(out["msgs_by_slot"]),
+        _p(out["slot_row"]),
         _p(out["packed_recv_count"]), _p(out["packed_recv_layout_range"])), "ll_dispatch")
     out["status"] = rc
     return out

@@ -441,14 +441,28 @@ int oracle_combine(int R, int T, int H, int K, int64_t cap, const int32_t* send_
  * The messages are written to msgs_by_slot[s][t][k][:] (indexed by slot;
  * the receive buffer holds the same bytes at [d][j][row]); slot_row gets
  * the row, -1 for masked slots and for rows past the R*maxT capacity.
+ *
+ * Rank masking ([P1] low-latency receive excerpt: a rank that timed out is
+ * marked in mask_buffer, and is_rank_masked skips sends to it): when
+ * rank_mask is non-NULL, a slot whose destination rank d or whose source
+ * rank s has rank_mask != 0 is treated as a masked slot (-1): no message, not
+ * counted, slot_row -1.  Reading: a masked rank neither receives nor sends.
  * ---------------------------------------------------------------------- */
 int64_t oracle_ll_msg_bytes(int H, int use_fp8) {
     return use_fp8 ? 16 + (int64_t)H + 4 * (int64_t)(H / 128) : 16 + 2 * (int64_t)H;
 }
 
+/* The expert of slot i of source s, or -1 when the slot is masked or either rank is masked. */
+static int64_t ll_slot_expert(const int64_t* topk_idx, size_t i, int s, int EL, const int32_t* rank_mask) {
+    int64_t e = topk_idx[i];
+    if (e < 0) return -1;
+    if (rank_mask && (rank_mask[s] != 0 || rank_mask[e / EL] != 0)) return -1;
+    return e;
+}
+
 int oracle_ll_dispatch(int R, int T, int maxT, int H, int K, int E, const uint16_t* x,
-                       const int64_t* topk_idx, int use_fp8, int round_scale, int use_ue8m0,
-                       uint8_t* msgs_by_slot, int32_t* slot_row,
+                       const int64_t* topk_idx, const int32_t* rank_mask, int use_fp8, int round_scale,
+                       int use_ue8m0, uint8_t* msgs_by_slot, int32_t* slot_row,
                        int32_t* packed_recv_count, int64_t* packed_recv_layout_range) {
     if (R <= 0 || T < 0 || T > maxT || H <= 0 || K <= 0 || E <= 0 || E % R != 0) return ORACLE_BAD_ARG;
     if (use_fp8 && H % 128 != 0) return ORACLE_BAD_ARG;
@@ -476,6 +490,8 @@ int oracle_ll_dispatch(int R, int T, int maxT, int H, int K, int E, const uint16
                 int64_t e = topk_idx[((size_t)s * T + t) * K + k];
                 if (e == -1) continue;
                 if (e < 0 || e >= E) { status = ORACLE_BAD_EXPERT; goto done; }
+                e = ll_slot_expert(topk_idx, ((size_t)s * T + t) * K + k, s, EL, rank_mask);
+                if (e < 0) continue;
                 cnt[(size_t)s * E + e] += 1;
             }
     for (int e = 0; e < E; ++e) {
@@ -503,7 +519,7 @@ int oracle_ll_dispatch(int R, int T, int maxT, int H, int K, int E, const uint16
                 size_t slot = ((size_t)s * T + t) * K + k;
                 uint8_t* m = msgs_by_slot + slot * msg;
                 memset(m, 0, (size_t)msg);
-                int64_t e = topk_idx[slot];
+                int64_t e = ll_slot_expert(topk_idx, slot, s, EL, rank_mask);
                 if (e < 0) { slot_row[slot] = -1; continue; }
                 int64_t row = begin[(size_t)e * R + s] + running[e];
                 running[e] += 1;

@@ -222,13 +222,14 @@ LL_CASES = [
 LL_FORMATS = ["bf16", "fp8", "fp8_round", "fp8_ue8m0"]
 
 
-def run_ll(shape, fmt):
+def run_ll(shape, fmt, mask=None, h=None):
     use_fp8 = fmt != "bf16"
     idx, w = W.routing(shape)
     x = W.tokens_x(shape)
     maxT = shape.max_tokens
     cfg = P.config_of(shape, 0)
-    h = ep.Handle(cfg)
+    if h is None:
+        h = ep.Handle(cfg)
     msg = ep.ep_ll_msg_bytes(shape.H, use_fp8)
     msgs = P.Guarded((shape.R, shape.EL, shape.R * maxT, msg), torch.uint8)
     stats = torch.full((shape.R, shape.EL), 3, dtype=torch.int32, device=P.DEV)
@@ -237,8 +238,22 @@ def run_ll(shape, fmt):
                             cumulative_local_expert_recv_stats=stats)
     status = h.status()
     ora = O.ll_dispatch(W.bf16_bits(x), idx, maxT, shape.E, use_fp8=use_fp8, round_scale=fmt == "fp8_round",
-                        use_ue8m0=fmt == "fp8_ue8m0")
+                        use_ue8m0=fmt == "fp8_ue8m0", rank_mask=mask)
     return dict(h=h, idx=idx, w=w, x=x, out=out, ora=ora, msgs=msgs, stats=stats, status=status, msg=msg)
+
+
+def compare_ll(r, shape):
+    ora, out, idx = r["ora"], r["out"], r["idx"]
+    np.testing.assert_array_equal(P.host(out["packed_recv_count"]), ora["packed_recv_count"])
+    np.testing.assert_array_equal(P.host(out["packed_recv_layout_range"]), ora["packed_recv_layout_range"])
+    slot = P.host(r["h"].export("ll_slot_row"))[:, :shape.T]
+    np.testing.assert_array_equal(slot, ora["slot_row"])
+    msgs = P.host(out["recv_msgs"])
+    s_, t_, k_ = np.nonzero(ora["slot_row"] >= 0)
+    e = idx[s_, t_, k_]
+    rows = ora["slot_row"][s_, t_, k_]
+    np.testing.assert_array_equal(msgs[e // shape.EL, e % shape.EL, rows], ora["msgs_by_slot"][s_, t_, k_])
+    r["msgs"].check()
 
 
 @pytest.mark.parametrize("fmt", LL_FORMATS)
@@ -293,3 +308,42 @@ def test_ll_views():
     np.testing.assert_array_equal(P.host(src)[e // shape.EL, e % shape.EL, rows], t_)
     q = P.host(px.contiguous())[e // shape.EL, e % shape.EL, rows]
     np.testing.assert_array_equal(q, r["ora"]["msgs_by_slot"][s_, t_, k_, 16:16 + shape.H])
+
+
+@pytest.mark.parametrize("shape", LL_CASES[:4], ids=lambda s: s.name)
+def test_ll_rank_mask(shape):
+    """A masked rank neither sends nor receives; cleaning the mask restores the full dispatch."""
+    h = ep.Handle(P.config_of(shape, 0))
+    masked_rank = shape.R - 1
+    ep.ep_update_mask_buffer(h, masked_rank, True)
+    mask = np.zeros(shape.R, np.int32)
+    mask[masked_rank] = 1
+    np.testing.assert_array_equal(ep.ep_query_mask_buffer(h).numpy(), mask)
+    r = run_ll(shape, "fp8_ue8m0", mask=mask, h=h)
+    assert r["status"] == 0
+    compare_ll(r, shape)
+    assert (P.host(r["out"]["packed_recv_count"])[masked_rank] == 0).all()
+    # weighted combine skips every masked slot
+    maxT = shape.max_tokens
+    y = W.normal_bf16((shape.R, shape.EL, shape.R * maxT, shape.H), shape.seed, "masky", device=P.DEV)
+    got = ep.ep_ll_combine(h, y, torch.from_numpy(r["idx"]).to(P.DEV), torch.from_numpy(r["w"]).to(P.DEV))
+    want = O.ll_combine(P.host(y), r["idx"], r["w"], r["ora"]["slot_row"], maxT, shape.E)
+    np.testing.assert_array_equal(P.host(got), want)
+    ep.ep_clean_mask_buffer(h)
+    assert (ep.ep_query_mask_buffer(h).numpy() == 0).all()
+    r2 = run_ll(shape, "fp8_ue8m0", h=h)
+    compare_ll(r2, shape)
+
+
+def test_bounded_wait_times_out_and_masks():
+    """A wait on an mbarrier that nothing completes gives up, reports EP_ERR_TIMEOUT and masks the
+    rank; the context stays usable and the next dispatch leaves that rank out."""
+    shape = LL_CASES[1]
+    h = ep.Handle(P.config_of(shape, 0))
+    ep.ep_selftest_bounded_wait(h, 2000, 2)
+    assert h.status() == 3  # EP_ERR_TIMEOUT
+    mask = ep.ep_query_mask_buffer(h).numpy()
+    np.testing.assert_array_equal(mask, [0, 0, 1, 0])
+    r = run_ll(shape, "fp8", mask=mask, h=h)
+    assert r["status"] == 0
+    compare_ll(r, shape)

@@ -41,11 +41,15 @@ def f32_of_bits(b):
 
 # --------------------------------------------------------------------- P1
 
-@pytest.fixture(scope="module")
-def p1():
+def load_p1():
     g = gold("p1_hand_case.json")
     g["idx"] = np.array(g["topk_idx"], np.int64)
     return g
+
+
+@pytest.fixture(scope="module")
+def p1():
+    return load_p1()
 
 
 def test_p1_layout(p1):
@@ -516,3 +520,25 @@ def test_sampled_tokens_match_full():
     cf = O.combine(full["recv_x"], n["send_head"], out_fp32=True, num_topk=shape.K)
     cp = O.combine(full["recv_x"], n["send_head"], out_fp32=True, num_topk=shape.K, tokens=toks)
     np.testing.assert_array_equal(cp["out"].reshape(-1, shape.H)[toks], cf["out"].reshape(-1, shape.H)[toks])
+
+
+@pytest.mark.parametrize("case", CASES[1:6])
+def test_low_latency_rank_mask(case):
+    """Masking a rank equals removing every slot that starts or ends on it (both sides agree)."""
+    shape, idx, w, x = _case(*case, H=512)
+    R, T, E, EL = shape.R, shape.T, shape.E, shape.EL
+    mask = np.zeros(R, np.int32)
+    mask[R // 2] = 1
+    masked = O.ll_dispatch(x, idx, T + 1, E, use_fp8=True, use_ue8m0=True, rank_mask=mask)
+    idx2 = idx.copy()
+    for s in range(R):
+        for t in range(T):
+            for k in range(shape.K):
+                e = idx2[s, t, k]
+                if e >= 0 and (mask[s] or mask[e // EL]):
+                    idx2[s, t, k] = -1
+    plain = O.ll_dispatch(x, idx2, T + 1, E, use_fp8=True, use_ue8m0=True)
+    for key in ("slot_row", "packed_recv_count", "packed_recv_layout_range", "msgs_by_slot"):
+        np.testing.assert_array_equal(masked[key], plain[key], err_msg=key)
+    assert (masked["packed_recv_count"][R // 2] == 0).all()
+    assert (masked["slot_row"][R // 2] == -1).all()
