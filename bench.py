@@ -395,7 +395,8 @@ def run_ours(args):
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "traffic": traffic, "algorithmic_bytes": dom_bytes},
         "cpu_baseline": cpu, "clocks": clocks.summary(), "e2e": e2e,
-        "gpu_launches": 4 * args.steps,  # layout, notify, dispatch, combine "wall_s_timed": round(wall, 3), "ops": ops,
+        "gpu_launches": 4 * args.steps,  # layout, notify, dispatch, combine per step
+        "wall_s_timed": round(wall, 3), "ops": ops,
     }
     if rank == 0:
         print(json.dumps(result), flush=True)
