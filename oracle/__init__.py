@@ -57,13 +57,14 @@ def _bind(lib):
     lib.oracle_fp8_quantize_group.restype = None
     lib.oracle_get_dispatch_layout.argtypes = [I, I, I, I, P, P, P, P, P]
     lib.oracle_dispatch_notify.argtypes = [I, I, I, I, I, L, P, P, P, P, P, P, P, P, P, P]
+    lib.oracle_rdma_prefix.argtypes = [I, I, I, P, P, P]
     lib.oracle_dispatch.argtypes = [I, I, I, I, I, L, I, P, P, P, P, P, P, L, P, P, P, P]
     lib.oracle_combine.argtypes = [I, I, I, I, L, P, P, P, P, P, I, P, L, P, P]
     lib.oracle_ll_msg_bytes.argtypes = [I, I]
     lib.oracle_ll_msg_bytes.restype = L
     lib.oracle_ll_dispatch.argtypes = [I, I, I, I, I, I, P, P, P, I, I, I, P, P, P, P]
     lib.oracle_ll_combine.argtypes = [I, I, I, I, I, I, P, P, P, P, P, L, P]
-    for name in ("oracle_get_dispatch_layout", "oracle_dispatch_notify", "oracle_dispatch",
+    for name in ("oracle_get_dispatch_layout", "oracle_dispatch_notify", "oracle_rdma_prefix", "oracle_dispatch",
                  "oracle_combine", "oracle_ll_dispatch", "oracle_ll_combine"):
         getattr(lib, name).restype = I
     return lib
@@ -188,6 +189,19 @@ def dispatch_notify(num_tokens_per_rank, is_token_in_rank, num_tokens_per_expert
         _p(out["recv_channel_prefix_matrix"]), _p(out["num_recv"]), _p(out["send_head"]),
         _p(out["recv_src_idx"]), _p(out["num_recv_tokens_per_expert"])), "dispatch_notify")
     out["status"] = rc
+    return out
+
+
+def rdma_prefix(is_token_in_rank, num_channels: int):
+    """Node-level record of whole nodes of 8 ranks (R > 8, R % 8 == 0): RDMA channel prefix
+    [R][NN][C] and, per receiving rank, the RDMA rank prefix [R][NN]."""
+    R, T, _ = is_token_in_rank.shape
+    NN = R // 8
+    out = dict(rdma_channel_prefix_matrix=np.zeros((R, NN, num_channels), np.int32),
+               recv_rdma_rank_prefix_sum=np.zeros((R, NN), np.int32))
+    _check(_load().oracle_rdma_prefix(R, T, num_channels, _p(_c(is_token_in_rank, np.uint8)),
+                                      _p(out["rdma_channel_prefix_matrix"]), _p(out["recv_rdma_rank_prefix_sum"])),
+           "rdma_prefix")
     return out
 
 

@@ -300,6 +300,53 @@ int oracle_dispatch_notify(int R, int T, int E, int C, int A, int64_t cap,
 }
 
 /* ------------------------------------------------------------------------
+ * Node-level (RDMA rank) record of a two-level dispatch ([P3] §4.2: the
+ * internode handle adds RDMA channel prefix matrices and RDMA rank prefix
+ * sums; [P1]: 8 NVLink peers per node, the GPUs of a node share one RDMA
+ * rank in normal mode, and the RDMA team is the ranks with the same GPU
+ * index).  Whole nodes only: R > 8 and R % 8 == 0; rank r = 8 n + l is
+ * GPU l of node n, NN = R / 8.
+ *
+ * A token "goes to node n" when it is sent to at least one rank of node n:
+ * source (m, l) moves it once over RDMA, to rank (n, l), which forwards it
+ * over NVLink.  With the channels of oracle_dispatch_notify:
+ *   rdma_channel_prefix[s][n][c] = #t < end(c) of source s that go to node n
+ *                                  (inclusive prefix over channels)
+ *   recv_rdma_rank_prefix[r][m]  = for r = (n, l): #t of the sources (m', l),
+ *                                  m' <= m, that go to node n (inclusive
+ *                                  prefix over source nodes)
+ * The rank-level matrices are those of oracle_dispatch_notify.
+ * ---------------------------------------------------------------------- */
+int oracle_rdma_prefix(int R, int T, int C, const uint8_t* is_token_in_rank,
+                       int32_t* rdma_channel_prefix, int32_t* recv_rdma_rank_prefix) {
+    if (R <= 8 || R % 8 != 0 || T < 0 || C <= 0) return ORACLE_BAD_ARG;
+    const int NN = R / 8;
+    const int chunk = (T + C - 1) / C;
+    for (int s = 0; s < R; ++s)
+        for (int n = 0; n < NN; ++n)
+            for (int c = 0; c < C; ++c) {
+                int end = (c + 1) * chunk < T ? (c + 1) * chunk : T;
+                int32_t count = 0;
+                for (int t = 0; t < end; ++t) {
+                    int goes = 0;
+                    for (int r = 8 * n; r < 8 * n + 8; ++r)
+                        goes |= is_token_in_rank[((size_t)s * T + t) * R + r] != 0;
+                    count += goes;
+                }
+                rdma_channel_prefix[((size_t)s * NN + n) * C + c] = count;
+            }
+    for (int r = 0; r < R; ++r) {
+        const int n = r / 8, l = r % 8;
+        int32_t acc = 0;
+        for (int m = 0; m < NN; ++m) {
+            acc += rdma_channel_prefix[((size_t)(8 * m + l) * NN + n) * C + (C - 1)];
+            recv_rdma_rank_prefix[(size_t)r * NN + m] = acc;
+        }
+    }
+    return ORACLE_OK;
+}
+
+/* ------------------------------------------------------------------------
  * Normal dispatch ([P3] §4.1 intranode_dispatch; §4.4 FP8 input).
  * For every token (s,t) in the list (all tokens when tokens == NULL) and
  * every rank r with row = send_head[s][t][r] in [0, cap):

@@ -41,6 +41,16 @@ MUTATIONS = [
      "int64_t row = begin[(size_t)e * R + s] + (cnt[(size_t)s * E + e] - 1 - running[e]);"),
     ("ll header carries the source rank", "int32_t header[4] = {t, 0, 0, 0};", "int32_t header[4] = {t, s, 0, 0};"),
     ("ll combine ignores the weight", "acc = fmaf(topk_weights[(size_t)g * K + k], v, acc);", "acc = acc + v;"),
+    ("node record with 4 ranks per node", "for (int r = 8 * n; r < 8 * n + 8; ++r)\n                        goes |=",
+     "for (int r = 4 * n; r < 4 * n + 4; ++r)\n                        goes |="),
+    ("node receive prefix from every source of the node",
+     "acc += rdma_channel_prefix[((size_t)(8 * m + l) * NN + n) * C + (C - 1)];",
+     "for (int q = 0; q < 8; ++q) acc += rdma_channel_prefix[((size_t)(8 * m + q) * NN + n) * C + (C - 1)];"),
+    ("node receive prefix from the first channel",
+     "acc += rdma_channel_prefix[((size_t)(8 * m + l) * NN + n) * C + (C - 1)];",
+     "acc += rdma_channel_prefix[((size_t)(8 * m + l) * NN + n) * C + 0];"),
+    ("node receive prefix with node and GPU index swapped", "const int n = r / 8, l = r % 8;",
+     "const int l = r / 8, n = r % 8 % NN;"),
     ("ll mask ignores the source", "if (rank_mask && (rank_mask[s] != 0 || rank_mask[e / EL] != 0)) return -1;",
      "if (rank_mask && rank_mask[e / EL] != 0) return -1;"),
 ]
@@ -70,6 +80,9 @@ def _pin_checks():
         checks.append((f"ll combine {case}", lambda c=case: pins.test_low_latency_combine(c)))
         checks.append((f"ll rank mask {case}", lambda c=case: pins.test_low_latency_rank_mask(c)))
     checks.append(("dispatch fp8 modes", pins.test_dispatch_fp8_modes))
+    checks.append(("two-level hand case", pins.test_two_level_hand_case))
+    for case in pins.TWO_LEVEL_CASES:
+        checks.append((f"two-level {case}", lambda c=case: pins.test_two_level_invariants(c)))
     return checks
 
 

@@ -542,3 +542,67 @@ def test_low_latency_rank_mask(case):
         np.testing.assert_array_equal(masked[key], plain[key], err_msg=key)
     assert (masked["packed_recv_count"][R // 2] == 0).all()
     assert (masked["slot_row"][R // 2] == -1).all()
+
+
+# --------------------------------------------------------------------- two-level (node) record
+
+def _two_level_hand():
+    g = gold("two_level_hand_case.json")
+    R, T = g["R"], g["T"]
+    itr = np.zeros((R, T, R), np.uint8)
+    for s, toks in g["hits"].items():
+        for t, ranks in enumerate(toks):
+            for r in ranks:
+                itr[int(s), t, r] = 1
+    return g, itr
+
+
+def test_two_level_hand_case():
+    g, itr = _two_level_hand()
+    R, C = g["R"], g["C"]
+    out = O.rdma_prefix(itr, C)
+    rcp = np.zeros((R, R // 8, C), np.int32)
+    for s, v in g["rdma_channel_prefix_matrix"].items():
+        rcp[int(s)] = v
+    rrp = np.zeros((R, R // 8), np.int32)
+    for r, v in g["recv_rdma_rank_prefix_sum"].items():
+        rrp[int(r)] = v
+    np.testing.assert_array_equal(out["rdma_channel_prefix_matrix"], rcp)
+    np.testing.assert_array_equal(out["recv_rdma_rank_prefix_sum"], rrp)
+
+
+def test_two_level_needs_whole_nodes():
+    for R in (8, 9, 17):
+        with pytest.raises(ValueError):
+            O.rdma_prefix(np.zeros((R, 2, R), np.uint8), 2)
+
+
+TWO_LEVEL_CASES = [c for c in CASES if c[0] > 8 and c[0] % 8 == 0] + [
+    (24, 40, 48, 3, "zipf", 0.1, 5, 1), (32, 20, 64, 4, "uniform", 0.0, 12, 1), (16, 0, 32, 2, "uniform", 0.0, 3, 1),
+    (16, 30, 32, 4, "uniform", 1.0, 4, 1)]
+
+
+@pytest.mark.parametrize("case", TWO_LEVEL_CASES)
+def test_two_level_invariants(case):
+    shape, idx, w, x = _case(*case)
+    R, T, C = shape.R, shape.T, shape.C
+    lay = O.get_dispatch_layout(idx, shape.E)
+    out = O.rdma_prefix(lay["is_token_in_rank"], C)
+    rcp, rrp = out["rdma_channel_prefix_matrix"], out["recv_rdma_rank_prefix_sum"]
+    NN = R // 8
+    # last channel = the layout's per-node token counts; prefixes never decrease
+    np.testing.assert_array_equal(rcp[:, :, -1], lay["num_tokens_per_rdma_rank"])
+    assert (np.diff(rcp, axis=2) >= 0).all() and (np.diff(rrp, axis=1) >= 0).all()
+    # channel bins by an independent formulation: node hit per token, cumulative count at each channel end
+    node_hit = lay["is_token_in_rank"].reshape(R, T, NN, 8).any(axis=3)
+    chunk = -(-T // C) if T else 0
+    ends = [min(T, (c + 1) * chunk) for c in range(C)]
+    csum = np.concatenate([np.zeros((R, 1, NN), np.int64), np.cumsum(node_hit, axis=1)], axis=1)
+    np.testing.assert_array_equal(rcp, np.stack([csum[:, e, :] for e in ends], axis=2))
+    # rank (n, l) receives from the sources (m, l): per node, its 8 receivers together get every token
+    # that reaches the node exactly once, and each receiver's total is a column of the layout counts
+    tprdma = lay["num_tokens_per_rdma_rank"]
+    for n in range(NN):
+        np.testing.assert_array_equal(rrp[8 * n:8 * n + 8, -1].sum(), tprdma[:, n].sum())
+        for l in range(8):
+            np.testing.assert_array_equal(rrp[8 * n + l], np.cumsum(tprdma[l::8, n]))
