@@ -81,24 +81,28 @@ def load_peaks():
     return 6800.0, "fallback"
 
 
-def source_digest():
+KERNEL_SOURCES = ("ep_common.cuh", "ep_dispatch.cu")  # where the dispatch and combine kernels live
+
+
+def source_digest(names=None):
+    """Hash of the kernel sources (all of csrc/ when names is None)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "combine_get_dispatch_03_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    for name in sorted(names or os.listdir(csrc)):
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
 
 
 def recorded_traffic(kernel):
-    """DRAM bytes per launch from a committed ncu summary, if taken on the current kernel sources."""
+    """DRAM bytes per launch from a committed ncu summary, if taken on the kernel's current sources."""
     path = os.path.join(ROOT, "profiles", "traffic_per_launch.txt")
     if not os.path.exists(path):
         return None
     with open(path) as f:
         rec = json.load(f)
     ent = rec.get(kernel)
-    if not ent or ent.get("source_digest") != source_digest():
+    if not ent or ent.get("source_digest") != source_digest(ent.get("sources")):
         return None
     return ent.get("dram_bytes_per_launch")
 
@@ -512,25 +516,46 @@ def measure_other_ops(ep, dev, peak, reps=10):
     del msgs, y, out
     torch.cuda.empty_cache()
 
-    # the small case (L2-resident)
+    # the small case (L2-resident, launch-bound): eager calls and one CUDA graph of the step
     shape = W.WORKLOADS["normal_small"]
     st = prepare_normal(ep, shape, dev)
     h = st["h"]
-    lay = ep.ep_get_dispatch_layout(h, st["idx_d"])
+    R, T, H, E, K, cap = shape.R, shape.T, shape.H, shape.E, shape.K, st["cap"]
+    lay = dict(num_tokens_per_rank=torch.empty((R, R), dtype=torch.int32, device=dev), num_tokens_per_rdma_rank=None,
+               num_tokens_per_expert=torch.empty((R, E), dtype=torch.int32, device=dev),
+               is_token_in_rank=torch.empty((R, T, R), dtype=torch.bool, device=dev))
+    bufs = dict(recv_x=torch.empty((R, cap, H), dtype=torch.bfloat16, device=dev),
+                recv_topk_idx=torch.empty((R, cap, K), dtype=torch.int64, device=dev),
+                recv_topk_weights=torch.empty((R, cap, K), dtype=torch.float32, device=dev),
+                num_recv_tokens_per_expert=torch.empty((R, shape.EL), dtype=torch.int32, device=dev))
+    out = torch.empty((R, T, H), dtype=torch.bfloat16, device=dev)
+    cw = torch.empty((R, T, K), dtype=torch.float32, device=dev)
 
     def small_step():
-        l2 = ep.ep_get_dispatch_layout(h, st["idx_d"])
-        d2 = ep.ep_dispatch(h, st["x_d"], topk_idx=st["idx_d"], topk_weights=st["w_d"],
-                            num_tokens_per_rank=l2["num_tokens_per_rank"], is_token_in_rank=l2["is_token_in_rank"],
-                            num_tokens_per_expert=l2["num_tokens_per_expert"])
-        ep.ep_combine(h, d2["recv_x"], topk_weights=d2["recv_topk_weights"])
+        ep.ep_get_dispatch_layout(h, st["idx_d"], **lay)
+        ep.ep_dispatch(h, st["x_d"], topk_idx=st["idx_d"], topk_weights=st["w_d"],
+                       num_tokens_per_rank=lay["num_tokens_per_rank"], is_token_in_rank=lay["is_token_in_rank"],
+                       num_tokens_per_expert=lay["num_tokens_per_expert"], **bufs)
+        ep.ep_combine(h, bufs["recv_x"], topk_weights=bufs["recv_topk_weights"], combined_x=out,
+                      combined_topk_weights=cw)
 
     ms = timed(small_step, reps, stream)
     h.check()
-    b = normal_bytes(shape.R, shape.T, shape.H, shape.K, st["hits"])
+    b = normal_bytes(R, T, H, K, st["hits"])
     step_b = {"payload": b["dispatch"]["payload"] + b["combine"]["payload"],
               "meta": sum(v["meta"] for v in b.values())}
-    report("normal_small.step", ms, step_b, {"note": "L2-resident; outputs allocated by torch in each call"})
+    report("normal_small.step", ms, step_b, {"note": "L2-resident; eager calls, launch-bound"})
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        small_step()
+    stream.wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        small_step()
+    ms = timed(graph.replay, reps, stream)
+    h.check()
+    report("normal_small.step_graph", ms, step_b, {"note": "the same step captured once in a CUDA graph"})
     h.destroy()
     return res
 

@@ -3,7 +3,9 @@
 // The handle plays the role of the Buffer object of the pages ("第 4 章 V1：
 // 布局、dispatch 与 combine" §4.1-§4.3): it fixes the sizes, owns the device
 // arrays of the dispatch record (rank / channel prefix matrices,
-// recv_src_idx, send_head; the low-latency slot map) and the status word that
+// recv_src_idx, send_head; with two or more whole nodes of 8 ranks the
+// node-level prefix matrices of the two-level layout; the low-latency slot
+// map) and the status word that
 // kernels use to report errors without trapping.
 #include <cstdarg>
 #include <cstdio>
@@ -34,6 +36,8 @@ struct ep_handle {
     int32_t* ll_slot = nullptr;              // [R][maxT][K]
     int32_t* ll_cnt = nullptr;               // [R][E]
     int32_t* rank_mask = nullptr;            // [R], nonzero = masked
+    int32_t* rdma_channel_prefix = nullptr;    // [R][NN][C], NN = R / 8 whole nodes (see has_nodes)
+    int32_t* recv_rdma_rank_prefix = nullptr;  // [R][NN]
     int normal_tokens = -1;                  // T of the current dispatch record, -1 = none
     bool prepared = false;                   // record built by ep_notify_dispatch, not yet used
     int ll_tokens = -1;                      // T of the last LL dispatch, -1 = none
@@ -55,6 +59,15 @@ ep_status fail(ep_status code, const char* fmt, ...) {
 
 ep_status cuda_fail(cudaError_t err, const char* what) {
     return fail(EP_ERR_CUDA, "%s: %s", what, cudaGetErrorString(err));
+}
+
+// Two or more whole nodes of 8 ranks: the handle keeps the node-level record.
+bool has_nodes(const ep_config& c) { return c.num_ranks > 8 && c.num_ranks % 8 == 0; }
+
+// The node-level arrays the notify fills (0: channel prefix, 1: receive prefix), NULL without whole nodes.
+int32_t* node_record(const ep_handle* h, int which) {
+    if (!has_nodes(h->cfg)) return nullptr;
+    return which == 0 ? h->rdma_channel_prefix : h->recv_rdma_rank_prefix;
 }
 
 #define EP_CHECK_ARG(cond, ...)                                  \
@@ -172,10 +185,12 @@ ep_status ep_handle_create(const ep_config* cfg, ep_handle** out) {
 
     const size_t R = cfg->num_ranks, C = cfg->num_channels, T = cfg->num_max_tokens, K = cfg->num_topk;
     const size_t E = cfg->num_experts, cap = static_cast<size_t>(cfg->recv_capacity);
-    const size_t sizes[] = {1, R * R, R * R * C, R * R * C, R, R * cap, R * T * R, R * T * K, R * E, R};
+    const size_t NN = (R + 7) / 8;
+    const size_t sizes[] = {1, R * R, R * R * C, R * R * C, R, R * cap, R * T * R, R * T * K, R * E, R,
+                            R * NN * C, R * NN};
     int32_t** slots[] = {&h->status,   &h->rank_prefix,  &h->channel_prefix, &h->recv_channel_prefix,
                          &h->num_recv, &h->recv_src_idx, &h->send_head,      &h->ll_slot,
-                         &h->ll_cnt,   &h->rank_mask};
+                         &h->ll_cnt,   &h->rank_mask,    &h->rdma_channel_prefix, &h->recv_rdma_rank_prefix};
     size_t total = 0;
     for (size_t s : sizes) total += align_up(s * sizeof(int32_t), 256);
     err = cudaMalloc(&h->dmem, total);
@@ -246,6 +261,8 @@ size_t ep_handle_field_bytes(const ep_handle* h, ep_handle_field field) {
         case EP_FIELD_SEND_HEAD: return sizeof(int32_t) * R * T * R;
         case EP_FIELD_NUM_RECV: return sizeof(int32_t) * R;
         case EP_FIELD_LL_SLOT_ROW: return sizeof(int32_t) * R * T * K;
+        case EP_FIELD_RDMA_CHANNEL_PREFIX_MATRIX: return has_nodes(h->cfg) ? sizeof(int32_t) * R * (R / 8) * C : 0;
+        case EP_FIELD_RECV_RDMA_RANK_PREFIX_SUM: return has_nodes(h->cfg) ? sizeof(int32_t) * R * (R / 8) : 0;
     }
     return 0;
 }
@@ -253,6 +270,12 @@ size_t ep_handle_field_bytes(const ep_handle* h, ep_handle_field field) {
 ep_status ep_handle_export(const ep_handle* h, ep_handle_field field, void* dst, size_t bytes,
                            ep_stream_t stream) {
     if (h == nullptr || dst == nullptr) return fail(EP_ERR_INVALID_ARG, "NULL argument");
+    const bool node_field =
+        field == EP_FIELD_RDMA_CHANNEL_PREFIX_MATRIX || field == EP_FIELD_RECV_RDMA_RANK_PREFIX_SUM;
+    if (node_field && !has_nodes(h->cfg))
+        return fail(EP_ERR_UNSUPPORTED,
+                    "the node-level record needs two or more whole nodes of 8 ranks (handle has %d ranks)",
+                    h->cfg.num_ranks);
     const size_t need = ep_handle_field_bytes(h, field);
     if (need == 0 && field != EP_FIELD_RECV_SRC_IDX && field != EP_FIELD_SEND_HEAD && field != EP_FIELD_LL_SLOT_ROW)
         return fail(EP_ERR_INVALID_ARG, "unknown field %d", static_cast<int>(field));
@@ -266,6 +289,8 @@ ep_status ep_handle_export(const ep_handle* h, ep_handle_field field, void* dst,
         case EP_FIELD_SEND_HEAD: src = h->send_head; break;
         case EP_FIELD_NUM_RECV: src = h->num_recv; break;
         case EP_FIELD_LL_SLOT_ROW: src = h->ll_slot; break;
+        case EP_FIELD_RDMA_CHANNEL_PREFIX_MATRIX: src = h->rdma_channel_prefix; break;
+        case EP_FIELD_RECV_RDMA_RANK_PREFIX_SUM: src = h->recv_rdma_rank_prefix; break;
         default: return fail(EP_ERR_INVALID_ARG, "unknown field %d", static_cast<int>(field));
     }
     if (need == 0) return EP_OK;
@@ -370,7 +395,8 @@ ep_status ep_dispatch(ep_handle* h, int32_t num_tokens, const void* x, ep_dtype 
                                          c.recv_capacity, num_tokens_per_rank, is_token_in_rank,
                                          num_tokens_per_expert, h->rank_prefix, h->channel_prefix,
                                          h->recv_channel_prefix, h->num_recv, h->send_head, h->recv_src_idx,
-                                         num_recv_tokens_per_expert, h->status, stream);
+                                         num_recv_tokens_per_expert, node_record(h, 0), node_record(h, 1),
+                                         h->status, stream);
         if (err != cudaSuccess) return cuda_fail(err, "dispatch_notify launch");
         h->normal_tokens = num_tokens;
     }
@@ -401,8 +427,8 @@ ep_status ep_notify_dispatch(ep_handle* h, int32_t num_tokens, const int32_t* nu
     cudaError_t err = ep::launch_dispatch_notify(
         c.num_ranks, num_tokens, c.num_experts, c.num_channels, c.expert_alignment, c.recv_capacity,
         num_tokens_per_rank, is_token_in_rank, num_tokens_per_expert, h->rank_prefix, h->channel_prefix,
-        h->recv_channel_prefix, h->num_recv, h->send_head, h->recv_src_idx, num_recv_tokens_per_expert, h->status,
-        stream);
+        h->recv_channel_prefix, h->num_recv, h->send_head, h->recv_src_idx, num_recv_tokens_per_expert,
+        node_record(h, 0), node_record(h, 1), h->status, stream);
     if (err != cudaSuccess) return cuda_fail(err, "dispatch_notify launch");
     h->normal_tokens = num_tokens;
     h->prepared = true;

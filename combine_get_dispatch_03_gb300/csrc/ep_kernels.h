@@ -40,7 +40,8 @@ cudaError_t launch_dispatch_notify(int R, int T, int E, int C, int A, int64_t ca
                                    const uint8_t* itr, const int32_t* tpe, int32_t* rank_prefix,
                                    int32_t* channel_prefix, int32_t* recv_channel_prefix, int32_t* num_recv,
                                    int32_t* send_head, int32_t* recv_src_idx, int32_t* num_recv_per_expert,
-                                   int32_t* status, cudaStream_t stream);
+                                   int32_t* rdma_channel_prefix, int32_t* recv_rdma_rank_prefix, int32_t* status,
+                                   cudaStream_t stream);
 
 cudaError_t launch_dispatch(const LaunchPlan& plan, int mode, int R, int T, int H, int K, int EL, int64_t cap,
                             const void* x, const float* x_scales, const int64_t* topk_idx,

@@ -5,7 +5,15 @@
 // is_token_in_rank mask.  dispatch_notify (same section, the handle's prefix
 // matrices, recv_src_idx and send_head): every hit (s, t, r) gets its receive
 // row, ordered by source rank then token, with channel prefix matrices at
-// the boundaries of C contiguous token ranges.
+// the boundaries of C contiguous token ranges.  When the ranks form two or
+// more whole nodes of 8 (the two-level layout of §4.2 of the same page; rank
+// r = 8 n + l is GPU l of node n) the notify also builds the node-level
+// record: per source and node, the tokens that reach any rank of the node at
+// every channel end; per rank (n, l), the inclusive prefix over source nodes
+// m of the tokens of source (m, l) that reach node n -- the tokens (n, l)
+// receives over RDMA, since the GPUs of a node share one RDMA rank and the
+// RDMA team is the ranks with the same GPU index ("DeepEP Normal vs
+// Low-Latency 双模式深度分析").
 //
 // Both kernels give each source rank one thread-block cluster of kClusterCtas
 // CTAs; CTA q of the cluster owns the q-th contiguous slice of that rank's
@@ -27,6 +35,9 @@ constexpr int kClusterCtas = 8;      // CTAs per source rank (portable cluster s
 constexpr int kLayoutRound = 2048;   // tokens of one round of the layout kernel (mask staging in smem)
 constexpr int kLayoutUnroll = 8;     // top-k entries in flight per thread
 constexpr int kNotifyWarps = kNotifyThreads / kWarpSize;
+constexpr int kRanksPerNode = 8;     // NVLink peers of one node
+constexpr int kMaxNodes = kMaxRanks / kRanksPerNode;
+constexpr int kMaxColumns = kMaxRanks + kMaxNodes;  // notify count columns: ranks, then nodes
 
 // Mask of destination ranks of one token from its R-byte is_token_in_rank row.
 __device__ __forceinline__ uint32_t load_rank_mask(const uint8_t* row, int R) {
@@ -58,6 +69,12 @@ __device__ __forceinline__ void store_rank_mask(uint8_t* row, int R, uint32_t m)
     } else {
         for (int r = 0; r < R; ++r) row[r] = static_cast<uint8_t>((m >> r) & 1u);
     }
+}
+
+// Column col of a token's hits: rank col for col < R, else whether any rank of node col - R is hit.
+__device__ __forceinline__ bool column_bit(uint32_t m, int col, int R) {
+    return col < R ? ((m >> col) & 1u) != 0u
+                   : ((m >> (kRanksPerNode * (col - R))) & ((1u << kRanksPerNode) - 1u)) != 0u;
 }
 
 // Token slice [lo, hi) of CTA q of a cluster over T tokens.
@@ -159,22 +176,26 @@ __global__ void __launch_bounds__(kLayoutThreads)
 }
 
 // grid (kClusterCtas, R + 1), cluster (kClusterCtas, 1, 1).  Cluster s < R: the
-// rows of source s.  Cluster R: rank_prefix_matrix, num_recv and the aligned
-// per-expert receive counts.
+// rows of source s, and with NN > 0 node columns its row of the node-level
+// channel prefix matrix.  Cluster R: rank_prefix_matrix, num_recv and the
+// aligned per-expert receive counts.  Counts are kept per column: R rank
+// columns, then NN node columns (0 when there is no node-level record).
 __global__ void __launch_bounds__(kNotifyThreads)
-    dispatch_notify_kernel(int R, int T, int E, int C, int A, int64_t cap, const int32_t* __restrict__ tpr,
-                           const uint8_t* __restrict__ itr, const int32_t* __restrict__ tpe,
-                           int32_t* __restrict__ rank_prefix, int32_t* __restrict__ channel_prefix,
-                           int32_t* __restrict__ recv_channel_prefix, int32_t* __restrict__ num_recv,
+    dispatch_notify_kernel(int R, int NN, int T, int E, int C, int A, int64_t cap,
+                           const int32_t* __restrict__ tpr, const uint8_t* __restrict__ itr,
+                           const int32_t* __restrict__ tpe, int32_t* __restrict__ rank_prefix,
+                           int32_t* __restrict__ channel_prefix, int32_t* __restrict__ recv_channel_prefix,
+                           int32_t* __restrict__ rdma_channel_prefix, int32_t* __restrict__ num_recv,
                            int32_t* __restrict__ send_head, int32_t* __restrict__ recv_src_idx,
                            int32_t* __restrict__ num_recv_per_expert, int32_t* status) {
     pdl_enter();
-    __shared__ int32_t s_cnt[kMaxRanks];                 // hits of this CTA's slice, per rank
-    __shared__ int32_t s_base[kMaxRanks];                // rows taken by earlier sources
-    __shared__ int32_t s_before[kMaxRanks];              // hits of this source before the current round
-    __shared__ int32_t s_warp[kMaxRanks][kNotifyWarps];  // per-warp counts -> exclusive prefixes
-    __shared__ int32_t s_total[kMaxRanks];               // hits of the current round
+    __shared__ int32_t s_cnt[kMaxColumns];                 // hits of this CTA's slice, per column
+    __shared__ int32_t s_base[kMaxRanks];                  // rows taken by earlier sources
+    __shared__ int32_t s_before[kMaxColumns];              // hits of this source before the current round
+    __shared__ int32_t s_warp[kMaxColumns][kNotifyWarps];  // per-warp counts -> exclusive prefixes
+    __shared__ int32_t s_total[kMaxColumns];               // hits of the current round
     static_assert(kNotifyWarps == kWarpSize, "the column scan gives one lane per warp");
+    static_assert(kMaxColumns <= kNotifyThreads, "one thread per column");
 
     cg::cluster_group cluster = cg::this_cluster();
     const int q = static_cast<int>(cluster.block_rank());
@@ -182,6 +203,7 @@ __global__ void __launch_bounds__(kNotifyThreads)
     const int tid = threadIdx.x;
     const int lane = lane_id();
     const int warp = tid / kWarpSize;
+    const int NC = R + NN;
 
     if (s == R) {
         const int per = kNotifyThreads * kClusterCtas;
@@ -206,30 +228,32 @@ __global__ void __launch_bounds__(kNotifyThreads)
     cluster_slice(T, q, lo, hi);
     const uint8_t* itr_s = itr + static_cast<int64_t>(s) * T * R;
     int32_t* head_s = send_head + static_cast<int64_t>(s) * T * R;
-    if (tid < kMaxRanks) s_cnt[tid] = 0;
+    if (tid < kMaxColumns) s_cnt[tid] = 0;
     __syncthreads();
 
-    // Pass 1: hits of this slice per destination rank.
+    // Pass 1: hits of this slice per column.
     for (int t0 = lo; t0 < hi; t0 += kNotifyThreads) {
         const int t = t0 + tid;
         const uint32_t m = t < hi ? load_rank_mask(itr_s + static_cast<int64_t>(t) * R, R) : 0u;
-        for (int r = 0; r < R; ++r) {
-            const unsigned b = __ballot_sync(kFullMask, (m >> r) & 1u);
-            if (lane == 0 && b) atomicAdd(&s_cnt[r], __popc(b));
+        for (int col = 0; col < NC; ++col) {
+            const unsigned b = __ballot_sync(kFullMask, column_bit(m, col, R));
+            if (lane == 0 && b) atomicAdd(&s_cnt[col], __popc(b));
         }
     }
     cluster.sync();
-    // Rows before this slice: earlier sources (from the counts) and earlier slices of this source.
+    // Hits before this slice: earlier slices of this source; rows before it also count earlier sources.
+    if (tid < NC) {
+        int32_t before = 0;
+        for (int p = 0; p < q; ++p) before += cluster.map_shared_rank(s_cnt, p)[tid];
+        s_before[tid] = before;
+    }
     if (tid < R) {
         int32_t base = 0;
         for (int sp = 0; sp < s; ++sp) base += __ldg(tpr + sp * R + tid);
-        int32_t before = 0;
-        for (int p = 0; p < q; ++p) before += cluster.map_shared_rank(s_cnt, p)[tid];
         s_base[tid] = base;
-        s_before[tid] = before;
         if (q == kClusterCtas - 1) {
             // this slice ends the source: the per-source total must match the counts
-            const int32_t total = before + s_cnt[tid];
+            const int32_t total = s_before[tid] + s_cnt[tid];
             if (total != __ldg(tpr + s * R + tid)) report(status, EP_ERR_INCONSISTENT);
         }
     }
@@ -241,21 +265,22 @@ __global__ void __launch_bounds__(kNotifyThreads)
         const int t = t0 + tid;
         const bool live = t < hi;
         const uint32_t m = live ? load_rank_mask(itr_s + static_cast<int64_t>(t) * R, R) : 0u;
-        for (int r = 0; r < R; ++r) {
-            const unsigned b = __ballot_sync(kFullMask, (m >> r) & 1u);
-            if (lane == 0) s_warp[r][warp] = __popc(b);
+        for (int col = 0; col < NC; ++col) {
+            const unsigned b = __ballot_sync(kFullMask, column_bit(m, col, R));
+            if (lane == 0) s_warp[col][warp] = __popc(b);
         }
         __syncthreads();
-        if (warp < R) {  // warp r: exclusive prefix over the warps of this round, column r
-            const int32_t v = s_warp[warp][lane];
+        // warp w scans columns w, w + 32, ...: exclusive prefix over the warps of this round
+        for (int col = warp; col < NC; col += kNotifyWarps) {
+            const int32_t v = s_warp[col][lane];
             int32_t incl = v;
 #pragma unroll
             for (int off = 1; off < kWarpSize; off <<= 1) {
                 const int32_t o = __shfl_up_sync(kFullMask, incl, off);
                 if (lane >= off) incl += o;
             }
-            s_warp[warp][lane] = s_before[warp] + incl - v;
-            if (lane == kWarpSize - 1) s_total[warp] = incl;
+            s_warp[col][lane] = s_before[col] + incl - v;
+            if (lane == kWarpSize - 1) s_total[col] = incl;
         }
         __syncthreads();
         int32_t rows[kMaxRanks];
@@ -271,6 +296,12 @@ __global__ void __launch_bounds__(kNotifyThreads)
                 recv_channel_prefix[(static_cast<int64_t>(r) * R + s) * C + c] = s_base[r] + excl;
                 if (c > 0) channel_prefix[(static_cast<int64_t>(s) * R + r) * C + c - 1] = excl;
             }
+        }
+        for (int n = 0; n < NN; ++n) {  // node columns: tokens of s that reach node n, before t
+            const unsigned b = __ballot_sync(kFullMask, column_bit(m, R + n, R));
+            if (live && t > 0 && (t % chunk) == 0)
+                rdma_channel_prefix[(static_cast<int64_t>(s) * NN + n) * C + t / chunk - 1] =
+                    s_warp[R + n][warp] + __popc(b & lt);
         }
         if (live) {
             int32_t* dst = head_s + static_cast<int64_t>(t) * R;
@@ -295,7 +326,7 @@ __global__ void __launch_bounds__(kNotifyThreads)
         }
         // the next round starts after this round's hits
         __syncthreads();
-        if (tid < R) s_before[tid] += s_total[tid];
+        if (tid < NC) s_before[tid] += s_total[tid];
         __syncthreads();
     }
 
@@ -310,6 +341,29 @@ __global__ void __launch_bounds__(kNotifyThreads)
             if (start == T) recv_channel_prefix[(static_cast<int64_t>(r) * R + s) * C + c] = s_base[r] + total;
         }
     }
+    if (q == kClusterCtas - 1 && tid >= R && tid < NC) {
+        const int n = tid - R;  // s_before now holds the source's whole count for the column
+        for (int c = 0; c < C; ++c)
+            if (min(static_cast<int64_t>(T), static_cast<int64_t>(c + 1) * chunk) == T)
+                rdma_channel_prefix[(static_cast<int64_t>(s) * NN + n) * C + c] = s_before[tid];
+    }
+}
+
+// One CTA, after the notify, R = 8 NN: recv_rdma_rank_prefix[r][m] for r = (n, l)
+// = sum over m' <= m of the last channel of the node-level channel prefix
+// matrix of source (m', l) towards node n.
+__global__ void __launch_bounds__(kMaxRanks * kMaxNodes)
+    node_prefix_kernel(int R, int NN, int C, const int32_t* __restrict__ rdma_channel_prefix,
+                       int32_t* __restrict__ recv_rdma_rank_prefix) {
+    pdl_enter();
+    const int i = threadIdx.x;
+    if (i >= R * NN) return;
+    const int r = i / NN, m = i % NN;
+    const int n = r / kRanksPerNode, l = r % kRanksPerNode;
+    int32_t acc = 0;
+    for (int mp = 0; mp <= m; ++mp)
+        acc += rdma_channel_prefix[(static_cast<int64_t>(kRanksPerNode * mp + l) * NN + n) * C + C - 1];
+    recv_rdma_rank_prefix[i] = acc;
 }
 
 }  // namespace
@@ -326,10 +380,18 @@ cudaError_t launch_dispatch_notify(int R, int T, int E, int C, int A, int64_t ca
                                    const uint8_t* itr, const int32_t* tpe, int32_t* rank_prefix,
                                    int32_t* channel_prefix, int32_t* recv_channel_prefix, int32_t* num_recv,
                                    int32_t* send_head, int32_t* recv_src_idx, int32_t* num_recv_per_expert,
-                                   int32_t* status, cudaStream_t stream) {
-    return launch_kernel(dispatch_notify_kernel, dim3(kClusterCtas, R + 1, 1), dim3(kNotifyThreads, 1, 1), 0, stream,
-                         kClusterCtas, R, T, E, C, A, cap, tpr, itr, tpe, rank_prefix, channel_prefix,
-                         recv_channel_prefix, num_recv, send_head, recv_src_idx, num_recv_per_expert, status);
+                                   int32_t* rdma_channel_prefix, int32_t* recv_rdma_rank_prefix, int32_t* status,
+                                   cudaStream_t stream) {
+    const bool nodes = rdma_channel_prefix != nullptr && recv_rdma_rank_prefix != nullptr;
+    if (nodes && (R <= kRanksPerNode || R % kRanksPerNode != 0)) return cudaErrorInvalidValue;
+    const int NN = nodes ? R / kRanksPerNode : 0;
+    cudaError_t err = launch_kernel(dispatch_notify_kernel, dim3(kClusterCtas, R + 1, 1), dim3(kNotifyThreads, 1, 1),
+                                    0, stream, kClusterCtas, R, NN, T, E, C, A, cap, tpr, itr, tpe, rank_prefix,
+                                    channel_prefix, recv_channel_prefix, rdma_channel_prefix, num_recv, send_head,
+                                    recv_src_idx, num_recv_per_expert, status);
+    if (err != cudaSuccess || !nodes) return err;
+    return launch_kernel(node_prefix_kernel, dim3(1, 1, 1), dim3(kMaxRanks * kMaxNodes, 1, 1), 0, stream, 1, R, NN, C,
+                         static_cast<const int32_t*>(rdma_channel_prefix), recv_rdma_rank_prefix);
 }
 
 }  // namespace ep

@@ -24,7 +24,8 @@ STATUS_NAMES = {0: "EP_OK", 1: "EP_ERR_INVALID_ARG", 2: "EP_ERR_CAPACITY", 3: "E
 EP_BF16, EP_FP8_E4M3, EP_FP32 = 0, 1, 2
 EP_DISPATCH_FRESH, EP_DISPATCH_CACHED, EP_DISPATCH_PREPARED = 0, 1, 2
 FIELDS = {"rank_prefix_matrix": 0, "channel_prefix_matrix": 1, "recv_channel_prefix_matrix": 2,
-          "recv_src_idx": 3, "send_head": 4, "num_recv": 5, "ll_slot_row": 6}
+          "recv_src_idx": 3, "send_head": 4, "num_recv": 5, "ll_slot_row": 6,
+          "rdma_channel_prefix_matrix": 7, "recv_rdma_rank_prefix_sum": 8}
 
 
 class EPError(RuntimeError):
@@ -145,6 +146,11 @@ class Config:
     recv_capacity: int = 0
 
     @property
+    def num_nodes(self) -> int:
+        """Nodes of 8 ranks in the two-level layout."""
+        return (self.num_ranks + 7) // 8
+
+    @property
     def num_local_experts(self) -> int:
         return self.num_experts // self.num_ranks
 
@@ -209,9 +215,13 @@ class Handle:
                   "recv_src_idx": (c.num_ranks, c.recv_capacity),
                   "send_head": (c.num_ranks, c.num_max_tokens, c.num_ranks),
                   "num_recv": (c.num_ranks,),
-                  "ll_slot_row": (c.num_ranks, c.num_max_tokens, c.num_topk)}
+                  "ll_slot_row": (c.num_ranks, c.num_max_tokens, c.num_topk),
+                  "rdma_channel_prefix_matrix": (c.num_ranks, c.num_nodes, c.num_channels),
+                  "recv_rdma_rank_prefix_sum": (c.num_ranks, c.num_nodes)}
         out = torch.empty(shapes[field], dtype=torch.int32, device=self.device)
         nbytes = lib().ep_handle_field_bytes(self.ptr, FIELDS[field])
+        if field.startswith(("rdma_", "recv_rdma_")) and nbytes == 0:
+            nbytes = out.numel() * 4  # the call below reports that the record needs whole nodes
         assert nbytes == out.numel() * 4
         if nbytes:
             _raise(lib().ep_handle_export(self.ptr, FIELDS[field], ctypes.c_void_p(out.data_ptr()), nbytes,

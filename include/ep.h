@@ -91,7 +91,18 @@ typedef enum ep_handle_field {
     EP_FIELD_RECV_SRC_IDX = 3,               /* int32 [R][cap]                                */
     EP_FIELD_SEND_HEAD = 4,                  /* int32 [R][maxT][R] (first T*R*... rows valid) */
     EP_FIELD_NUM_RECV = 5,                   /* int32 [R]                                     */
-    EP_FIELD_LL_SLOT_ROW = 6                 /* int32 [R][maxT][K]                            */
+    EP_FIELD_LL_SLOT_ROW = 6,                /* int32 [R][maxT][K]                            */
+    /* The node-level record of the two-level layout ("第 4 章 V1：布局、dispatch 与
+     * combine" §4.2, the internode handle), kept when the ranks form two or more
+     * whole nodes of 8 (R > 8, R % 8 == 0): rank r = 8n + l is GPU l of node n,
+     * NN = R / 8.  The GPUs of a node share one RDMA rank and the RDMA team is
+     * the ranks with the same GPU index ("DeepEP Normal vs Low-Latency 双模式深度
+     * 分析"), so rank (n, l) receives over RDMA the tokens of the sources (m, l)
+     * that reach node n.  Exporting either otherwise is EP_ERR_UNSUPPORTED. */
+    EP_FIELD_RDMA_CHANNEL_PREFIX_MATRIX = 7, /* int32 [R][NN][C]: [s][n][c] = tokens t < end of
+                                                channel c of source s that reach any rank of node n */
+    EP_FIELD_RECV_RDMA_RANK_PREFIX_SUM = 8   /* int32 [R][NN]: [r][m], r = (n, l) = tokens of the
+                                                sources (m', l), m' <= m, that reach node n      */
 } ep_handle_field;
 
 /* ------------------------------------------------------------------ handle */
@@ -176,6 +187,10 @@ ep_status ep_notify_dispatch(ep_handle* h, int32_t num_tokens, const int32_t* nu
  *   recv_channel_prefix_matrix[r][s][c] = first row of that channel in r
  *   num_recv_tokens_per_expert[r][j] (int32 [R][EL], output) = received
  *     top-k slots of local expert j, rounded up to expert_alignment
+ *   with two or more whole nodes of 8 ranks ([P3] §4.2, the two-level
+ *     layout), the node-level record as well (EP_FIELD_RDMA_CHANNEL_PREFIX_MATRIX,
+ *     EP_FIELD_RECV_RDMA_RANK_PREFIX_SUM): a token counts once per node it
+ *     reaches, whatever the number of that node's ranks
  * Cached mode (EP_DISPATCH_CACHED): reuses the record of the last fresh or
  * prepared dispatch on this handle with the same num_tokens; topk_idx,
  * topk_weights, the three layout inputs, recv_topk_* and
