@@ -17,7 +17,7 @@ struct LaunchPlan {
     int ll_combine_blocks = 0;
     int bulk_stages[3] = {0, 0, 0};      // bulk-copy dispatch: stages per CTA (0 = not usable)
     unsigned bulk_smem[3] = {0, 0, 0};   // its dynamic shared memory
-    int bulk_blocks[3] = {0, 0, 0};      // its resident grid
+    int bulk_resident[3] = {1, 1, 1};    // its CTAs resident on the GPU at once
 };
 
 constexpr int kLayoutThreads = 1024;

@@ -133,8 +133,10 @@ __global__ void ll_finish_kernel(int R, int T, int maxT, int K, int E, int exper
     *sp = row;
 }
 
-// Bulk-copy low-latency dispatch: each CTA walks tokens blockIdx.x + j * gridDim.x
-// through `stages` shared-memory buffers.  A stage holds one complete message
+// Bulk-copy low-latency dispatch: CTA b takes the contiguous tokens [b * per_cta,
+// (b + 1) * per_cta) -- the grid covers all tokens, so the messages in flight
+// stay a contiguous window of the token order -- and walks them through
+// `stages` shared-memory buffers.  A stage holds one complete message
 // (header, payload, FP8 scales) -- for bf16 the row is loaded straight into the
 // payload position -- and warp 0 lane 0 writes it to every valid slot's row with
 // one bulk store each.  In FP8 mode the CTA's warps first cast the staged bf16
@@ -156,7 +158,7 @@ __host__ __device__ __forceinline__ LLBulkSmem ll_bulk_smem(bool fp8, int H, int
 }
 
 template <bool kFp8>
-__global__ void ll_dispatch_bulk_kernel(int R, int T, int maxT, int H, int K, int E, int stages,
+__global__ void ll_dispatch_bulk_kernel(int R, int T, int maxT, int H, int K, int E, int stages, int per_cta,
                                         const uint8_t* __restrict__ x, const int64_t* __restrict__ topk_idx,
                                         bool round_scale, bool use_ue8m0, const int32_t* __restrict__ slot,
                                         uint8_t* __restrict__ recv_msgs, int64_t msg_bytes, int32_t* status) {
@@ -178,8 +180,8 @@ __global__ void ll_dispatch_bulk_kernel(int R, int T, int maxT, int H, int K, in
     uint8_t* in_base = msg_base + S * lay.msg_stride;
     const int64_t slots = static_cast<int64_t>(R) * maxT;
     const int64_t n_tokens = static_cast<int64_t>(R) * T;
-    const int64_t first = blockIdx.x, stride = gridDim.x;
-    const int64_t n_local = first < n_tokens ? (n_tokens - 1 - first) / stride + 1 : 0;
+    const int64_t first = static_cast<int64_t>(blockIdx.x) * per_cta;
+    const int64_t n_local = first < n_tokens ? (n_tokens - first < per_cta ? n_tokens - first : per_cta) : 0;
     if (n_local == 0) return;
     if (tid == 0) {
         for (int s = 0; s < S; ++s) mbar_init(&bars[s], 1 + kWarpSize);
@@ -189,7 +191,7 @@ __global__ void ll_dispatch_bulk_kernel(int R, int T, int maxT, int H, int K, in
 
     auto produce = [&](int64_t j) {
         const int st = static_cast<int>(j % S);
-        const int64_t g = first + j * stride;
+        const int64_t g = first + j;
         const int64_t s = g / T;
         const int64_t t = g - s * T;
         if (lane < K) {
@@ -215,7 +217,7 @@ __global__ void ll_dispatch_bulk_kernel(int R, int T, int maxT, int H, int K, in
         __syncthreads();
         if (*s_flag == 0) break;
         uint8_t* msg = msg_base + st * lay.msg_stride;
-        const int64_t g = first + j * stride;
+        const int64_t g = first + j;
         if constexpr (kFp8) {
             const int4* xin = reinterpret_cast<const int4*>(in_base + st * lay.in_stride);
             int2* q = reinterpret_cast<int2*>(msg + 16);
@@ -503,6 +505,7 @@ size_t ll_count_smem(int E) { return sizeof(int32_t) * static_cast<size_t>(kLLCo
 }  // namespace
 
 constexpr uint32_t kLLBulkMaxSmem = 200u * 1024u;  // larger messages use the register kernel
+constexpr int kLLBulkRoundsPerCta = 1;              // bulk LL dispatch: at most stages x this tokens per CTA
 
 cudaError_t plan_ll(LaunchPlan* plan, int num_experts) {
     const int n = plan->num_sms;
@@ -549,36 +552,25 @@ cudaError_t launch_ll_dispatch(const LaunchPlan& plan, int R, int T, int maxT, i
     S = S < 2 ? 2 : (S > 8 ? 8 : S);
     const uint32_t smem = ll_bulk_smem(use_fp8, H, msg, S).total;
     if (smem <= kLLBulkMaxSmem) {
-        // resident CTAs per SM from the shared memory (227 KB per SM, 1 KB reserved per CTA); a larger
-        // grid would only queue, since no CTA waits for another
+        // contiguous token blocks: enough CTAs to fill the GPU once (CTAs resident per SM from the
+        // shared memory: 227 KB per SM, 1 KB reserved per CTA), at most one round of the stages
         int per_sm = static_cast<int>((227u * 1024u) / (smem + 1024u));
-        per_sm = per_sm < 1 ? 1 : (per_sm > 8 ? 8 : per_sm);
-        const int64_t want = static_cast<int64_t>(per_sm) * plan.num_sms;
-        const int grid = static_cast<int>(want < n_tokens ? want : n_tokens);
-        const uint8_t* xb = static_cast<const uint8_t*>(x);
-        uint8_t* mb = static_cast<uint8_t*>(recv_msgs);
-        if (use_fp8)
-            err = launch_kernel(ll_dispatch_bulk_kernel<true>, dim3(grid), dim3(4 * kWarpSize), smem, stream, 1,
-            R, T, maxT, H, K, E, S, xb, topk_idx,
-                                                                              rs, use_ue8m0, slot, mb, msg, status);
-        else
-            err = launch_kernel(ll_dispatch_bulk_kernel<false>, dim3(grid), dim3(kWarpSize), smem, stream, 1,
-            R, T, maxT, H, K, E, S, xb, topk_idx, rs,
-                                                                            use_ue8m0, slot, mb, msg, status);
-        return err;
+        per_sm = per_sm < 1 ? 1 : (per_sm > 32 ? 32 : per_sm);
+        const int64_t resident = static_cast<int64_t>(per_sm) * plan.num_sms;
+        const int64_t fill = (n_tokens + resident - 1) / resident;
+        const int cap_cta = S * kLLBulkRoundsPerCta;
+        const int per_cta = static_cast<int>(fill < 1 ? 1 : (fill > cap_cta ? cap_cta : fill));
+        const int grid = static_cast<int>((n_tokens + per_cta - 1) / per_cta);
+        auto kernel = use_fp8 ? ll_dispatch_bulk_kernel<true> : ll_dispatch_bulk_kernel<false>;
+        return launch_kernel(kernel, dim3(grid), dim3(use_fp8 ? 4 * kWarpSize : kWarpSize), smem, stream, 1, R, T,
+                             maxT, H, K, E, S, per_cta, static_cast<const uint8_t*>(x), topk_idx, rs, use_ue8m0,
+                             static_cast<const int32_t*>(slot), static_cast<uint8_t*>(recv_msgs), msg, status);
     }
     const int grid = clamp_grid(plan.ll_dispatch_blocks[use_fp8 ? 1 : 0], n_tokens, kLLDispatchThreads / kWarpSize);
-    if (use_fp8)
-        err = launch_kernel(ll_dispatch_kernel<true>, dim3(grid), dim3(kLLDispatchThreads), 0, stream, 1,
-            
-            R, T, maxT, H, K, E, static_cast<const int4*>(x), topk_idx, rs, use_ue8m0, slot,
-            static_cast<uint8_t*>(recv_msgs), msg);
-    else
-        err = launch_kernel(ll_dispatch_kernel<false>, dim3(grid), dim3(kLLDispatchThreads), 0, stream, 1,
-            
-            R, T, maxT, H, K, E, static_cast<const int4*>(x), topk_idx, rs, use_ue8m0, slot,
-            static_cast<uint8_t*>(recv_msgs), msg);
-    return err;
+    auto kernel = use_fp8 ? ll_dispatch_kernel<true> : ll_dispatch_kernel<false>;
+    return launch_kernel(kernel, dim3(grid), dim3(kLLDispatchThreads), 0, stream, 1, R, T, maxT, H, K, E,
+                         static_cast<const int4*>(x), topk_idx, rs, use_ue8m0, static_cast<const int32_t*>(slot),
+                         static_cast<uint8_t*>(recv_msgs), msg);
 }
 
 cudaError_t launch_ll_combine(const LaunchPlan& plan, int R, int T, int maxT, int H, int K, int E,
