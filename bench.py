@@ -370,10 +370,13 @@ def run_ours(args):
         h.check()
         del x_in, idx_in, w_in, outs, outws
 
-    ops = {}
+    ops, launch_model = {}, None
     if not args.no_ops and rank == 0:
         del recv_x, recv_i, recv_w, out, out_w
         h.destroy()
+        torch.cuda.empty_cache()
+        launch_model = measure_launch_model(ep, dev, peak, st)
+        del st
         torch.cuda.empty_cache()
         ops = measure_other_ops(ep, dev, peak)
 
@@ -393,6 +396,7 @@ def run_ours(args):
                          % (R * cap * H * 2 / 1e9),
                    "parallelism": "replicas" if world > 1 else "single GPU, R=8 virtual ranks"},
         "tokens_per_s": round(R * T * world / (elapsed / args.steps), 1),
+        "launch_model": launch_model,
         "hbm_frac_step": round(alg / (step_ms / 1e3) / 1e9 / peak, 4),
         "op_ms": {k: round(v, 4) for k, v in op_ms.items()},
         "roofline": {"bound": "hbm", "kernel": kernel_name, "achieved": round(achieved, 1), "peak": peak,
@@ -422,6 +426,60 @@ def timed(fn, reps, stream, warmup=3, batches=5):
         b.synchronize()
         times.append(a.elapsed_time(b) / reps)
     return statistics.median(times)
+
+
+def measure_launch_model(ep, dev, peak, st, reps=10, probe_sms=(16, 32)):
+    """The SM-count model on the headline workload: per-SM rates of the dispatch (writes) and the
+    combine (reads) measured with max_sms capping the data kernels, the SM counts the model then
+    suggests, and the dispatch / combine timed at those counts against the full GPU."""
+    stream = torch.cuda.current_stream(dev)
+    shape = W.WORKLOADS[HEADLINE]
+    R, T, H, E, K = shape.R, shape.T, shape.H, shape.E, shape.K
+    n, hits, cap = R * T, st["hits"], st["cap"]
+    disp_read, disp_write = 2 * H * n, 2 * H * hits
+    comb_read, comb_write = 2 * H * hits, 2 * H * n
+    recv_x = torch.empty((R, cap, H), dtype=torch.bfloat16, device=dev)
+    out = torch.empty((R, T, H), dtype=torch.bfloat16, device=dev)
+
+    def timed_pair(max_sms):
+        h = ep.Handle(ep.Config(R, T, H, E, K, shape.C, shape.A, cap, max_sms=max_sms), dev)
+        lay = ep.ep_get_dispatch_layout(h, st["idx_d"])
+        ep.ep_dispatch(h, st["x_d"], topk_idx=st["idx_d"], num_tokens_per_rank=lay["num_tokens_per_rank"],
+                       is_token_in_rank=lay["is_token_in_rank"], num_tokens_per_expert=lay["num_tokens_per_expert"],
+                       recv_x=recv_x)
+        d_ms = timed(lambda: ep.ep_dispatch(h, st["x_d"], cached=True, recv_x=recv_x), reps, stream)
+        c_ms = timed(lambda: ep.ep_combine(h, recv_x, combined_x=out), reps, stream)
+        h.check()
+        h.destroy()
+        return d_ms, c_ms
+
+    per_sm = {}
+    for m in probe_sms:
+        d_ms, c_ms = timed_pair(m)
+        per_sm[str(m)] = {"dispatch_us": round(d_ms * 1e3, 2), "combine_us": round(c_ms * 1e3, 2),
+                          "dispatch_write_gbs_per_sm": round(disp_write / (d_ms / 1e3) / 1e9 / m, 2),
+                          "combine_read_gbs_per_sm": round(comb_read / (c_ms / 1e3) / 1e9 / m, 2)}
+    # the model's per-SM capabilities: the best rates seen with the GPU not yet saturated
+    sm_write = max(v["dispatch_write_gbs_per_sm"] for v in per_sm.values())
+    sm_read = max(v["combine_read_gbs_per_sm"] for v in per_sm.values())
+    num_sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    model = dict(hbm_gbs=peak, sm_read_gbs=sm_read, sm_write_gbs=sm_write, num_device_sms=num_sms,
+                 prefer_overlap_with_compute=True)
+    n_d = ep.theoretical_num_sms(R, E, K, for_combine=False, **model)
+    n_c = ep.theoretical_num_sms(R, E, K, for_combine=True, **model)
+    d_ms, _ = timed_pair(n_d)
+    _, c_ms = timed_pair(n_c)
+    d_full, c_full = timed_pair(0)
+    del recv_x, out
+    return {"workload": f"{HEADLINE} (cached dispatch, combine of the received rows)",
+            "rho_model": round(ep.expected_topk(R, E, K), 4), "rho_measured": round(hits / n, 4),
+            "probe": per_sm, "sm_read_gbs": sm_read, "sm_write_gbs": sm_write, "hbm_gbs": peak,
+            "suggested_sms": {"dispatch": n_d, "combine": n_c},
+            "at_suggested": {"dispatch_us": round(d_ms * 1e3, 2), "combine_us": round(c_ms * 1e3, 2),
+                             "full_gpu_dispatch_us": round(d_full * 1e3, 2),
+                             "full_gpu_combine_us": round(c_full * 1e3, 2),
+                             "dispatch_vs_full_gpu": round(d_full / d_ms, 3),
+                             "combine_vs_full_gpu": round(c_full / c_ms, 3)}}
 
 
 def measure_other_ops(ep, dev, peak, reps=10):

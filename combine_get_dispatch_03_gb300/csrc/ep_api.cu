@@ -114,7 +114,7 @@ ep_status check_config(const ep_config* c) {
         return fail(EP_ERR_UNSUPPORTED, "num_topk %d outside [1, %d]", c->num_topk, ep::kMaxTopk);
     if (c->num_channels < 1) return fail(EP_ERR_INVALID_ARG, "num_channels %d < 1", c->num_channels);
     if (c->expert_alignment < 1) return fail(EP_ERR_INVALID_ARG, "expert_alignment %d < 1", c->expert_alignment);
-    if (c->reserved != 0) return fail(EP_ERR_INVALID_ARG, "reserved field must be 0");
+    if (c->max_sms < 0) return fail(EP_ERR_INVALID_ARG, "max_sms %d < 0", c->max_sms);
     if (c->recv_capacity < 0 || c->recv_capacity > INT32_MAX)
         return fail(EP_ERR_INVALID_ARG, "recv_capacity %lld outside [0, 2^31)",
                     static_cast<long long>(c->recv_capacity));
@@ -176,6 +176,10 @@ ep_status ep_handle_create(const ep_config* cfg, ep_handle** out) {
         return cuda_fail(err, "cudaGetDevice");
     }
     err = cudaDeviceGetAttribute(&h->plan.num_sms, cudaDevAttrMultiProcessorCount, h->device);
+    if (err == cudaSuccess && cfg->max_sms > 0 && cfg->max_sms < h->plan.num_sms) {
+        h->plan.num_sms = cfg->max_sms;
+        h->plan.sm_limited = true;
+    }
     if (err == cudaSuccess) err = ep::plan_dispatch_combine(&h->plan, cfg->hidden);
     if (err == cudaSuccess) err = ep::plan_ll(&h->plan, cfg->num_experts);
     if (err != cudaSuccess) {
@@ -486,21 +490,32 @@ ep_status ep_ll_dispatch(ep_handle* h, int32_t num_tokens, const void* x, const 
     return EP_OK;
 }
 
-ep_status ep_ll_combine(ep_handle* h, const void* x, const int64_t* topk_idx, const float* topk_weights,
-                        void* combined_x, ep_stream_t stream) {
+ep_status ep_ll_combine_strided(ep_handle* h, const void* x, int64_t x_row_bytes, const int64_t* topk_idx,
+                                const float* topk_weights, void* combined_x, ep_stream_t stream) {
     if (h == nullptr) return fail(EP_ERR_INVALID_ARG, "handle is NULL");
     if (h->ll_tokens < 0) return fail(EP_ERR_STATE, "low-latency combine without a prior low-latency dispatch");
     const ep_config& c = h->cfg;
     const int T = h->ll_tokens;
     EP_CHECK_ARG(x != nullptr && aligned16(x), "x must be a 16-byte aligned device pointer");
+    EP_CHECK_ARG(x_row_bytes >= 2 * static_cast<int64_t>(c.hidden) && x_row_bytes % 16 == 0,
+                 "x_row_bytes %lld must be a multiple of 16 and at least 2 * hidden = %d",
+                 static_cast<long long>(x_row_bytes), 2 * c.hidden);
     EP_CHECK_ARG(T == 0 || (topk_idx && topk_weights && combined_x && aligned8(topk_idx) && aligned4(topk_weights) &&
                             aligned16(combined_x)),
                  "topk_idx, topk_weights and a 16-byte aligned combined_x are required");
     DeviceGuard guard(h->device);
     cudaError_t err = ep::launch_ll_combine(h->plan, c.num_ranks, T, c.num_max_tokens, c.hidden, c.num_topk,
-                                            c.num_experts, x, topk_idx, topk_weights, h->ll_slot, combined_x, stream);
+                                            c.num_experts, x, x_row_bytes, topk_idx, topk_weights, h->ll_slot,
+                                            combined_x, stream);
     if (err != cudaSuccess) return cuda_fail(err, "low-latency combine launch");
     return EP_OK;
+}
+
+ep_status ep_ll_combine(ep_handle* h, const void* x, const int64_t* topk_idx, const float* topk_weights,
+                        void* combined_x, ep_stream_t stream) {
+    if (h == nullptr) return fail(EP_ERR_INVALID_ARG, "handle is NULL");
+    return ep_ll_combine_strided(h, x, 2 * static_cast<int64_t>(h->cfg.hidden), topk_idx, topk_weights, combined_x,
+                                 stream);
 }
 
 ep_status ep_update_mask_buffer(ep_handle* h, int32_t rank, int32_t masked, ep_stream_t stream) {

@@ -490,7 +490,8 @@ cudaError_t launch_dispatch(const LaunchPlan& plan, int mode, int R, int T, int 
         const int S = plan.bulk_stages[mode];
         // contiguous token blocks: enough CTAs to fill the GPU once, at most the stage rounds above
         const int64_t fill = (n_tokens + plan.bulk_resident[mode] - 1) / plan.bulk_resident[mode];
-        const int cap_cta = S * kBulkRoundsPerCta[mode];
+        // (with max_sms, one resident wave takes all tokens)
+        const int cap_cta = plan.sm_limited ? INT32_MAX : S * kBulkRoundsPerCta[mode];
         const int per_cta = static_cast<int>(fill < 1 ? 1 : (fill > cap_cta ? cap_cta : fill));
         const int grid = static_cast<int>((n_tokens + per_cta - 1) / per_cta);
         const uint32_t smem = plan.bulk_smem[mode];

@@ -10,7 +10,8 @@ namespace ep {
 
 // Launch shapes, chosen once per device when a handle is created.
 struct LaunchPlan {
-    int num_sms = 0;
+    int num_sms = 0;        // SMs the data kernels may fill: the device's, or ep_config.max_sms if fewer
+    bool sm_limited = false;  // num_sms was capped by max_sms: one resident wave covers all tokens
     int dispatch_blocks[3] = {0, 0, 0};  // per payload mode
     int combine_blocks[2] = {0, 0};      // bf16 out, fp32 out
     int ll_dispatch_blocks[2] = {0, 0};  // bf16, fp8
@@ -64,7 +65,7 @@ cudaError_t launch_bounded_wait_selftest(uint32_t max_iterations, int rank, int3
                                          cudaStream_t stream);
 
 cudaError_t launch_ll_combine(const LaunchPlan& plan, int R, int T, int maxT, int H, int K, int E,
-                              const void* y, const int64_t* topk_idx, const float* topk_weights,
+                              const void* y, int64_t y_row_bytes, const int64_t* topk_idx, const float* topk_weights,
                               const int32_t* slot, void* out, cudaStream_t stream);
 
 }  // namespace ep

@@ -18,7 +18,11 @@
 //      shared memory, then one bulk store per destination slot (a register
 //      kernel, one warp per token, serves messages too long to stage).
 // LL combine (§4.3): one warp per token gathers its K expert outputs and
-// accumulates w_k * y in fp32 with fused multiply-adds in slot order.
+// accumulates w_k * y in fp32 with fused multiply-adds in slot order.  The
+// expert-output rows may be strided (row stride >= 2H bytes): the bf16
+// payloads of the dispatch messages themselves, written over in place by the
+// experts, serve as the combine input with no copy (the zero-copy combine
+// buffer of §4.3).
 #include "ep_common.cuh"
 #include "ep_kernels.h"
 
@@ -47,19 +51,22 @@ __global__ void __launch_bounds__(kLLCountThreads)
     const int64_t* idx_s = topk_idx + static_cast<int64_t>(s) * T * K;
     int32_t* slot_s = slot + static_cast<int64_t>(s) * maxT * K;
 
+    __shared__ int32_t s_mask[kMaxRanks];  // rank mask (0 everywhere without one)
     for (int e = tid; e < E; e += kLLCountThreads) s_run[e] = 0;
+    if (tid < kMaxRanks) s_mask[tid] = rank_mask != nullptr && tid < R ? __ldg(rank_mask + tid) : 0;
+    int64_t next = tid < n ? __ldg(idx_s + tid) : -1;  // the next chunk's entry, loaded one chunk ahead
     for (int base = 0; base < n; base += kLLCountThreads) {
         for (int i = tid; i < kLLCountWarps * E; i += kLLCountThreads) s_warp[i] = 0;
         __syncthreads();
         const int i = base + tid;
+        const int64_t v = next;
+        if (base + kLLCountThreads + tid < n) next = __ldg(idx_s + base + kLLCountThreads + tid);
         int e = -1;
         if (i < n) {
-            const int64_t v = __ldg(idx_s + i);
             if (v >= 0 && v < E) e = static_cast<int>(v);
             else if (v != -1) report(status, EP_ERR_BAD_EXPERT);
             // a masked rank neither sends nor receives
-            if (e >= 0 && rank_mask != nullptr && (__ldg(rank_mask + s) != 0 || __ldg(rank_mask + e / (E / R)) != 0))
-                e = -1;
+            if (e >= 0 && (s_mask[s] != 0 || s_mask[e / (E / R)] != 0)) e = -1;
         }
         const unsigned peers = __match_any_sync(kFullMask, e);
         const int before = __popc(peers & lanemask_lt());
@@ -126,8 +133,14 @@ __global__ void ll_finish_kernel(int R, int T, int maxT, int K, int E, int exper
     const int32_t pos = *sp;
     int32_t row = -1;
     if (v >= 0 && v < E && pos >= 0) {
+        // the counts of the earlier sources, all loads in flight at once (R <= kMaxRanks)
+        int32_t part[kMaxRanks];
+#pragma unroll
+        for (int sp2 = 0; sp2 < kMaxRanks; ++sp2)
+            part[sp2] = sp2 < s ? __ldg(cnt + static_cast<int64_t>(sp2) * E + v) : 0;
         int64_t begin = 0;
-        for (int sp2 = 0; sp2 < s; ++sp2) begin += __ldg(cnt + static_cast<int64_t>(sp2) * E + v);
+#pragma unroll
+        for (int sp2 = 0; sp2 < kMaxRanks; ++sp2) begin += part[sp2];
         if (begin + pos < slots) row = static_cast<int32_t>(begin + pos);
     }
     *sp = row;
@@ -396,7 +409,7 @@ __global__ void __launch_bounds__(kLLDispatchThreads)
 }
 
 __global__ void __launch_bounds__(kLLCombineThreads)
-    ll_combine_kernel(int R, int T, int maxT, int H, int K, int E, const int4* __restrict__ y,
+    ll_combine_kernel(int R, int T, int maxT, int H, int K, int E, const int4* __restrict__ y, int64_t y_row16,
                       const int64_t* __restrict__ topk_idx, const float* __restrict__ topk_weights,
                       const int32_t* __restrict__ slot, int4* __restrict__ out) {
     pdl_enter();
@@ -447,7 +460,7 @@ __global__ void __launch_bounds__(kLLCombineThreads)
 #pragma unroll
                     for (int u = 0; u < kLLCombineUnroll; ++u) {
                         const int i = i0 + u * kWarpSize + lane;
-                        if (kk[j] >= 0 && i < n16) v[j][u] = ld_stream_v4(y + sr[j] * n16 + i);
+                        if (kk[j] >= 0 && i < n16) v[j][u] = ld_stream_v4(y + sr[j] * y_row16 + i);
                     }
 #pragma unroll
                 for (int j = 0; j < kLLCombineFanIn; ++j) {
@@ -558,7 +571,7 @@ cudaError_t launch_ll_dispatch(const LaunchPlan& plan, int R, int T, int maxT, i
         per_sm = per_sm < 1 ? 1 : (per_sm > 32 ? 32 : per_sm);
         const int64_t resident = static_cast<int64_t>(per_sm) * plan.num_sms;
         const int64_t fill = (n_tokens + resident - 1) / resident;
-        const int cap_cta = S * kLLBulkRoundsPerCta;
+        const int cap_cta = plan.sm_limited ? INT32_MAX : S * kLLBulkRoundsPerCta;  // max_sms: one wave
         const int per_cta = static_cast<int>(fill < 1 ? 1 : (fill > cap_cta ? cap_cta : fill));
         const int grid = static_cast<int>((n_tokens + per_cta - 1) / per_cta);
         auto kernel = use_fp8 ? ll_dispatch_bulk_kernel<true> : ll_dispatch_bulk_kernel<false>;
@@ -574,17 +587,14 @@ cudaError_t launch_ll_dispatch(const LaunchPlan& plan, int R, int T, int maxT, i
 }
 
 cudaError_t launch_ll_combine(const LaunchPlan& plan, int R, int T, int maxT, int H, int K, int E,
-                              const void* y, const int64_t* topk_idx, const float* topk_weights,
+                              const void* y, int64_t y_row_bytes, const int64_t* topk_idx, const float* topk_weights,
                               const int32_t* slot, void* out, cudaStream_t stream) {
-    cudaError_t err = cudaSuccess;
     const int64_t n_tokens = static_cast<int64_t>(R) * T;
     if (n_tokens == 0) return cudaSuccess;
     const int grid = clamp_grid(plan.ll_combine_blocks, n_tokens, kLLCombineThreads / kWarpSize);
-    err = launch_kernel(ll_combine_kernel, dim3(grid), dim3(kLLCombineThreads), 0, stream, 1,
-            R, T, maxT, H, K, E, static_cast<const int4*>(y),
-                                                              topk_idx, topk_weights, slot,
-                                                              static_cast<int4*>(out));
-    return err;
+    return launch_kernel(ll_combine_kernel, dim3(grid), dim3(kLLCombineThreads), 0, stream, 1, R, T, maxT, H, K, E,
+                         static_cast<const int4*>(y), y_row_bytes / 16, topk_idx, topk_weights, slot,
+                         static_cast<int4*>(out));
 }
 
 cudaError_t launch_bounded_wait_selftest(uint32_t max_iterations, int rank, int32_t* rank_mask, int32_t* status,

@@ -37,8 +37,13 @@ class EPError(RuntimeError):
 class ep_config(ctypes.Structure):
     _fields_ = [("num_ranks", ctypes.c_int32), ("num_max_tokens", ctypes.c_int32), ("hidden", ctypes.c_int32),
                 ("num_experts", ctypes.c_int32), ("num_topk", ctypes.c_int32), ("num_channels", ctypes.c_int32),
-                ("expert_alignment", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("expert_alignment", ctypes.c_int32), ("max_sms", ctypes.c_int32),
                 ("recv_capacity", ctypes.c_int64)]
+
+
+class ep_sm_model(ctypes.Structure):
+    _fields_ = [("hbm_gbs", ctypes.c_double), ("sm_read_gbs", ctypes.c_double), ("sm_write_gbs", ctypes.c_double),
+                ("num_device_sms", ctypes.c_int32), ("prefer_overlap_with_compute", ctypes.c_int32)]
 
 
 _lib = None
@@ -46,7 +51,8 @@ EXPORTS = ("ep_handle_create", "ep_handle_destroy", "ep_handle_status", "ep_hand
            "ep_handle_field_bytes", "ep_handle_export", "ep_status_string", "ep_last_error",
            "ep_get_dispatch_layout", "ep_dispatch", "ep_combine", "ep_ll_msg_bytes", "ep_ll_dispatch",
            "ep_ll_combine", "ep_ll_dispatch_noalloc", "ep_notify_dispatch", "ep_update_mask_buffer",
-           "ep_query_mask_buffer", "ep_clean_mask_buffer", "ep_selftest_bounded_wait")
+           "ep_query_mask_buffer", "ep_clean_mask_buffer", "ep_selftest_bounded_wait", "ep_ll_combine_strided",
+           "ep_expected_topk", "ep_theoretical_num_sms")
 
 
 def library_path() -> str:
@@ -81,6 +87,11 @@ def lib():
         L.ep_ll_msg_bytes.restype = I64
         L.ep_ll_dispatch.argtypes = [P, I32, P, P, I32, I32, I32, P, P, P, P, P]
         L.ep_ll_combine.argtypes = [P, P, P, P, P, P]
+        L.ep_ll_combine_strided.argtypes = [P, P, I64, P, P, P, P]
+        L.ep_expected_topk.argtypes = [I32, I32, I32]
+        L.ep_expected_topk.restype = ctypes.c_double
+        L.ep_theoretical_num_sms.argtypes = [ctypes.POINTER(ep_sm_model), I32, I32, I32, I32]
+        L.ep_theoretical_num_sms.restype = I32
         L.ep_notify_dispatch.argtypes = [P, I32, P, P, P, P, P]
         L.ep_update_mask_buffer.argtypes = [P, I32, I32, P]
         L.ep_query_mask_buffer.argtypes = [P, P, P]
@@ -91,7 +102,8 @@ def lib():
         for name in ("ep_handle_create", "ep_handle_status", "ep_handle_num_recv", "ep_handle_export",
                      "ep_get_dispatch_layout", "ep_dispatch", "ep_combine", "ep_ll_dispatch", "ep_ll_combine",
                      "ep_ll_dispatch_noalloc", "ep_notify_dispatch", "ep_update_mask_buffer",
-                     "ep_query_mask_buffer", "ep_clean_mask_buffer", "ep_selftest_bounded_wait"):
+                     "ep_query_mask_buffer", "ep_clean_mask_buffer", "ep_selftest_bounded_wait",
+                     "ep_ll_combine_strided"):
             getattr(L, name).restype = S
         _lib = L
     return _lib
@@ -144,6 +156,7 @@ class Config:
     num_channels: int = 12
     expert_alignment: int = 1
     recv_capacity: int = 0
+    max_sms: int = 0  # 0: fill the GPU; n: at most n SMs' worth of CTAs resident (ep_theoretical_num_sms)
 
     @property
     def num_nodes(self) -> int:
@@ -156,7 +169,7 @@ class Config:
 
     def c(self) -> ep_config:
         return ep_config(self.num_ranks, self.num_max_tokens, self.hidden, self.num_experts, self.num_topk,
-                         self.num_channels, self.expert_alignment, 0, self.recv_capacity)
+                         self.num_channels, self.expert_alignment, self.max_sms, self.recv_capacity)
 
 
 class Handle:
@@ -436,9 +449,23 @@ def ll_views(recv_msgs: torch.Tensor, hidden: int, use_fp8: bool):
     return px, scales, src_info
 
 
+def _row_stride_bytes(x: torch.Tensor, R: int, EL: int, rows: int, H: int):
+    """Row stride in bytes of a [R][EL][rows][H] view whose rows are evenly spaced (contiguous rows
+    or the payloads of the message buffer), else None."""
+    if tuple(x.shape) != (R, EL, rows, H) or x.stride(3) != 1:
+        return None
+    r = x.stride(2)
+    if x.stride(1) != rows * r or x.stride(0) != EL * rows * r:
+        return None
+    return r * x.element_size()
+
+
 def ep_ll_combine(h: Handle, x: torch.Tensor, topk_idx: torch.Tensor, topk_weights: torch.Tensor,
                   combined_x=None, stream=None):
-    """Low-latency combine: top-k weighted fp32 sum of the expert outputs, bf16 out."""
+    """Low-latency combine: top-k weighted fp32 sum of the expert outputs, bf16 out.
+
+    x is [R][EL][R*maxT][H] bf16, contiguous or with evenly spaced rows -- e.g. the packed_recv_x
+    view of a bf16 message buffer (ll_views), which the experts overwrite in place (zero-copy)."""
     c, d = h.cfg, h.device
     R, H, K, EL, maxT = c.num_ranks, c.hidden, c.num_topk, c.num_local_experts, c.num_max_tokens
     if h.ll_tokens is None:
@@ -446,9 +473,48 @@ def ep_ll_combine(h: Handle, x: torch.Tensor, topk_idx: torch.Tensor, topk_weigh
     T = h.ll_tokens
     if combined_x is None:
         combined_x = _empty((R, T, H), torch.bfloat16, d)
-    _raise(lib().ep_ll_combine(
-        h.ptr, _ptr(x, "x", torch.bfloat16, (R, EL, R * maxT, H), d),
+    if not isinstance(x, torch.Tensor) or x.dtype != torch.bfloat16 or x.device != d:
+        raise TypeError(f"x must be a bf16 tensor on {d}")
+    row_bytes = _row_stride_bytes(x, R, EL, R * maxT, H)
+    if row_bytes is None:
+        raise ValueError(f"x must be [R={R}][EL={EL}][{R * maxT}][H={H}] with evenly spaced rows")
+    _raise(lib().ep_ll_combine_strided(
+        h.ptr, ctypes.c_void_p(x.data_ptr()), row_bytes,
         _ptr(topk_idx, "topk_idx", torch.int64, (R, T, K), d),
         _ptr(topk_weights, "topk_weights", torch.float32, (R, T, K), d),
         _ptr(combined_x, "combined_x", torch.bfloat16, (R, T, H), d), _stream(stream)))
     return combined_x
+
+
+def recv_hook(stream=None):
+    """Deferred receive (the return_recv_hook of the low-latency calls, [P3] section 4.3): records an
+    event on `stream` (default: the current stream) after the calls already enqueued there and
+    returns a function that makes the stream current at call time wait for it.  Launch a dispatch
+    on a communication stream, keep computing, call the hook where the received data is needed."""
+    s = stream if stream is not None else torch.cuda.current_stream()
+    ev = torch.cuda.Event()
+    ev.record(s)
+
+    def hook(wait_stream=None):
+        (wait_stream if wait_stream is not None else torch.cuda.current_stream()).wait_event(ev)
+
+    return hook
+
+
+def expected_topk(num_groups: int, num_experts: int, num_topk: int) -> float:
+    """Expected groups (ranks) hit by one token's top-k (the library's launch model)."""
+    v = lib().ep_expected_topk(num_groups, num_experts, num_topk)
+    if v < 0:
+        raise ValueError(lib().ep_last_error().decode())
+    return v
+
+
+def theoretical_num_sms(num_ranks: int, num_experts: int, num_topk: int, *, hbm_gbs: float, sm_read_gbs: float,
+                        sm_write_gbs: float, num_device_sms: int, prefer_overlap_with_compute: bool = True,
+                        for_combine: bool = False) -> int:
+    """SMs a dispatch (or combine) needs to keep HBM busy; a value for Config.max_sms."""
+    m = ep_sm_model(hbm_gbs, sm_read_gbs, sm_write_gbs, num_device_sms, int(bool(prefer_overlap_with_compute)))
+    n = lib().ep_theoretical_num_sms(ctypes.byref(m), num_ranks, num_experts, num_topk, int(bool(for_combine)))
+    if n < 0:
+        raise ValueError(lib().ep_last_error().decode())
+    return n

@@ -76,7 +76,10 @@ typedef struct ep_config {
     int32_t num_channels;     /* C >= 1: channels of the prefix matrices; the pages' tests run
                                  24 SMs, i.e. 12 channels ([P1] num_channels = num_sms / 2)     */
     int32_t expert_alignment; /* A >= 1: per-expert receive counts are rounded up to A ([P3] §4.1) */
-    int32_t reserved;         /* must be 0                                                      */
+    int32_t max_sms;          /* 0: the data kernels may fill the GPU; n > 0: they keep at most n
+                                 SMs' worth of CTAs resident at once and leave the rest of the
+                                 GPU to concurrent work ([P1] get_theoretical_num_sms and
+                                 prefer_overlap_with_compute; ep_theoretical_num_sms suggests n) */
     int64_t recv_capacity;    /* cap: rows per destination rank in normal-mode receive buffers
                                  (the num_worst_tokens bound of [P3] §4.1); 0 disables normal mode */
 } ep_config;
@@ -283,6 +286,18 @@ ep_status ep_ll_dispatch(ep_handle* h, int32_t num_tokens, const void* x, const 
 ep_status ep_ll_combine(ep_handle* h, const void* x, const int64_t* topk_idx,
                         const float* topk_weights, void* combined_x, ep_stream_t stream);
 
+/* ep_ll_combine() with strided expert-output rows: row (e, row) of x starts at
+ * x + (e * R*maxT + row) * x_row_bytes (x 16-byte aligned; x_row_bytes a
+ * multiple of 16, at least 2*H; the first 2*H bytes of a row are the bf16
+ * outputs).  This is the zero-copy combine input of [P3] §4.3 (low-latency
+ * combine can take its input straight from the communication buffer): after a
+ * bf16 ep_ll_dispatch, x = recv_msgs + 16 with x_row_bytes =
+ * ep_ll_msg_bytes(H, 0) reads the expert outputs written over the message
+ * payloads in place.  EP_ERR_INVALID_ARG for a bad stride or alignment;
+ * otherwise as ep_ll_combine(), which is this call with x_row_bytes = 2*H. */
+ep_status ep_ll_combine_strided(ep_handle* h, const void* x, int64_t x_row_bytes, const int64_t* topk_idx,
+                                const float* topk_weights, void* combined_x, ep_stream_t stream);
+
 /* ------------------------------------------------------- rank masking */
 
 /* The handle's mask buffer ([P1] low-latency: mask_buffer, is_rank_masked,
@@ -341,6 +356,41 @@ ep_status ep_ll_dispatch_noalloc(int32_t num_ranks, int32_t num_tokens, int32_t 
                                  int64_t* packed_recv_layout_range,
                                  int32_t* cumulative_local_expert_recv_stats, int32_t* slot_row,
                                  int32_t* status, ep_stream_t stream);
+
+/* ------------------------------------------------------------ launch model
+ * The SM-count model of [P1] (get_theoretical_num_sms, elastic.py), with the
+ * one link of a single GPU -- HBM -- as the bottleneck.  All host-side; no
+ * device call. */
+
+/* Expected number of distinct groups hit by one token's top-k experts, for
+ * num_experts experts split evenly into num_groups groups and the k experts
+ * drawn uniformly without replacement ([P1] get_expected_topk):
+ *   num_groups * (1 - C(E - E/G, k) / C(E, k)).
+ * With G = num_ranks this is rho, the expected destination ranks per token.
+ * Returns -1 (and sets ep_last_error) unless 1 <= G <= E, E % G == 0 and
+ * 1 <= k <= E. */
+double ep_expected_topk(int32_t num_groups, int32_t num_experts, int32_t num_topk);
+
+/* Inputs of ep_theoretical_num_sms: bandwidths in GB/s. */
+typedef struct ep_sm_model {
+    double hbm_gbs;       /* HBM bandwidth the data kernels can reach (read + write bytes)   */
+    double sm_read_gbs;   /* reads one SM of the data kernels sustains                       */
+    double sm_write_gbs;  /* writes one SM of the data kernels sustains                      */
+    int32_t num_device_sms;
+    int32_t prefer_overlap_with_compute; /* 0: never fewer than min(64, num_device_sms) SMs  */
+} ep_sm_model;
+
+/* SMs a dispatch (for_combine == 0) or combine (for_combine != 0) needs to
+ * keep HBM busy, by the steps of [P1] get_theoretical_num_sms with
+ * rho = ep_expected_topk(num_ranks, num_experts, num_topk).  Per received
+ * row, a dispatch reads 1/rho source rows and writes one row, a combine reads
+ * one row and writes 1/rho rows, and HBM carries 1 + 1/rho rows:
+ *   sms = max(hbm / (1 + 1/rho) * read / sm_read, hbm / (1 + 1/rho) * write / sm_write)
+ *   sms = align_up(max(4, ceil(1.25 * sms)), 2)
+ *   sms = max(sms, 64) unless prefer_overlap_with_compute; then min(sms, num_device_sms).
+ * Returns -1 (and sets ep_last_error) for invalid arguments. */
+int32_t ep_theoretical_num_sms(const ep_sm_model* model, int32_t num_ranks, int32_t num_experts, int32_t num_topk,
+                               int32_t for_combine);
 
 #ifdef __cplusplus
 }

@@ -47,10 +47,10 @@ class Guarded:
         assert bool((head == self.fill).all()) and bool((tail == self.fill).all()), "write outside the buffer"
 
 
-def config_of(shape: W.Shape, cap: int) -> ep.Config:
+def config_of(shape: W.Shape, cap: int, max_sms: int = 0) -> ep.Config:
     return ep.Config(num_ranks=shape.R, num_max_tokens=max(shape.max_tokens or shape.T, shape.T), hidden=shape.H,
                      num_experts=shape.E, num_topk=shape.K, num_channels=shape.C,
-                     expert_alignment=shape.A, recv_capacity=cap)
+                     expert_alignment=shape.A, recv_capacity=cap, max_sms=max_sms)
 
 
 def needed_capacity(idx: np.ndarray, E: int) -> int:
@@ -83,7 +83,7 @@ def valid_rows(num_recv: np.ndarray, cap: int):
 
 
 def run_normal(shape: W.Shape, *, mode: int = O.MODE_BF16, cap: int | None = None, with_weights=True,
-               biases=False, out_fp32=False, y_seed: int | None = None):
+               biases=False, out_fp32=False, y_seed: int | None = None, max_sms: int = 0):
     """Layout -> fresh dispatch -> combine on the GPU and in the oracle; returns both sides' outputs."""
     idx, w = W.routing(shape)
     x = W.tokens_x(shape)  # bf16 on the host
@@ -91,7 +91,7 @@ def run_normal(shape: W.Shape, *, mode: int = O.MODE_BF16, cap: int | None = Non
     need = needed_capacity(idx, shape.E)
     if cap is None:
         cap = max(need, 1)
-    cfg = config_of(shape, cap)
+    cfg = config_of(shape, cap, max_sms)
     h = ep.Handle(cfg)
     idx_d = torch.from_numpy(idx).to(DEV)
     w_d = torch.from_numpy(w).to(DEV)

@@ -311,6 +311,56 @@ def test_ll_views():
 
 
 @pytest.mark.parametrize("shape", LL_CASES[:4], ids=lambda s: s.name)
+def test_ll_zero_copy_combine_in_message_buffer(shape):
+    """bf16 messages: the experts overwrite the payloads in place and the combine reads them there
+    (strided rows, no copy); same result as the oracle on the same outputs.  Headers stay intact."""
+    r = run_ll(shape, "bf16")
+    assert r["status"] == 0
+    maxT = shape.max_tokens
+    px, _, src = ep.ll_views(r["out"]["recv_msgs"], shape.H, False)
+    src_before = P.host(src).copy()
+    y = W.normal_bf16((shape.R, shape.EL, shape.R * maxT, shape.H), shape.seed, "zcy", device=P.DEV)
+    px.copy_(y)  # the expert writes its outputs over the payloads
+    idx_d, w_d = torch.from_numpy(r["idx"]).to(P.DEV), torch.from_numpy(r["w"]).to(P.DEV)
+    got = ep.ep_ll_combine(r["h"], px, idx_d, w_d)
+    assert r["h"].status() == 0
+    want = O.ll_combine(P.host(y), r["idx"], r["w"], r["ora"]["slot_row"], maxT, shape.E)
+    np.testing.assert_array_equal(P.host(got), want)
+    np.testing.assert_array_equal(P.host(src), src_before)
+    r["msgs"].check()
+    # the contiguous call on a copy of the same outputs agrees bit for bit
+    np.testing.assert_array_equal(P.host(ep.ep_ll_combine(r["h"], px.contiguous(), idx_d, w_d)), want)
+    with pytest.raises(ValueError):
+        ep.ep_ll_combine(r["h"], px[:, :, ::2], idx_d, w_d)
+
+
+def test_ll_recv_hook_defers_the_wait():
+    """Dispatch on a communication stream, take the hook, run other work on the compute stream,
+    call the hook, then combine: the received messages are complete and correct."""
+    shape = LL_CASES[2]
+    h = ep.Handle(P.config_of(shape, 0))
+    idx, w = W.routing(shape)
+    x = W.tokens_x(shape).to(P.DEV)
+    idx_d, w_d = torch.from_numpy(idx).to(P.DEV), torch.from_numpy(w).to(P.DEV)
+    comm = torch.cuda.Stream()
+    comm.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(comm):
+        out = ep.ep_ll_dispatch(h, x, idx_d, use_fp8=True, use_ue8m0=True, stream=comm)
+        hook = ep.recv_hook(comm)
+    busy = torch.randn(2048, 2048, device=P.DEV) @ torch.randn(2048, 2048, device=P.DEV)  # overlapped work
+    hook()
+    msgs = P.host(out["recv_msgs"])
+    ora = O.ll_dispatch(W.bf16_bits(W.tokens_x(shape)), idx, shape.max_tokens, shape.E, use_fp8=True,
+                        use_ue8m0=True)
+    s_, t_, k_ = np.nonzero(ora["slot_row"] >= 0)
+    e = idx[s_, t_, k_]
+    rows = ora["slot_row"][s_, t_, k_]
+    np.testing.assert_array_equal(msgs[e // shape.EL, e % shape.EL, rows], ora["msgs_by_slot"][s_, t_, k_])
+    assert torch.isfinite(busy).all()
+    assert h.status() == 0
+
+
+@pytest.mark.parametrize("shape", LL_CASES[:4], ids=lambda s: s.name)
 def test_ll_rank_mask(shape):
     """A masked rank neither sends nor receives; cleaning the mask restores the full dispatch."""
     h = ep.Handle(P.config_of(shape, 0))
@@ -333,6 +383,27 @@ def test_ll_rank_mask(shape):
     assert (ep.ep_query_mask_buffer(h).numpy() == 0).all()
     r2 = run_ll(shape, "fp8_ue8m0", h=h)
     compare_ll(r2, shape)
+
+
+@pytest.mark.parametrize("max_sms", [1, 7, 16])
+def test_max_sms_keeps_every_result(max_sms):
+    """With the data kernels capped to a few SMs' worth of CTAs (one resident wave takes every
+    token), dispatch (bf16 and FP8 cast), combine and the LL path stay bit-exact."""
+    shape = NORMAL_CASES[3]
+    for mode in (O.MODE_BF16, O.MODE_CAST_FP8):
+        res = P.run_normal(shape, mode=mode, biases=mode == O.MODE_BF16, max_sms=max_sms)
+        assert res["status"] == 0
+        P.compare_dispatch(res, shape, mode)
+        if mode == O.MODE_BF16:
+            np.testing.assert_array_equal(P.host(res["c"]["combined_x"]), res["ora_c"]["out"])
+    ll = LL_CASES[2]
+    r = run_ll(ll, "fp8_ue8m0", h=ep.Handle(P.config_of(ll, 0, max_sms)))
+    assert r["status"] == 0
+    compare_ll(r, ll)
+    y = W.normal_bf16((ll.R, ll.EL, ll.R * ll.max_tokens, ll.H), ll.seed, "msy", device=P.DEV)
+    got = ep.ep_ll_combine(r["h"], y, torch.from_numpy(r["idx"]).to(P.DEV), torch.from_numpy(r["w"]).to(P.DEV))
+    want = O.ll_combine(P.host(y), r["idx"], r["w"], r["ora"]["slot_row"], ll.max_tokens, ll.E)
+    np.testing.assert_array_equal(P.host(got), want)
 
 
 def test_bounded_wait_times_out_and_masks():
