@@ -482,6 +482,38 @@ def measure_launch_model(ep, dev, peak, st, reps=10, probe_sms=(16, 32)):
                              "combine_vs_full_gpu": round(c_full / c_ms, 3)}}
 
 
+def run_ll_calls(n):
+    """The low-latency path of ll_v3 alone, n dispatches then n combines back to back (a short, fixed
+    launch sequence for profilers); prints the CUDA-event time per call."""
+    from combine_get_dispatch_03_gb300 import ep
+    dev = torch.device("cuda", 0)
+    shape = W.WORKLOADS["ll_v3"]
+    idx, w = W.routing(shape)
+    idx_d, w_d = torch.from_numpy(idx).to(dev), torch.from_numpy(w).to(dev)
+    x_d = W.tokens_x(shape, device=dev)
+    h = ep.Handle(ep.Config(shape.R, shape.max_tokens, shape.H, shape.E, shape.K, shape.C, 1, 0), dev)
+    rows = shape.R * shape.max_tokens
+    msgs = torch.empty((shape.R, shape.EL, rows, ep.ep_ll_msg_bytes(shape.H, True)), dtype=torch.uint8, device=dev)
+    y = W.normal_bf16((shape.R, shape.EL, rows, shape.H), shape.seed, "lly", device=dev)
+    out = torch.empty((shape.R, shape.T, shape.H), dtype=torch.bfloat16, device=dev)
+    s = torch.cuda.current_stream(dev)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(s)
+    for _ in range(n):
+        ep.ep_ll_dispatch(h, x_d, idx_d, use_fp8=True, use_ue8m0=True, recv_msgs=msgs)
+    b.record(s)
+    b.synchronize()
+    d_us = a.elapsed_time(b) * 1e3 / n
+    a.record(s)
+    for _ in range(n):
+        ep.ep_ll_combine(h, y, idx_d, w_d, combined_x=out)
+    b.record(s)
+    b.synchronize()
+    h.check()
+    print(json.dumps({"ll_calls": n, "ll_dispatch_us": round(d_us, 2),
+                      "ll_combine_us": round(a.elapsed_time(b) * 1e3 / n, 2)}))
+
+
 def measure_other_ops(ep, dev, peak, reps=10):
     """Per-op times of the other workloads (median of reps, after warm-up)."""
     stream = torch.cuda.current_stream(dev)
@@ -698,13 +730,17 @@ def main():
     ap.add_argument("--cpu-fraction", type=int, default=8, help="oracle sample = T / this many tokens per rank")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-ops", action="store_true")
+    ap.add_argument("--ll-calls", type=int, default=0,
+                    help="only run the ll_v3 low-latency dispatch and combine this many times each (profiling)")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--tokens", type=int, default=0,
                     help="tokens per rank of the headline workload (0 = its full 4096; smaller only for profiling)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
-    if args.impl == "reference":
+    if args.ll_calls:
+        run_ll_calls(args.ll_calls)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)
