@@ -26,6 +26,7 @@ namespace {
 constexpr int kDispatchUnroll = 4;  // 16-byte vectors in flight per lane (payload read)
 constexpr int kCombineUnroll = 2;   // 16-byte columns per lane per pass
 constexpr int kCombineFanIn = 4;    // source rows loaded together before accumulation
+constexpr int kCombineWeightRanks = 8;  // source ranks whose top-k weights are loaded ahead of the rows
 constexpr bool kUseBulkDispatch = true;  // bulk-copy (TMA 1D) dispatch where the rows fit in shared memory
 // Bulk dispatch: at most stages x this many tokens per CTA (bf16, cast, FP8 input).  Measured on
 // the 7168-wide workloads: one round of the stages is best for a plain copy; the cast, with its
@@ -345,19 +346,28 @@ __global__ void __launch_bounds__(kCombineThreads)
     const int64_t n_tokens = static_cast<int64_t>(R) * T;
     const int n16 = H / 8;
 
-    for (int64_t g = static_cast<int64_t>(blockIdx.x) * kWarps + threadIdx.x / kWarpSize; g < n_tokens;
-         g += static_cast<int64_t>(gridDim.x) * kWarps) {
-        const int32_t row = dest_row(send_head, g, R, cap, lane);
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * kWarps;
+    int64_t g = static_cast<int64_t>(blockIdx.x) * kWarps + threadIdx.x / kWarpSize;
+    // the send_head row of the warp's next token is loaded one token ahead
+    int32_t next_row = g < n_tokens ? dest_row(send_head, g, R, cap, lane) : -1;
+    for (; g < n_tokens; g += stride) {
+        const int32_t row = next_row;
+        if (g + stride < n_tokens) next_row = dest_row(send_head, g + stride, R, cap, lane);
         const unsigned src_ranks = __ballot_sync(kFullMask, row >= 0);
 
-        if (cw != nullptr && recv_w != nullptr) {
-            float acc = 0.0f;
-            for (unsigned m = src_ranks; m; m &= m - 1) {
-                const int r = __ffs(m) - 1;
+        // Top-k weights of the first kCombineWeightRanks source ranks: loaded now, summed (in
+        // rank order) after the rows, so their latency hides behind the row loads.
+        const bool with_w = cw != nullptr && recv_w != nullptr;
+        float wv[kCombineWeightRanks];
+        unsigned w_left = src_ranks;
+        if (with_w) {
+#pragma unroll
+            for (int j = 0; j < kCombineWeightRanks; ++j) {
+                const int r = w_left ? __ffs(w_left) - 1 : 0;
                 const int64_t rr = __shfl_sync(kFullMask, row, r);
-                if (lane < K) acc = acc + __ldg(recv_w + (static_cast<int64_t>(r) * cap + rr) * K + lane);
+                wv[j] = (w_left && lane < K) ? __ldg(recv_w + (static_cast<int64_t>(r) * cap + rr) * K + lane) : 0.0f;
+                if (w_left) w_left &= w_left - 1;
             }
-            if (lane < K) cw[g * K + lane] = acc;
         }
 
         for (int i0 = 0; i0 < n16; i0 += kWarpSize * kCombineUnroll) {
@@ -418,6 +428,20 @@ __global__ void __launch_bounds__(kCombineThreads)
                     reinterpret_cast<int4*>(out)[g * n16 + i] = pack8_bf16(acc[u]);
                 }
             }
+        }
+
+        if (with_w) {
+            float acc = 0.0f;
+            const int nw = __popc(src_ranks);
+#pragma unroll
+            for (int j = 0; j < kCombineWeightRanks; ++j)
+                if (j < nw) acc = acc + wv[j];
+            for (unsigned m = w_left; m; m &= m - 1) {  // ranks past the first kCombineWeightRanks
+                const int r = __ffs(m) - 1;
+                const int64_t rr = __shfl_sync(kFullMask, row, r);
+                if (lane < K) acc = acc + __ldg(recv_w + (static_cast<int64_t>(r) * cap + rr) * K + lane);
+            }
+            if (lane < K) cw[g * K + lane] = acc;
         }
     }
 }
