@@ -514,6 +514,33 @@ def run_ll_calls(n):
                       "ll_combine_us": round(a.elapsed_time(b) * 1e3 / n, 2)}))
 
 
+def run_fp8_calls(n, tokens=0):
+    """The FP8 dispatch of fp8_zipf alone (fresh record, fused cast, top-k metadata), n calls back to
+    back for profilers (tokens per rank cut to `tokens` if given); prints the CUDA-event time per call."""
+    from combine_get_dispatch_03_gb300 import ep
+    dev = torch.device("cuda", 0)
+    shape = W.WORKLOADS["fp8_zipf"]
+    if tokens:
+        shape = shape.scaled(T=tokens)
+    st = prepare_normal(ep, shape, dev)
+    h, cap = st["h"], st["cap"]
+    lay = ep.ep_get_dispatch_layout(h, st["idx_d"])
+    bufs = dict(recv_x=torch.empty((shape.R, cap, shape.H), dtype=torch.float8_e4m3fn, device=dev),
+                recv_x_scales=torch.empty((shape.R, cap, shape.H // 128), dtype=torch.float32, device=dev))
+    s = torch.cuda.current_stream(dev)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(s)
+    for _ in range(n):
+        ep.ep_dispatch(h, st["x_d"], topk_idx=st["idx_d"], topk_weights=st["w_d"], cast_to_fp8=True,
+                       num_tokens_per_rank=lay["num_tokens_per_rank"], is_token_in_rank=lay["is_token_in_rank"],
+                       num_tokens_per_expert=lay["num_tokens_per_expert"], **bufs)
+    b.record(s)
+    b.synchronize()
+    h.check()
+    print(json.dumps({"fp8_calls": n, "tokens_per_rank": shape.T,
+                      "fp8_dispatch_us": round(a.elapsed_time(b) * 1e3 / n, 2)}))
+
+
 def measure_other_ops(ep, dev, peak, reps=10):
     """Per-op times of the other workloads (median of reps, after warm-up)."""
     stream = torch.cuda.current_stream(dev)
@@ -732,6 +759,8 @@ def main():
     ap.add_argument("--no-ops", action="store_true")
     ap.add_argument("--ll-calls", type=int, default=0,
                     help="only run the ll_v3 low-latency dispatch and combine this many times each (profiling)")
+    ap.add_argument("--fp8-calls", type=int, default=0,
+                    help="only run the fp8_zipf FP8 dispatch (fresh record, cast) this many times (profiling)")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--tokens", type=int, default=0,
                     help="tokens per rank of the headline workload (0 = its full 4096; smaller only for profiling)")
@@ -740,6 +769,8 @@ def main():
         ap.error("--warmup must be at least 3")
     if args.ll_calls:
         run_ll_calls(args.ll_calls)
+    elif args.fp8_calls:
+        run_fp8_calls(args.fp8_calls, args.tokens)
     elif args.impl == "reference":
         run_reference(args)
     else:

@@ -28,10 +28,12 @@ constexpr int kCombineUnroll = 2;   // 16-byte columns per lane per pass
 constexpr int kCombineFanIn = 4;    // source rows loaded together before accumulation
 constexpr int kCombineWeightRanks = 8;  // source ranks whose top-k weights are loaded ahead of the rows
 constexpr bool kUseBulkDispatch = true;  // bulk-copy (TMA 1D) dispatch where the rows fit in shared memory
-// Bulk dispatch: at most stages x this many tokens per CTA (bf16, cast, FP8 input).  Measured on
-// the 7168-wide workloads: one round of the stages is best for a plain copy; the cast, with its
-// heavier per-CTA start, is best with two.
-constexpr int kBulkRoundsPerCta[3] = {1, 2, 1};
+// Shared memory for the stages of one CTA (bf16, cast, FP8 input).  The cast keeps fewer stages
+// (two rows of bf16 + FP8 at 7168 channels) so that more CTAs -- and their cast work -- share an
+// SM; measured on the 7168-wide workloads, with one round of the stages per CTA (a CTA takes at
+// most `stages` tokens): 652 us for fp8_zipf against 692 us with three stages and two rounds.
+constexpr uint32_t kBulkStageBudget[3] = {65536u, 45056u, 65536u};
+constexpr int kBulkCastWarps = 4;  // warps of a cast CTA
 
 // Row of rank `lane` for token g, or -1 (not sent / past capacity).
 __device__ __forceinline__ int32_t dest_row(const int32_t* send_head, int64_t g, int R, int64_t cap, int lane) {
@@ -462,13 +464,13 @@ int clamp_grid(int planned, int64_t warps_needed, int warps_per_block) {
 }  // namespace
 
 int bulk_stages(int mode, int H) {
-    // about 64 KB of row buffers per CTA, between 2 and 8 stages
+    // kBulkStageBudget[mode] bytes of row buffers per CTA, between 2 and 8 stages
     const uint32_t per = bulk_smem(mode, H, 1).in_stride + bulk_smem(mode, H, 1).out_stride;
-    int s = static_cast<int>(65536u / per);
+    int s = static_cast<int>(kBulkStageBudget[mode] / per);
     return s < 2 ? 2 : (s > 8 ? 8 : s);
 }
 
-int bulk_threads(int mode) { return mode == kModeCastFp8 ? 4 * kWarpSize : kWarpSize; }
+int bulk_threads(int mode) { return mode == kModeCastFp8 ? kBulkCastWarps * kWarpSize : kWarpSize; }
 
 template <int kMode>
 cudaError_t plan_bulk(LaunchPlan* plan, int H) {
@@ -512,10 +514,10 @@ cudaError_t launch_dispatch(const LaunchPlan& plan, int mode, int R, int T, int 
     if (n_tokens == 0) return cudaSuccess;
     if (kUseBulkDispatch && plan.bulk_stages[mode] > 0) {
         const int S = plan.bulk_stages[mode];
-        // contiguous token blocks: enough CTAs to fill the GPU once, at most the stage rounds above
+        // contiguous token blocks: enough CTAs to fill the GPU once, at most one round of the stages
         const int64_t fill = (n_tokens + plan.bulk_resident[mode] - 1) / plan.bulk_resident[mode];
         // (with max_sms, one resident wave takes all tokens)
-        const int cap_cta = plan.sm_limited ? INT32_MAX : S * kBulkRoundsPerCta[mode];
+        const int cap_cta = plan.sm_limited ? INT32_MAX : S;
         const int per_cta = static_cast<int>(fill < 1 ? 1 : (fill > cap_cta ? cap_cta : fill));
         const int grid = static_cast<int>((n_tokens + per_cta - 1) / per_cta);
         const uint32_t smem = plan.bulk_smem[mode];
