@@ -208,6 +208,25 @@ class Events:
         return self.ev[a].elapsed_time(self.ev[b])
 
 
+def headline_config(T, recv_gb, world):
+    """The `config` of the headline line (both arms)."""
+    return {"workload": f"{HEADLINE}: R=8 T={T} H=7168 E=256 K=8 Gumbel routing A=128 C=12; step = "
+                        "get_dispatch_layout + notify_dispatch + dispatch (bf16, top-k metadata) + "
+                        "combine (received rows, top-k weight reduction)",
+            "l2": "no flush; inputs larger than L2 (x 470 MB, receive buffer %.2f GB vs 129 MB L2)" % recv_gb,
+            "parallelism": "replicas" if world > 1 else "single GPU, R=8 virtual ranks"}
+
+
+def receive_capacity(shape):
+    """Rows of the largest destination rank for the workload's routing (host arithmetic)."""
+    idx, _ = W.routing(shape)
+    dest = np.where(idx >= 0, idx // shape.EL, -1)  # [R][T][K] destination rank per slot
+    hit = np.zeros((shape.R, shape.T, shape.R), dtype=bool)
+    s_, t_, k_ = np.nonzero(dest >= 0)
+    hit[s_, t_, dest[s_, t_, k_]] = True
+    return int(hit.sum(axis=(0, 1)).max())
+
+
 def prepare_normal(ep, shape, dev, with_e2e=True):
     idx, w = W.routing(shape)
     idx_d = torch.from_numpy(idx).to(dev)
@@ -389,12 +408,7 @@ def run_ours(args):
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(step_ms, 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded routing and N(0,1) bf16 tokens)",
-        "config": {"workload": f"{HEADLINE}: R=8 T={T} H=7168 E=256 K=8 Gumbel routing A=128 C=12; step = "
-                               "get_dispatch_layout + notify_dispatch + dispatch (bf16, top-k metadata) + "
-                               "combine (received rows, top-k weight reduction)",
-                   "l2": "no flush; inputs larger than L2 (x 470 MB, receive buffer %.2f GB vs 129 MB L2)"
-                         % (R * cap * H * 2 / 1e9),
-                   "parallelism": "replicas" if world > 1 else "single GPU, R=8 virtual ranks"},
+        "config": headline_config(T, R * cap * H * 2 / 1e9, world),
         "tokens_per_s": round(R * T * world / (elapsed / args.steps), 1),
         "launch_model": launch_model,
         "hbm_frac_step": round(alg / (step_ms / 1e3) / 1e9 / peak, 4),
@@ -741,7 +755,7 @@ def run_reference(args):
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": 1,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * sum(secs) / len(secs), 2),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-            "data": "synthetic", "config": {"workload": desc},
+            "data": "synthetic", "config": headline_config(shape.T, shape.R * receive_capacity(shape) * shape.H * 2 / 1e9, 1),
             "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": desc},
             "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
