@@ -385,6 +385,32 @@ def test_ll_rank_mask(shape):
     compare_ll(r2, shape)
 
 
+def test_maximum_sizes():
+    """The largest configuration the library takes: 32 ranks, 2048 experts, top-32, with masked
+    slots; normal dispatch (bf16 and FP8 cast) and combine at H = 7168, and the LL path, against the
+    oracle."""
+    shape = S("max", 32, 24, 7168, 2048, 32, routing="zipf", mask_p=0.05, C=12, A=128, seed=90)
+    for mode in (O.MODE_BF16, O.MODE_CAST_FP8):
+        res = P.run_normal(shape, mode=mode, biases=mode == O.MODE_BF16)
+        assert res["status"] == 0
+        P.compare_layout(res["lay"], res["ora_lay"])
+        P.compare_record(res["h"], res["ora_n"], shape.T)
+        P.compare_dispatch(res, shape, mode)
+        if mode == O.MODE_BF16:
+            np.testing.assert_array_equal(P.host(res["c"]["combined_x"]), res["ora_c"]["out"])
+            np.testing.assert_array_equal(P.host(res["c"]["combined_topk_weights"]),
+                                          res["ora_c"]["combined_topk_weights"])
+    # LL at H = 512: its buffers hold E * R * maxT rows (64 local experts x 768 rows per rank here)
+    ll = S("max_ll", 32, 24, 512, 2048, 32, routing="zipf", mask_p=0.05, seed=91, max_tokens=24)
+    r = run_ll(ll, "fp8_ue8m0")
+    assert r["status"] == 0
+    compare_ll(r, ll)
+    y = W.normal_bf16((ll.R, ll.EL, ll.R * ll.max_tokens, ll.H), ll.seed, "maxy", device=P.DEV)
+    got = ep.ep_ll_combine(r["h"], y, torch.from_numpy(r["idx"]).to(P.DEV), torch.from_numpy(r["w"]).to(P.DEV))
+    want = O.ll_combine(P.host(y), r["idx"], r["w"], r["ora"]["slot_row"], ll.max_tokens, ll.E)
+    np.testing.assert_array_equal(P.host(got), want)
+
+
 @pytest.mark.parametrize("max_sms", [1, 7, 16])
 def test_max_sms_keeps_every_result(max_sms):
     """With the data kernels capped to a few SMs' worth of CTAs (one resident wave takes every
