@@ -208,6 +208,10 @@ class Events:
         return self.ev[a].elapsed_time(self.ev[b])
 
 
+STEP_OPS = ("layout_notify", "dispatch", "combine")  # timed parts of the headline step
+EV_PER_STEP = len(STEP_OPS) + 1
+
+
 def headline_config(T, recv_gb, world):
     """The `config` of the headline line (both arms)."""
     return {"workload": f"{HEADLINE}: R=8 T={T} H=7168 E=256 K=8 Gumbel routing A=128 C=12; step = "
@@ -268,41 +272,50 @@ def run_ours(args):
     out = torch.empty((R, T, H), dtype=torch.bfloat16, device=dev)
     out_w = torch.empty((R, T, K), dtype=torch.float32, device=dev)
 
-    # The dispatch runs as its two parts, notify (the record) and the prepared data movement,
-    # so that the data kernel has its own pair of events.
+    # The layout and the dispatch record come from one call (one cooperative launch); the
+    # prepared dispatch then moves the rows, so the data kernel has its own pair of events.
     def step(idx_in, w_in, x_in, ev=None, base=0):
         if ev: ev.rec(base, stream)
-        ep.ep_get_dispatch_layout(h, idx_in, **lay)
+        ep.ep_layout_notify(h, idx_in, num_recv_tokens_per_expert=nrpe, **lay)
         if ev: ev.rec(base + 1, stream)
-        ep.ep_notify_dispatch(h, lay["num_tokens_per_rank"], lay["is_token_in_rank"], lay["num_tokens_per_expert"],
-                              num_recv_tokens_per_expert=nrpe)
-        if ev: ev.rec(base + 2, stream)
         ep.ep_dispatch(h, x_in, topk_idx=idx_in, topk_weights=w_in, recv_x=recv_x, recv_topk_idx=recv_i,
                        recv_topk_weights=recv_w, prepared=True)
-        if ev: ev.rec(base + 3, stream)
+        if ev: ev.rec(base + 2, stream)
         ep.ep_combine(h, recv_x, topk_weights=recv_w, combined_x=out, combined_topk_weights=out_w)
-        if ev: ev.rec(base + 4, stream)
+        if ev: ev.rec(base + 3, stream)
 
     for _ in range(args.warmup):
         step(idx_d, w_d, x_d)
     torch.cuda.synchronize(dev)
     h.check()
 
-    ev = Events(5 * args.steps + 1)
+    ev = Events(EV_PER_STEP * args.steps + 1)
     barrier(world)
     with ClockSampler(dev.index) as clocks:
         torch.cuda.synchronize(dev)
         t0 = time.perf_counter()
         for i in range(args.steps):
-            step(idx_d, w_d, x_d, ev, 5 * i)
-        ev.rec(5 * args.steps, stream)
+            step(idx_d, w_d, x_d, ev, EV_PER_STEP * i)
+        ev.rec(EV_PER_STEP * args.steps, stream)
         torch.cuda.synchronize(dev)
         wall = time.perf_counter() - t0
     barrier(world)
     h.check()
-    step_ms = ev.ms(0, 5 * args.steps) / args.steps
-    op_ms = {name: statistics.mean(ev.ms(5 * i + j, 5 * i + j + 1) for i in range(args.steps))
-             for j, name in enumerate(("layout", "notify", "dispatch", "combine"))}
+    step_ms = ev.ms(0, EV_PER_STEP * args.steps) / args.steps
+    op_ms = {name: statistics.mean(ev.ms(EV_PER_STEP * i + j, EV_PER_STEP * i + j + 1) for i in range(args.steps))
+             for j, name in enumerate(STEP_OPS)}
+
+    # the layout and the record as one launch against the two separate calls (same outputs)
+    ln_one = timed(lambda: ep.ep_layout_notify(h, idx_d, num_recv_tokens_per_expert=nrpe, **lay), 10, stream)
+
+    def two_calls():
+        ep.ep_get_dispatch_layout(h, idx_d, **lay)
+        ep.ep_notify_dispatch(h, lay["num_tokens_per_rank"], lay["is_token_in_rank"], lay["num_tokens_per_expert"],
+                              num_recv_tokens_per_expert=nrpe)
+
+    ln_two = timed(two_calls, 10, stream)
+    h.check()
+    layout_notify = {"one_launch_us": round(ln_one * 1e3, 2), "two_launches_us": round(ln_two * 1e3, 2)}
 
     bm = normal_bytes(R, T, H, K, hits)
     payload = bm["dispatch"]["payload"] + bm["combine"]["payload"]
@@ -355,9 +368,7 @@ def run_ours(args):
                 uploaded[b].record(up)
             stream.wait_event(uploaded[b])
             stream.wait_event(downloaded[b])         # this output set has been read back
-            ep.ep_get_dispatch_layout(h, idx_in[b], **lay)
-            ep.ep_notify_dispatch(h, lay["num_tokens_per_rank"], lay["is_token_in_rank"],
-                                  lay["num_tokens_per_expert"], num_recv_tokens_per_expert=nrpe)
+            ep.ep_layout_notify(h, idx_in[b], num_recv_tokens_per_expert=nrpe, **lay)
             ep.ep_dispatch(h, x_in[b], topk_idx=idx_in[b], topk_weights=w_in[b], recv_x=recv_x,
                            recv_topk_idx=recv_i, recv_topk_weights=recv_w, prepared=True)
             ep.ep_combine(h, recv_x, topk_weights=recv_w, combined_x=outs[b], combined_topk_weights=outws[b])
@@ -411,13 +422,14 @@ def run_ours(args):
         "config": headline_config(T, R * cap * H * 2 / 1e9, world),
         "tokens_per_s": round(R * T * world / (elapsed / args.steps), 1),
         "launch_model": launch_model,
+        "layout_notify": layout_notify,
         "hbm_frac_step": round(alg / (step_ms / 1e3) / 1e9 / peak, 4),
         "op_ms": {k: round(v, 4) for k, v in op_ms.items()},
         "roofline": {"bound": "hbm", "kernel": kernel_name, "achieved": round(achieved, 1), "peak": peak,
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "traffic": traffic, "algorithmic_bytes": dom_bytes},
         "cpu_baseline": cpu, "clocks": clocks.summary(), "e2e": e2e,
-        "gpu_launches": 4 * args.steps,  # layout, notify, dispatch, combine per step
+        "gpu_launches": 3 * args.steps,  # layout + notify (one launch), dispatch, combine per step
         "wall_s_timed": round(wall, 3), "ops": ops,
     }
     if rank == 0:

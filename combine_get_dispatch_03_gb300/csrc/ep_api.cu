@@ -38,6 +38,7 @@ struct ep_handle {
     int32_t* rank_mask = nullptr;            // [R], nonzero = masked
     int32_t* rdma_channel_prefix = nullptr;    // [R][NN][C], NN = R / 8 whole nodes (see has_nodes)
     int32_t* recv_rdma_rank_prefix = nullptr;  // [R][NN]
+    int32_t* barrier = nullptr;                // [2]: count and generation of the layout + notify grid barrier
     int normal_tokens = -1;                  // T of the current dispatch record, -1 = none
     bool prepared = false;                   // record built by ep_notify_dispatch, not yet used
     int ll_tokens = -1;                      // T of the last LL dispatch, -1 = none
@@ -182,6 +183,7 @@ ep_status ep_handle_create(const ep_config* cfg, ep_handle** out) {
     }
     if (err == cudaSuccess) err = ep::plan_dispatch_combine(&h->plan, cfg->hidden);
     if (err == cudaSuccess) err = ep::plan_ll(&h->plan, cfg->num_experts);
+    if (err == cudaSuccess) h->plan.layout_notify_fused = ep::layout_notify_fits(cfg->num_ranks, cfg->num_experts);
     if (err != cudaSuccess) {
         delete h;
         return cuda_fail(err, "planning launches");
@@ -191,10 +193,11 @@ ep_status ep_handle_create(const ep_config* cfg, ep_handle** out) {
     const size_t E = cfg->num_experts, cap = static_cast<size_t>(cfg->recv_capacity);
     const size_t NN = (R + 7) / 8;
     const size_t sizes[] = {1, R * R, R * R * C, R * R * C, R, R * cap, R * T * R, R * T * K, R * E, R,
-                            R * NN * C, R * NN};
+                            R * NN * C, R * NN, 2};
     int32_t** slots[] = {&h->status,   &h->rank_prefix,  &h->channel_prefix, &h->recv_channel_prefix,
                          &h->num_recv, &h->recv_src_idx, &h->send_head,      &h->ll_slot,
-                         &h->ll_cnt,   &h->rank_mask,    &h->rdma_channel_prefix, &h->recv_rdma_rank_prefix};
+                         &h->ll_cnt,   &h->rank_mask,    &h->rdma_channel_prefix, &h->recv_rdma_rank_prefix,
+                         &h->barrier};
     size_t total = 0;
     for (size_t s : sizes) total += align_up(s * sizeof(int32_t), 256);
     err = cudaMalloc(&h->dmem, total);
@@ -434,6 +437,48 @@ ep_status ep_notify_dispatch(ep_handle* h, int32_t num_tokens, const int32_t* nu
         h->recv_channel_prefix, h->num_recv, h->send_head, h->recv_src_idx, num_recv_tokens_per_expert,
         node_record(h, 0), node_record(h, 1), h->status, stream);
     if (err != cudaSuccess) return cuda_fail(err, "dispatch_notify launch");
+    h->normal_tokens = num_tokens;
+    h->prepared = true;
+    return EP_OK;
+}
+
+ep_status ep_layout_notify(ep_handle* h, int32_t num_tokens, const int64_t* topk_idx, int32_t* num_tokens_per_rank,
+                           int32_t* num_tokens_per_rdma_rank, int32_t* num_tokens_per_expert,
+                           uint8_t* is_token_in_rank, int32_t* num_recv_tokens_per_expert, ep_stream_t stream) {
+    if (h == nullptr) return fail(EP_ERR_INVALID_ARG, "handle is NULL");
+    ep_status st = check_tokens(h, num_tokens);
+    if (st != EP_OK) return st;
+    const ep_config& c = h->cfg;
+    EP_CHECK_ARG(c.recv_capacity > 0, "handle was created with recv_capacity 0 (normal mode disabled)");
+    EP_CHECK_ARG(num_tokens == 0 || topk_idx != nullptr, "topk_idx is NULL");
+    EP_CHECK_ARG(num_tokens_per_rank && num_tokens_per_expert && is_token_in_rank && num_recv_tokens_per_expert,
+                 "a layout output or num_recv_tokens_per_expert is NULL");
+    EP_CHECK_ARG(aligned8(topk_idx) && aligned4(num_tokens_per_rank) && aligned4(num_tokens_per_expert) &&
+                     aligned4(num_tokens_per_rdma_rank) && aligned16(is_token_in_rank) &&
+                     aligned4(num_recv_tokens_per_expert),
+                 "misaligned layout pointer");
+    DeviceGuard guard(h->device);
+    cudaError_t err;
+    if (h->plan.layout_notify_fused) {
+        err = ep::launch_layout_notify(topk_idx, c.num_ranks, num_tokens, c.num_topk, c.num_experts, c.num_channels,
+                                       c.expert_alignment, c.recv_capacity, num_tokens_per_rank,
+                                       num_tokens_per_rdma_rank, num_tokens_per_expert, is_token_in_rank,
+                                       h->rank_prefix, h->channel_prefix, h->recv_channel_prefix, h->num_recv,
+                                       h->send_head, h->recv_src_idx, num_recv_tokens_per_expert, node_record(h, 0),
+                                       node_record(h, 1), reinterpret_cast<uint32_t*>(h->barrier), h->status, stream);
+        if (err != cudaSuccess) return cuda_fail(err, "layout_notify launch");
+    } else {
+        err = ep::launch_get_dispatch_layout(topk_idx, c.num_ranks, num_tokens, c.num_topk, c.num_experts,
+                                             num_tokens_per_rank, num_tokens_per_rdma_rank, num_tokens_per_expert,
+                                             is_token_in_rank, h->status, stream);
+        if (err == cudaSuccess)
+            err = ep::launch_dispatch_notify(
+                c.num_ranks, num_tokens, c.num_experts, c.num_channels, c.expert_alignment, c.recv_capacity,
+                num_tokens_per_rank, is_token_in_rank, num_tokens_per_expert, h->rank_prefix, h->channel_prefix,
+                h->recv_channel_prefix, h->num_recv, h->send_head, h->recv_src_idx, num_recv_tokens_per_expert,
+                node_record(h, 0), node_record(h, 1), h->status, stream);
+        if (err != cudaSuccess) return cuda_fail(err, "layout / notify launch");
+    }
     h->normal_tokens = num_tokens;
     h->prepared = true;
     return EP_OK;

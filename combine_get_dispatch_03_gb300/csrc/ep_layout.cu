@@ -39,20 +39,21 @@ constexpr int kRanksPerNode = 8;     // NVLink peers of one node
 constexpr int kMaxNodes = kMaxRanks / kRanksPerNode;
 constexpr int kMaxColumns = kMaxRanks + kMaxNodes;  // notify count columns: ranks, then nodes
 
-// Mask of destination ranks of one token from its R-byte is_token_in_rank row.
+// Mask of destination ranks of one token from its R-byte is_token_in_rank row (L2 loads: the
+// one-launch layout + notify reads rows that the same launch wrote).
 __device__ __forceinline__ uint32_t load_rank_mask(const uint8_t* row, int R) {
     uint32_t m = 0;
     if ((R & 3) == 0) {
         const uint32_t* w = reinterpret_cast<const uint32_t*>(row);
         for (int i = 0; i < R / 4; ++i) {
-            const uint32_t v = __ldg(w + i);
+            const uint32_t v = __ldcg(w + i);
 #pragma unroll
             for (int b = 0; b < 4; ++b)
                 if ((v >> (8 * b)) & 0xffu) m |= 1u << (4 * i + b);
         }
     } else {
         for (int r = 0; r < R; ++r)
-            if (__ldg(row + r)) m |= 1u << r;
+            if (__ldcg(row + r)) m |= 1u << r;
     }
     return m;
 }
@@ -84,26 +85,21 @@ __device__ __forceinline__ void cluster_slice(int T, int q, int& lo, int& hi) {
     hi = min(T, lo + per);
 }
 
-// grid (kClusterCtas, R), cluster (kClusterCtas, 1, 1).
-__global__ void __launch_bounds__(kLayoutThreads)
-    get_dispatch_layout_kernel(const int64_t* __restrict__ topk_idx, int R, int T, int K, int E, int EL,
-                               int32_t* __restrict__ tpr, int32_t* __restrict__ tprdma,
-                               int32_t* __restrict__ tpe, uint8_t* __restrict__ itr, int32_t* status) {
-    pdl_enter();
-    extern __shared__ int32_t s_expert[];  // [E]
+// Layout of source s by CTA q of its cluster: the slice's tokens are marked in is_token_in_rank,
+// counted per expert, per destination rank and per node.  Leaves the slice's hits per rank in
+// s_cnt[0, R) and per node in s_cnt[R, R + ceil(R/8)) -- read by the rest of the cluster -- and
+// writes the source's totals (tpr, tprdma when given, tpe).  Ends with a cluster barrier.
+__device__ __forceinline__ void layout_source(const cg::cluster_group& cluster, int s, int q,
+                                              const int64_t* __restrict__ topk_idx, int R, int T, int K, int E,
+                                              int EL, int32_t* __restrict__ tpr, int32_t* __restrict__ tprdma,
+                                              int32_t* __restrict__ tpe, uint8_t* __restrict__ itr,
+                                              int32_t* status, int32_t* s_expert, int32_t* s_cnt) {
     __shared__ uint32_t s_mask[kLayoutRound];
-    __shared__ int32_t s_rank[kMaxRanks];
-    __shared__ int32_t s_node[kMaxRanks / 8];
-
-    cg::cluster_group cluster = cg::this_cluster();
-    const int q = static_cast<int>(cluster.block_rank());
-    const int s = blockIdx.y;
     const int tid = threadIdx.x;
     const int lane = lane_id();
-    const int NN = (R + 7) / 8;
+    const int NN = (R + kRanksPerNode - 1) / kRanksPerNode;
     for (int i = tid; i < E; i += kLayoutThreads) s_expert[i] = 0;
-    if (tid < kMaxRanks) s_rank[tid] = 0;
-    if (tid < kMaxRanks / 8) s_node[tid] = 0;
+    if (tid < kMaxColumns) s_cnt[tid] = 0;
 
     int lo, hi;
     cluster_slice(T, q, lo, hi);
@@ -145,11 +141,11 @@ __global__ void __launch_bounds__(kLayoutThreads)
             if (tl < len) store_rank_mask(itr_s + static_cast<int64_t>(round + tl) * R, R, m);
             for (int r = 0; r < R; ++r) {
                 const unsigned b = __ballot_sync(kFullMask, (m >> r) & 1u);
-                if (lane == 0 && b) atomicAdd(&s_rank[r], __popc(b));
+                if (lane == 0 && b) atomicAdd(&s_cnt[r], __popc(b));
             }
             for (int n = 0; n < NN; ++n) {
-                const unsigned b = __ballot_sync(kFullMask, ((m >> (8 * n)) & 0xffu) != 0u);
-                if (lane == 0 && b) atomicAdd(&s_node[n], __popc(b));
+                const unsigned b = __ballot_sync(kFullMask, column_bit(m, R + n, R));
+                if (lane == 0 && b) atomicAdd(&s_cnt[R + n], __popc(b));
             }
         }
         __syncthreads();
@@ -164,83 +160,79 @@ __global__ void __launch_bounds__(kLayoutThreads)
     }
     if (q == 0 && tid < R) {
         int32_t sum = 0;
-        for (int p = 0; p < kClusterCtas; ++p) sum += cluster.map_shared_rank(s_rank, p)[tid];
+        for (int p = 0; p < kClusterCtas; ++p) sum += cluster.map_shared_rank(s_cnt, p)[tid];
         tpr[s * R + tid] = sum;
     }
     if (q == 1 && tprdma != nullptr && tid < NN) {
         int32_t sum = 0;
-        for (int p = 0; p < kClusterCtas; ++p) sum += cluster.map_shared_rank(s_node, p)[tid];
+        for (int p = 0; p < kClusterCtas; ++p) sum += cluster.map_shared_rank(s_cnt, p)[R + tid];
         tprdma[s * NN + tid] = sum;
     }
     cluster.sync();  // keep every CTA's shared memory alive until the sums are read
 }
 
-// grid (kClusterCtas, R + 1), cluster (kClusterCtas, 1, 1).  Cluster s < R: the
-// rows of source s, and with NN > 0 node columns its row of the node-level
-// channel prefix matrix.  Cluster R: rank_prefix_matrix, num_recv and the
-// aligned per-expert receive counts.  Counts are kept per column: R rank
-// columns, then NN node columns (0 when there is no node-level record).
-__global__ void __launch_bounds__(kNotifyThreads)
-    dispatch_notify_kernel(int R, int NN, int T, int E, int C, int A, int64_t cap,
-                           const int32_t* __restrict__ tpr, const uint8_t* __restrict__ itr,
-                           const int32_t* __restrict__ tpe, int32_t* __restrict__ rank_prefix,
-                           int32_t* __restrict__ channel_prefix, int32_t* __restrict__ recv_channel_prefix,
-                           int32_t* __restrict__ rdma_channel_prefix, int32_t* __restrict__ num_recv,
-                           int32_t* __restrict__ send_head, int32_t* __restrict__ recv_src_idx,
-                           int32_t* __restrict__ num_recv_per_expert, int32_t* status) {
+// grid (kClusterCtas, R), cluster (kClusterCtas, 1, 1).
+__global__ void __launch_bounds__(kLayoutThreads)
+    get_dispatch_layout_kernel(const int64_t* __restrict__ topk_idx, int R, int T, int K, int E, int EL,
+                               int32_t* __restrict__ tpr, int32_t* __restrict__ tprdma,
+                               int32_t* __restrict__ tpe, uint8_t* __restrict__ itr, int32_t* status) {
     pdl_enter();
-    __shared__ int32_t s_cnt[kMaxColumns];                 // hits of this CTA's slice, per column
+    extern __shared__ int32_t s_expert[];  // [E]
+    __shared__ int32_t s_cnt[kMaxColumns];
+    cg::cluster_group cluster = cg::this_cluster();
+    layout_source(cluster, blockIdx.y, static_cast<int>(cluster.block_rank()), topk_idx, R, T, K, E, EL, tpr,
+                  tprdma, tpe, itr, status, s_expert, s_cnt);
+}
+
+// The summary of the dispatch record: rank_prefix_matrix, num_recv and the aligned
+// per-expert receive counts (cluster R of the notify grid).
+__device__ __forceinline__ void notify_summary(int q, int R, int E, int A, int64_t cap,
+                                               const int32_t* __restrict__ tpr, const int32_t* __restrict__ tpe,
+                                               int32_t* __restrict__ rank_prefix, int32_t* __restrict__ num_recv,
+                                               int32_t* __restrict__ num_recv_per_expert, int32_t* status) {
+    const int tid = threadIdx.x;
+    const int per = kNotifyThreads * kClusterCtas;
+    for (int r = q * kNotifyThreads + tid; r < R; r += per) {
+        int32_t acc = 0;
+        for (int sp = 0; sp < R; ++sp) {
+            acc += __ldcg(tpr + sp * R + r);
+            rank_prefix[sp * R + r] = acc;
+        }
+        num_recv[r] = acc;
+        if (acc > cap) report(status, EP_ERR_CAPACITY);
+    }
+    for (int e = q * kNotifyThreads + tid; e < E; e += per) {
+        int64_t sum = 0;
+        for (int sp = 0; sp < R; ++sp) sum += __ldcg(tpe + static_cast<int64_t>(sp) * E + e);
+        num_recv_per_expert[e] = static_cast<int32_t>(((sum + A - 1) / A) * A);
+    }
+}
+
+// The rows of source s, CTA q of its cluster, given the slice's hits per column in s_cnt (every
+// CTA of the cluster has filled its s_cnt before this is entered): send_head, recv_src_idx, the
+// channel prefix matrices and, with NN > 0 node columns, the node-level channel prefix matrix.
+__device__ __forceinline__ void notify_source(const cg::cluster_group& cluster, int s, int q, int R, int NN, int T,
+                                              int C, int64_t cap, const int32_t* __restrict__ tpr,
+                                              const uint8_t* __restrict__ itr, int32_t* __restrict__ channel_prefix,
+                                              int32_t* __restrict__ recv_channel_prefix,
+                                              int32_t* __restrict__ rdma_channel_prefix,
+                                              int32_t* __restrict__ send_head, int32_t* __restrict__ recv_src_idx,
+                                              int32_t* status, const int32_t* s_cnt) {
     __shared__ int32_t s_base[kMaxRanks];                  // rows taken by earlier sources
     __shared__ int32_t s_before[kMaxColumns];              // hits of this source before the current round
     __shared__ int32_t s_warp[kMaxColumns][kNotifyWarps];  // per-warp counts -> exclusive prefixes
     __shared__ int32_t s_total[kMaxColumns];               // hits of the current round
     static_assert(kNotifyWarps == kWarpSize, "the column scan gives one lane per warp");
     static_assert(kMaxColumns <= kNotifyThreads, "one thread per column");
-
-    cg::cluster_group cluster = cg::this_cluster();
-    const int q = static_cast<int>(cluster.block_rank());
-    const int s = blockIdx.y;
     const int tid = threadIdx.x;
     const int lane = lane_id();
     const int warp = tid / kWarpSize;
     const int NC = R + NN;
-
-    if (s == R) {
-        const int per = kNotifyThreads * kClusterCtas;
-        for (int r = q * kNotifyThreads + tid; r < R; r += per) {
-            int32_t acc = 0;
-            for (int sp = 0; sp < R; ++sp) {
-                acc += __ldg(tpr + sp * R + r);
-                rank_prefix[sp * R + r] = acc;
-            }
-            num_recv[r] = acc;
-            if (acc > cap) report(status, EP_ERR_CAPACITY);
-        }
-        for (int e = q * kNotifyThreads + tid; e < E; e += per) {
-            int64_t sum = 0;
-            for (int sp = 0; sp < R; ++sp) sum += __ldg(tpe + static_cast<int64_t>(sp) * E + e);
-            num_recv_per_expert[e] = static_cast<int32_t>(((sum + A - 1) / A) * A);
-        }
-        return;
-    }
-
     int lo, hi;
     cluster_slice(T, q, lo, hi);
     const uint8_t* itr_s = itr + static_cast<int64_t>(s) * T * R;
     int32_t* head_s = send_head + static_cast<int64_t>(s) * T * R;
-    if (tid < kMaxColumns) s_cnt[tid] = 0;
-    __syncthreads();
 
-    // Pass 1: hits of this slice per column.
-    for (int t0 = lo; t0 < hi; t0 += kNotifyThreads) {
-        const int t = t0 + tid;
-        const uint32_t m = t < hi ? load_rank_mask(itr_s + static_cast<int64_t>(t) * R, R) : 0u;
-        for (int col = 0; col < NC; ++col) {
-            const unsigned b = __ballot_sync(kFullMask, column_bit(m, col, R));
-            if (lane == 0 && b) atomicAdd(&s_cnt[col], __popc(b));
-        }
-    }
-    cluster.sync();
     // Hits before this slice: earlier slices of this source; rows before it also count earlier sources.
     if (tid < NC) {
         int32_t before = 0;
@@ -249,12 +241,12 @@ __global__ void __launch_bounds__(kNotifyThreads)
     }
     if (tid < R) {
         int32_t base = 0;
-        for (int sp = 0; sp < s; ++sp) base += __ldg(tpr + sp * R + tid);
+        for (int sp = 0; sp < s; ++sp) base += __ldcg(tpr + sp * R + tid);
         s_base[tid] = base;
         if (q == kClusterCtas - 1) {
             // this slice ends the source: the per-source total must match the counts
             const int32_t total = s_before[tid] + s_cnt[tid];
-            if (total != __ldg(tpr + s * R + tid)) report(status, EP_ERR_INCONSISTENT);
+            if (total != __ldcg(tpr + s * R + tid)) report(status, EP_ERR_INCONSISTENT);
         }
     }
     cluster.sync();  // peers are done reading this CTA's s_cnt
@@ -333,7 +325,7 @@ __global__ void __launch_bounds__(kNotifyThreads)
     // Channels that end at T (or hold no token): written by the last slice of the source.
     if (q == kClusterCtas - 1 && tid < R) {
         const int r = tid;
-        const int32_t total = __ldg(tpr + s * R + r);
+        const int32_t total = __ldcg(tpr + s * R + r);
         for (int c = 0; c < C; ++c) {
             const int64_t start = min(static_cast<int64_t>(T), static_cast<int64_t>(c) * chunk);
             const int64_t end = min(static_cast<int64_t>(T), static_cast<int64_t>(c + 1) * chunk);
@@ -347,6 +339,50 @@ __global__ void __launch_bounds__(kNotifyThreads)
             if (min(static_cast<int64_t>(T), static_cast<int64_t>(c + 1) * chunk) == T)
                 rdma_channel_prefix[(static_cast<int64_t>(s) * NN + n) * C + c] = s_before[tid];
     }
+}
+
+// grid (kClusterCtas, R + 1), cluster (kClusterCtas, 1, 1).  Cluster s < R: the
+// rows of source s, and with NN > 0 node columns its row of the node-level
+// channel prefix matrix.  Cluster R: rank_prefix_matrix, num_recv and the
+// aligned per-expert receive counts.  Counts are kept per column: R rank
+// columns, then NN node columns (0 when there is no node-level record).
+__global__ void __launch_bounds__(kNotifyThreads)
+    dispatch_notify_kernel(int R, int NN, int T, int E, int C, int A, int64_t cap,
+                           const int32_t* __restrict__ tpr, const uint8_t* __restrict__ itr,
+                           const int32_t* __restrict__ tpe, int32_t* __restrict__ rank_prefix,
+                           int32_t* __restrict__ channel_prefix, int32_t* __restrict__ recv_channel_prefix,
+                           int32_t* __restrict__ rdma_channel_prefix, int32_t* __restrict__ num_recv,
+                           int32_t* __restrict__ send_head, int32_t* __restrict__ recv_src_idx,
+                           int32_t* __restrict__ num_recv_per_expert, int32_t* status) {
+    pdl_enter();
+    __shared__ int32_t s_cnt[kMaxColumns];  // hits of this CTA's slice, per column
+    cg::cluster_group cluster = cg::this_cluster();
+    const int q = static_cast<int>(cluster.block_rank());
+    const int s = blockIdx.y;
+    if (s == R) {
+        notify_summary(q, R, E, A, cap, tpr, tpe, rank_prefix, num_recv, num_recv_per_expert, status);
+        return;
+    }
+    const int tid = threadIdx.x;
+    const int lane = lane_id();
+    const int NC = R + NN;
+    int lo, hi;
+    cluster_slice(T, q, lo, hi);
+    const uint8_t* itr_s = itr + static_cast<int64_t>(s) * T * R;
+    if (tid < kMaxColumns) s_cnt[tid] = 0;
+    __syncthreads();
+    // Pass 1: hits of this slice per column.
+    for (int t0 = lo; t0 < hi; t0 += kNotifyThreads) {
+        const int t = t0 + tid;
+        const uint32_t m = t < hi ? load_rank_mask(itr_s + static_cast<int64_t>(t) * R, R) : 0u;
+        for (int col = 0; col < NC; ++col) {
+            const unsigned b = __ballot_sync(kFullMask, column_bit(m, col, R));
+            if (lane == 0 && b) atomicAdd(&s_cnt[col], __popc(b));
+        }
+    }
+    cluster.sync();
+    notify_source(cluster, s, q, R, NN, T, C, cap, tpr, itr, channel_prefix, recv_channel_prefix,
+                  rdma_channel_prefix, send_head, recv_src_idx, status, s_cnt);
 }
 
 // One CTA, after the notify, R = 8 NN: recv_rdma_rank_prefix[r][m] for r = (n, l)
@@ -364,6 +400,37 @@ __global__ void __launch_bounds__(kMaxRanks * kMaxNodes)
     for (int mp = 0; mp <= m; ++mp)
         acc += rdma_channel_prefix[(static_cast<int64_t>(kRanksPerNode * mp + l) * NN + n) * C + C - 1];
     recv_rdma_rank_prefix[i] = acc;
+}
+
+// Layout and notify in one cooperative launch: grid (kClusterCtas, R + 1), cluster
+// (kClusterCtas, 1, 1).  The source clusters compute the layout (and keep each slice's
+// hits per column in shared memory, which is what the notify's first pass would count),
+// every CTA meets at one grid barrier -- the record needs every source's counts -- and then
+// the source clusters write their rows while cluster R writes the summary.
+__global__ void __launch_bounds__(kLayoutThreads)
+    layout_notify_kernel(const int64_t* __restrict__ topk_idx, int R, int NN, int T, int K, int E, int C, int A,
+                         int64_t cap, int32_t* __restrict__ tpr, int32_t* __restrict__ tprdma,
+                         int32_t* __restrict__ tpe, uint8_t* __restrict__ itr, int32_t* __restrict__ rank_prefix,
+                         int32_t* __restrict__ channel_prefix, int32_t* __restrict__ recv_channel_prefix,
+                         int32_t* __restrict__ rdma_channel_prefix, int32_t* __restrict__ num_recv,
+                         int32_t* __restrict__ send_head, int32_t* __restrict__ recv_src_idx,
+                         int32_t* __restrict__ num_recv_per_expert, uint32_t* barrier, int32_t* status) {
+    static_assert(kLayoutThreads == kNotifyThreads, "one block size for both phases");
+    pdl_enter();
+    extern __shared__ int32_t s_expert[];  // [E]
+    __shared__ int32_t s_cnt[kMaxColumns];
+    cg::cluster_group cluster = cg::this_cluster();
+    const int q = static_cast<int>(cluster.block_rank());
+    const int s = blockIdx.y;
+    if (s < R)
+        layout_source(cluster, s, q, topk_idx, R, T, K, E, E / R, tpr, tprdma, tpe, itr, status, s_expert, s_cnt);
+    if (!grid_barrier(barrier, barrier + 1, gridDim.x * gridDim.y, status)) return;
+    if (s == R) {
+        notify_summary(q, R, E, A, cap, tpr, tpe, rank_prefix, num_recv, num_recv_per_expert, status);
+        return;
+    }
+    notify_source(cluster, s, q, R, NN, T, C, cap, tpr, itr, channel_prefix, recv_channel_prefix,
+                  rdma_channel_prefix, send_head, recv_src_idx, status, s_cnt);
 }
 
 }  // namespace
@@ -389,6 +456,45 @@ cudaError_t launch_dispatch_notify(int R, int T, int E, int C, int A, int64_t ca
                                     0, stream, kClusterCtas, R, NN, T, E, C, A, cap, tpr, itr, tpe, rank_prefix,
                                     channel_prefix, recv_channel_prefix, rdma_channel_prefix, num_recv, send_head,
                                     recv_src_idx, num_recv_per_expert, status);
+    if (err != cudaSuccess || !nodes) return err;
+    return launch_kernel(node_prefix_kernel, dim3(1, 1, 1), dim3(kMaxRanks * kMaxNodes, 1, 1), 0, stream, 1, R, NN, C,
+                         static_cast<const int32_t*>(rdma_channel_prefix), recv_rdma_rank_prefix);
+}
+
+bool layout_notify_fits(int R, int E) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(kClusterCtas, R + 1, 1);
+    cfg.blockDim = dim3(kLayoutThreads, 1, 1);
+    cfg.dynamicSmemBytes = sizeof(int32_t) * static_cast<size_t>(E);
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = kClusterCtas;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    int clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&clusters, layout_notify_kernel, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    return clusters >= R + 1;
+}
+
+cudaError_t launch_layout_notify(const int64_t* topk_idx, int R, int T, int K, int E, int C, int A, int64_t cap,
+                                 int32_t* tpr, int32_t* tprdma, int32_t* tpe, uint8_t* itr, int32_t* rank_prefix,
+                                 int32_t* channel_prefix, int32_t* recv_channel_prefix, int32_t* num_recv,
+                                 int32_t* send_head, int32_t* recv_src_idx, int32_t* num_recv_per_expert,
+                                 int32_t* rdma_channel_prefix, int32_t* recv_rdma_rank_prefix, uint32_t* barrier,
+                                 int32_t* status, cudaStream_t stream) {
+    const bool nodes = rdma_channel_prefix != nullptr && recv_rdma_rank_prefix != nullptr;
+    if (nodes && (R <= kRanksPerNode || R % kRanksPerNode != 0)) return cudaErrorInvalidValue;
+    const int NN = nodes ? R / kRanksPerNode : 0;
+    cudaError_t err = launch_kernel_cooperative(
+        layout_notify_kernel, dim3(kClusterCtas, R + 1, 1), dim3(kLayoutThreads, 1, 1),
+        sizeof(int32_t) * static_cast<size_t>(E), stream, kClusterCtas, topk_idx, R, NN, T, K, E, C, A, cap, tpr,
+        tprdma, tpe, itr, rank_prefix, channel_prefix, recv_channel_prefix, rdma_channel_prefix, num_recv, send_head,
+        recv_src_idx, num_recv_per_expert, barrier, status);
     if (err != cudaSuccess || !nodes) return err;
     return launch_kernel(node_prefix_kernel, dim3(1, 1, 1), dim3(kMaxRanks * kMaxNodes, 1, 1), 0, stream, 1, R, NN, C,
                          static_cast<const int32_t*>(rdma_channel_prefix), recv_rdma_rank_prefix);

@@ -52,7 +52,7 @@ EXPORTS = ("ep_handle_create", "ep_handle_destroy", "ep_handle_status", "ep_hand
            "ep_get_dispatch_layout", "ep_dispatch", "ep_combine", "ep_ll_msg_bytes", "ep_ll_dispatch",
            "ep_ll_combine", "ep_ll_dispatch_noalloc", "ep_notify_dispatch", "ep_update_mask_buffer",
            "ep_query_mask_buffer", "ep_clean_mask_buffer", "ep_selftest_bounded_wait", "ep_ll_combine_strided",
-           "ep_expected_topk", "ep_theoretical_num_sms")
+           "ep_expected_topk", "ep_theoretical_num_sms", "ep_layout_notify")
 
 
 def library_path() -> str:
@@ -93,6 +93,7 @@ def lib():
         L.ep_theoretical_num_sms.argtypes = [ctypes.POINTER(ep_sm_model), I32, I32, I32, I32]
         L.ep_theoretical_num_sms.restype = I32
         L.ep_notify_dispatch.argtypes = [P, I32, P, P, P, P, P]
+        L.ep_layout_notify.argtypes = [P, I32, P, P, P, P, P, P, P]
         L.ep_update_mask_buffer.argtypes = [P, I32, I32, P]
         L.ep_query_mask_buffer.argtypes = [P, P, P]
         L.ep_clean_mask_buffer.argtypes = [P, P]
@@ -103,7 +104,7 @@ def lib():
                      "ep_get_dispatch_layout", "ep_dispatch", "ep_combine", "ep_ll_dispatch", "ep_ll_combine",
                      "ep_ll_dispatch_noalloc", "ep_notify_dispatch", "ep_update_mask_buffer",
                      "ep_query_mask_buffer", "ep_clean_mask_buffer", "ep_selftest_bounded_wait",
-                     "ep_ll_combine_strided"):
+                     "ep_ll_combine_strided", "ep_layout_notify"):
             getattr(L, name).restype = S
         _lib = L
     return _lib
@@ -324,6 +325,41 @@ def ep_notify_dispatch(h: Handle, num_tokens_per_rank, is_token_in_rank, num_tok
         _stream(stream)))
     h.normal_tokens = T
     return num_recv_tokens_per_expert
+
+
+def ep_layout_notify(h: Handle, topk_idx: torch.Tensor, num_tokens_per_rank=None, num_tokens_per_rdma_rank=None,
+                     num_tokens_per_expert=None, is_token_in_rank=None, num_recv_tokens_per_expert=None,
+                     with_rdma: bool | None = None, stream=None):
+    """Layout and the dispatch record in one launch; follow with ep_dispatch(..., prepared=True)."""
+    c, d = h.cfg, h.device
+    R, E = c.num_ranks, c.num_experts
+    if topk_idx.dim() != 3 or topk_idx.shape[0] != R or topk_idx.shape[2] != c.num_topk:
+        raise ValueError(f"topk_idx must be [R={R}][T][K={c.num_topk}], got {tuple(topk_idx.shape)}")
+    T = topk_idx.shape[1]
+    if with_rdma is None:
+        with_rdma = R > 8
+    nn = (R + 7) // 8
+    tpr = num_tokens_per_rank if num_tokens_per_rank is not None else _empty((R, R), torch.int32, d)
+    tpe = num_tokens_per_expert if num_tokens_per_expert is not None else _empty((R, E), torch.int32, d)
+    itr = is_token_in_rank if is_token_in_rank is not None else _empty((R, T, R), torch.bool, d)
+    if itr.dtype not in (torch.bool, torch.uint8):
+        raise TypeError("is_token_in_rank must be bool or uint8")
+    tprdma = num_tokens_per_rdma_rank
+    if tprdma is None and with_rdma:
+        tprdma = _empty((R, nn), torch.int32, d)
+    nrpe = num_recv_tokens_per_expert
+    if nrpe is None:
+        nrpe = _empty((R, c.num_local_experts), torch.int32, d)
+    _raise(lib().ep_layout_notify(
+        h.ptr, T, _ptr(topk_idx, "topk_idx", torch.int64, (R, T, c.num_topk), d),
+        _ptr(tpr, "num_tokens_per_rank", torch.int32, (R, R), d),
+        _ptr(tprdma, "num_tokens_per_rdma_rank", torch.int32, (R, nn), d),
+        _ptr(tpe, "num_tokens_per_expert", torch.int32, (R, E), d),
+        _ptr(itr, "is_token_in_rank", None, (R, T, R), d),
+        _ptr(nrpe, "num_recv_tokens_per_expert", torch.int32, (R, c.num_local_experts), d), _stream(stream)))
+    h.normal_tokens = T
+    return dict(num_tokens_per_rank=tpr, num_tokens_per_rdma_rank=tprdma, num_tokens_per_expert=tpe,
+                is_token_in_rank=itr, num_recv_tokens_per_expert=nrpe)
 
 
 def ep_dispatch(h: Handle, x: torch.Tensor, topk_idx=None, topk_weights=None, num_tokens_per_rank=None,

@@ -131,3 +131,54 @@ def test_low_latency_graph_replays_match_oracle():
         np.testing.assert_array_equal(P.host(msgs)[e // base.EL, e % base.EL, rows], ora["msgs_by_slot"][s_, t_, k_])
         want = O.ll_combine(W.bf16_bits(yv), idx, w, ora["slot_row"], maxT, base.E)
         np.testing.assert_array_equal(P.host(out), want)
+
+
+def test_layout_notify_graph_replays():
+    """The one-launch layout + record (its grid barrier counts generations) captured in a graph with
+    the prepared dispatch and the combine, replayed on three routings."""
+    base = W.Shape("graph_ln", R=16, T=300, H=512, E=128, K=8, routing="zipf", mask_p=0.05, seed=7201)
+    routes = [W.routing(W.Shape(**{**base.__dict__, "seed": base.seed + i})) for i in range(3)]
+    x_h = W.tokens_x(base)
+    cap = max(P.needed_capacity(r[0], base.E) for r in routes)
+    h = ep.Handle(P.config_of(base, cap))
+    idx_d = torch.empty((base.R, base.T, base.K), dtype=torch.int64, device=P.DEV)
+    x_d = x_h.to(P.DEV)
+    idx_d.copy_(torch.from_numpy(routes[0][0]))
+    R, E, EL = base.R, base.E, base.EL
+    lay = dict(num_tokens_per_rank=torch.empty((R, R), dtype=torch.int32, device=P.DEV),
+               num_tokens_per_rdma_rank=torch.empty((R, 2), dtype=torch.int32, device=P.DEV),
+               num_tokens_per_expert=torch.empty((R, E), dtype=torch.int32, device=P.DEV),
+               is_token_in_rank=torch.empty((R, base.T, R), dtype=torch.bool, device=P.DEV),
+               num_recv_tokens_per_expert=torch.empty((R, EL), dtype=torch.int32, device=P.DEV))
+    recv_x = torch.empty((R, cap, base.H), dtype=torch.bfloat16, device=P.DEV)
+    out = torch.empty((R, base.T, base.H), dtype=torch.bfloat16, device=P.DEV)
+
+    def step():
+        ep.ep_layout_notify(h, idx_d, **lay)
+        ep.ep_dispatch(h, x_d, topk_idx=idx_d, prepared=True, recv_x=recv_x, with_topk=False)
+        ep.ep_combine(h, recv_x, combined_x=out)
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        step()
+    torch.cuda.current_stream().wait_stream(side)
+    assert h.status() == 0
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    xb = W.bf16_bits(x_h)
+    for idx, _ in routes:
+        idx_d.copy_(torch.from_numpy(idx))
+        graph.replay()
+        torch.cuda.synchronize()
+        assert h.status() == 0
+        ora_lay = O.get_dispatch_layout(idx, E)
+        n = O.dispatch_notify(ora_lay["num_tokens_per_rank"], ora_lay["is_token_in_rank"],
+                              ora_lay["num_tokens_per_expert"], base.C, base.A, cap)
+        d = O.dispatch(xb, n["send_head"], cap, E)
+        c = O.combine(d["recv_x"], n["send_head"])
+        np.testing.assert_array_equal(P.host(lay["num_tokens_per_rdma_rank"]), ora_lay["num_tokens_per_rdma_rank"])
+        np.testing.assert_array_equal(P.host(lay["num_recv_tokens_per_expert"]), n["num_recv_tokens_per_expert"])
+        np.testing.assert_array_equal(P.host(out), c["out"])
+

@@ -138,6 +138,39 @@ def test_notify_then_prepared_dispatch_equals_fresh():
         ep.ep_dispatch(h2, P.dev_bf16(res["x"]), topk_idx=idx_d, prepared=True)
 
 
+@pytest.mark.parametrize("shape", NORMAL_CASES, ids=lambda s: s.name)
+def test_layout_notify_in_one_launch(shape):
+    """ep_layout_notify (layout and record in one cooperative launch) then a prepared dispatch and a
+    combine: every output equals the oracle, as with the separate calls."""
+    idx, w = W.routing(shape)
+    cap = max(P.needed_capacity(idx, shape.E), 1)
+    h = ep.Handle(P.config_of(shape, cap))
+    idx_d, w_d = torch.from_numpy(idx).to(P.DEV), torch.from_numpy(w).to(P.DEV)
+    x = W.tokens_x(shape)
+    lay = ep.ep_layout_notify(h, idx_d)
+    assert h.status() == 0
+    ora_lay = O.get_dispatch_layout(idx, shape.E)
+    P.compare_layout(lay, ora_lay)
+    ora_n = O.dispatch_notify(ora_lay["num_tokens_per_rank"], ora_lay["is_token_in_rank"],
+                              ora_lay["num_tokens_per_expert"], shape.C, shape.A, cap)
+    P.compare_record(h, ora_n, shape.T)
+    np.testing.assert_array_equal(P.host(lay["num_recv_tokens_per_expert"]), ora_n["num_recv_tokens_per_expert"])
+    if shape.R > 8 and shape.R % 8 == 0:
+        want = O.rdma_prefix(ora_lay["is_token_in_rank"], shape.C)
+        for key in want:
+            np.testing.assert_array_equal(P.host(h.export(key)), want[key], err_msg=key)
+    d = ep.ep_dispatch(h, x.to(P.DEV), topk_idx=idx_d, topk_weights=w_d, prepared=True)
+    assert h.status() == 0
+    ora_d = O.dispatch(W.bf16_bits(x), ora_n["send_head"], cap, shape.E, topk_idx=idx, topk_weights=w)
+    rows = P.valid_rows(ora_n["num_recv"], cap)
+    np.testing.assert_array_equal(P.host(d["recv_x"])[rows], ora_d["recv_x"][rows])
+    np.testing.assert_array_equal(P.host(d["recv_topk_idx"])[rows], ora_d["recv_topk_idx"][rows])
+    c = ep.ep_combine(h, d["recv_x"], topk_weights=d["recv_topk_weights"])
+    ora_c = O.combine(ora_d["recv_x"], ora_n["send_head"], recv_topk_weights=ora_d["recv_topk_weights"],
+                      num_topk=shape.K)
+    np.testing.assert_array_equal(P.host(c["combined_x"]), ora_c["out"])
+
+
 def test_combine_of_dispatch_restores_x():
     """combine(dispatch(x)) / (number of receiving ranks) == x exactly (fp32 out)."""
     shape = S("roundtrip", 8, 300, 1024, 32, 4, mask_p=0.1, seed=21)
