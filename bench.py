@@ -215,7 +215,7 @@ EV_PER_STEP = len(STEP_OPS) + 1
 def headline_config(T, recv_gb, world):
     """The `config` of the headline line (both arms)."""
     return {"workload": f"{HEADLINE}: R=8 T={T} H=7168 E=256 K=8 Gumbel routing A=128 C=12; step = "
-                        "get_dispatch_layout + notify_dispatch + dispatch (bf16, top-k metadata) + "
+                        "get_dispatch_layout + notify_dispatch (one launch) + dispatch (bf16, top-k metadata) + "
                         "combine (received rows, top-k weight reduction)",
             "l2": "no flush; inputs larger than L2 (x 470 MB, receive buffer %.2f GB vs 129 MB L2)" % recv_gb,
             "parallelism": "replicas" if world > 1 else "single GPU, R=8 virtual ranks"}
@@ -274,9 +274,17 @@ def run_ours(args):
 
     # The layout and the dispatch record come from one call (one cooperative launch); the
     # prepared dispatch then moves the rows, so the data kernel has its own pair of events.
+    def layout_notify(idx_in):
+        if args.layout_two_launches:
+            ep.ep_get_dispatch_layout(h, idx_in, **lay)
+            ep.ep_notify_dispatch(h, lay["num_tokens_per_rank"], lay["is_token_in_rank"],
+                                  lay["num_tokens_per_expert"], num_recv_tokens_per_expert=nrpe)
+        else:
+            ep.ep_layout_notify(h, idx_in, num_recv_tokens_per_expert=nrpe, **lay)
+
     def step(idx_in, w_in, x_in, ev=None, base=0):
         if ev: ev.rec(base, stream)
-        ep.ep_layout_notify(h, idx_in, num_recv_tokens_per_expert=nrpe, **lay)
+        layout_notify(idx_in)
         if ev: ev.rec(base + 1, stream)
         ep.ep_dispatch(h, x_in, topk_idx=idx_in, topk_weights=w_in, recv_x=recv_x, recv_topk_idx=recv_i,
                        recv_topk_weights=recv_w, prepared=True)
@@ -306,16 +314,21 @@ def run_ours(args):
              for j, name in enumerate(STEP_OPS)}
 
     # the layout and the record as one launch against the two separate calls (same outputs)
-    ln_one = timed(lambda: ep.ep_layout_notify(h, idx_d, num_recv_tokens_per_expert=nrpe, **lay), 10, stream)
+    layout_notify = None
+    if not args.no_ops:
+        ln_one = None if args.layout_two_launches else \
+            timed(lambda: ep.ep_layout_notify(h, idx_d, num_recv_tokens_per_expert=nrpe, **lay), 10, stream)
 
-    def two_calls():
-        ep.ep_get_dispatch_layout(h, idx_d, **lay)
-        ep.ep_notify_dispatch(h, lay["num_tokens_per_rank"], lay["is_token_in_rank"], lay["num_tokens_per_expert"],
-                              num_recv_tokens_per_expert=nrpe)
+        def two_calls():
+            ep.ep_get_dispatch_layout(h, idx_d, **lay)
+            ep.ep_notify_dispatch(h, lay["num_tokens_per_rank"], lay["is_token_in_rank"],
+                                  lay["num_tokens_per_expert"], num_recv_tokens_per_expert=nrpe)
 
-    ln_two = timed(two_calls, 10, stream)
-    h.check()
-    layout_notify = {"one_launch_us": round(ln_one * 1e3, 2), "two_launches_us": round(ln_two * 1e3, 2)}
+        ln_two = timed(two_calls, 10, stream)
+        h.check()
+        layout_notify = {"one_launch_us": round(ln_one * 1e3, 2) if ln_one else None,
+                         "two_launches_us": round(ln_two * 1e3, 2),
+                         "step_uses": "two launches" if args.layout_two_launches else "one launch"}
 
     bm = normal_bytes(R, T, H, K, hits)
     payload = bm["dispatch"]["payload"] + bm["combine"]["payload"]
@@ -368,7 +381,7 @@ def run_ours(args):
                 uploaded[b].record(up)
             stream.wait_event(uploaded[b])
             stream.wait_event(downloaded[b])         # this output set has been read back
-            ep.ep_layout_notify(h, idx_in[b], num_recv_tokens_per_expert=nrpe, **lay)
+            layout_notify(idx_in[b])
             ep.ep_dispatch(h, x_in[b], topk_idx=idx_in[b], topk_weights=w_in[b], recv_x=recv_x,
                            recv_topk_idx=recv_i, recv_topk_weights=recv_w, prepared=True)
             ep.ep_combine(h, recv_x, topk_weights=recv_w, combined_x=outs[b], combined_topk_weights=outws[b])
@@ -429,7 +442,8 @@ def run_ours(args):
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "traffic": traffic, "algorithmic_bytes": dom_bytes},
         "cpu_baseline": cpu, "clocks": clocks.summary(), "e2e": e2e,
-        "gpu_launches": 3 * args.steps,  # layout + notify (one launch), dispatch, combine per step
+        "gpu_launches": (4 if args.layout_two_launches else 3) * args.steps,  # per step: layout + notify
+                                                                              # (one or two), dispatch, combine
         "wall_s_timed": round(wall, 3), "ops": ops,
     }
     if rank == 0:
@@ -788,6 +802,9 @@ def main():
     ap.add_argument("--fp8-calls", type=int, default=0,
                     help="only run the fp8_zipf FP8 dispatch (fresh record, cast) this many times (profiling)")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--layout-two-launches", action="store_true",
+                    help="run the step's layout and notify as two launches (for profilers, which cannot launch "
+                         "the one-launch cooperative kernel)")
     ap.add_argument("--tokens", type=int, default=0,
                     help="tokens per rank of the headline workload (0 = its full 4096; smaller only for profiling)")
     args = ap.parse_args()
