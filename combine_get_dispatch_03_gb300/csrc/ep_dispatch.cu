@@ -25,7 +25,11 @@ namespace {
 
 constexpr int kDispatchUnroll = 4;  // 16-byte vectors in flight per lane (payload read)
 constexpr int kCombineUnroll = 2;   // 16-byte columns per lane per pass
-constexpr int kCombineFanIn = 4;    // source rows loaded together before accumulation
+// Source rows loaded together before accumulation: all of them up to 8 ranks (one batch), else
+// batches of 4 (measured on the 7168-wide workloads: 452 against 460 us at R = 8, and 1351
+// against 1399 us at R = 16, for the 8- and 4-row batches respectively).
+constexpr int kCombineFanInSmallR = 8;
+constexpr int kCombineFanIn = 4;
 constexpr int kCombineWeightRanks = 8;  // source ranks whose top-k weights are loaded ahead of the rows
 constexpr bool kUseBulkDispatch = true;  // bulk-copy (TMA 1D) dispatch where the rows fit in shared memory
 // Shared memory for the stages of one CTA (bf16, cast, FP8 input).  The cast keeps fewer stages
@@ -337,7 +341,7 @@ __global__ void dispatch_bulk_kernel(int R, int T, int H, int K, int EL, int64_t
     if (tid == 0) bulk_wait_all();
 }
 
-template <bool kOutF32>
+template <bool kOutF32, int kFanIn>
 __global__ void __launch_bounds__(kCombineThreads)
     combine_kernel(int R, int T, int H, int K, int64_t cap, const int32_t* __restrict__ send_head,
                    const int4* __restrict__ y, const float* __restrict__ recv_w, const int4* __restrict__ bias0,
@@ -389,17 +393,17 @@ __global__ void __launch_bounds__(kCombineThreads)
             }
             unsigned m = src_ranks;
             while (m) {
-                int rk[kCombineFanIn];
-                int64_t rr[kCombineFanIn];
+                int rk[kFanIn];
+                int64_t rr[kFanIn];
 #pragma unroll
-                for (int j = 0; j < kCombineFanIn; ++j) {
+                for (int j = 0; j < kFanIn; ++j) {
                     rk[j] = m ? __ffs(m) - 1 : -1;
                     if (m) m &= m - 1;
                     rr[j] = __shfl_sync(kFullMask, row, rk[j] < 0 ? 0 : rk[j]);
                 }
-                int4 v[kCombineFanIn][kCombineUnroll];
+                int4 v[kFanIn][kCombineUnroll];
 #pragma unroll
-                for (int j = 0; j < kCombineFanIn; ++j)
+                for (int j = 0; j < kFanIn; ++j)
 #pragma unroll
                     for (int u = 0; u < kCombineUnroll; ++u) {
                         const int i = i0 + u * kWarpSize + lane;
@@ -407,7 +411,7 @@ __global__ void __launch_bounds__(kCombineThreads)
                             v[j][u] = ld_stream_v4(y + (static_cast<int64_t>(rk[j]) * cap + rr[j]) * n16 + i);
                     }
 #pragma unroll
-                for (int j = 0; j < kCombineFanIn; ++j) {
+                for (int j = 0; j < kFanIn; ++j) {
                     if (rk[j] < 0) continue;
 #pragma unroll
                     for (int u = 0; u < kCombineUnroll; ++u) {
@@ -500,8 +504,10 @@ cudaError_t plan_dispatch_combine(LaunchPlan* plan, int H) {
     plan->dispatch_blocks[kModeBf16] = resident_blocks(dispatch_kernel<kModeBf16>, kDispatchThreads, n);
     plan->dispatch_blocks[kModeCastFp8] = resident_blocks(dispatch_kernel<kModeCastFp8>, kDispatchThreads, n);
     plan->dispatch_blocks[kModeFp8In] = resident_blocks(dispatch_kernel<kModeFp8In>, kDispatchThreads, n);
-    plan->combine_blocks[0] = resident_blocks(combine_kernel<false>, kCombineThreads, n);
-    plan->combine_blocks[1] = resident_blocks(combine_kernel<true>, kCombineThreads, n);
+    plan->combine_blocks[0] = resident_blocks(combine_kernel<false, kCombineFanIn>, kCombineThreads, n);
+    plan->combine_blocks[1] = resident_blocks(combine_kernel<true, kCombineFanIn>, kCombineThreads, n);
+    plan->combine_blocks[2] = resident_blocks(combine_kernel<false, kCombineFanInSmallR>, kCombineThreads, n);
+    plan->combine_blocks[3] = resident_blocks(combine_kernel<true, kCombineFanInSmallR>, kCombineThreads, n);
     return cudaGetLastError();
 }
 
@@ -547,11 +553,15 @@ cudaError_t launch_combine(const LaunchPlan& plan, bool out_fp32, int R, int T, 
                            cudaStream_t stream) {
     const int64_t n_tokens = static_cast<int64_t>(R) * T;
     if (n_tokens == 0) return cudaSuccess;
-    const int grid = clamp_grid(plan.combine_blocks[out_fp32 ? 1 : 0], n_tokens, kCombineThreads / kWarpSize);
+    const bool small_r = R <= kCombineFanInSmallR;
+    const int grid = clamp_grid(plan.combine_blocks[(out_fp32 ? 1 : 0) + (small_r ? 2 : 0)], n_tokens,
+                                kCombineThreads / kWarpSize);
     const int4* yv = static_cast<const int4*>(y);
     const int4* b0 = static_cast<const int4*>(bias0);
     const int4* b1 = static_cast<const int4*>(bias1);
-    auto kernel = out_fp32 ? combine_kernel<true> : combine_kernel<false>;
+    auto kernel = small_r ? (out_fp32 ? combine_kernel<true, kCombineFanInSmallR>
+                                      : combine_kernel<false, kCombineFanInSmallR>)
+                          : (out_fp32 ? combine_kernel<true, kCombineFanIn> : combine_kernel<false, kCombineFanIn>);
     return launch_kernel(kernel, dim3(grid), dim3(kCombineThreads), 0, stream, 1, R, T, H, K, cap, send_head, yv,
                          recv_topk_weights, b0, b1, out, combined_topk_weights);
 }

@@ -13,9 +13,10 @@ struct LaunchPlan {
     int num_sms = 0;        // SMs the data kernels may fill: the device's, or ep_config.max_sms if fewer
     bool sm_limited = false;  // num_sms was capped by max_sms: one resident wave covers all tokens
     int dispatch_blocks[3] = {0, 0, 0};  // per payload mode
-    int combine_blocks[2] = {0, 0};      // bf16 out, fp32 out
+    int combine_blocks[4] = {0, 0, 0, 0};  // bf16 out, fp32 out; then the same with the all-ranks batch
     int ll_dispatch_blocks[2] = {0, 0};  // bf16, fp8
     int ll_combine_blocks = 0;
+    int ll_combine_blocks_small_k = 0;  // the variant with every top-k slot in one batch
     int bulk_stages[3] = {0, 0, 0};      // bulk-copy dispatch: stages per CTA (0 = not usable)
     unsigned bulk_smem[3] = {0, 0, 0};   // its dynamic shared memory
     int bulk_resident[3] = {1, 1, 1};    // its CTAs resident on the GPU at once

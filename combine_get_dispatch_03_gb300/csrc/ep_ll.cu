@@ -33,7 +33,8 @@ namespace {
 constexpr int kLLCountWarps = kLLCountThreads / kWarpSize;
 constexpr int kLLUnroll = 4;
 constexpr int kLLCombineUnroll = 2;
-constexpr int kLLCombineFanIn = 4;
+constexpr int kLLCombineFanIn = 4;         // slots loaded together before accumulation
+constexpr int kLLCombineFanInSmallK = 8;   // ... with top-k up to 8: every slot in one batch
 
 __global__ void __launch_bounds__(kLLCountThreads)
     ll_count_kernel(int R, int T, int maxT, int K, int E, const int64_t* __restrict__ topk_idx,
@@ -408,6 +409,7 @@ __global__ void __launch_bounds__(kLLDispatchThreads)
     }
 }
 
+template <int kFanIn>
 __global__ void __launch_bounds__(kLLCombineThreads)
     ll_combine_kernel(int R, int T, int maxT, int H, int K, int E, const int4* __restrict__ y, int64_t y_row16,
                       const int64_t* __restrict__ topk_idx, const float* __restrict__ topk_weights,
@@ -443,27 +445,27 @@ __global__ void __launch_bounds__(kLLCombineThreads)
                 for (int q = 0; q < 8; ++q) acc[u][q] = 0.0f;
             unsigned m = valid;
             while (m) {
-                int kk[kLLCombineFanIn];
-                int64_t sr[kLLCombineFanIn];
-                float wk[kLLCombineFanIn];
+                int kk[kFanIn];
+                int64_t sr[kFanIn];
+                float wk[kFanIn];
 #pragma unroll
-                for (int j = 0; j < kLLCombineFanIn; ++j) {
+                for (int j = 0; j < kFanIn; ++j) {
                     kk[j] = m ? __ffs(m) - 1 : -1;
                     if (m) m &= m - 1;
                     const int srcl = kk[j] < 0 ? 0 : kk[j];
                     sr[j] = __shfl_sync(kFullMask, src_row, srcl);
                     wk[j] = __shfl_sync(kFullMask, w, srcl);
                 }
-                int4 v[kLLCombineFanIn][kLLCombineUnroll];
+                int4 v[kFanIn][kLLCombineUnroll];
 #pragma unroll
-                for (int j = 0; j < kLLCombineFanIn; ++j)
+                for (int j = 0; j < kFanIn; ++j)
 #pragma unroll
                     for (int u = 0; u < kLLCombineUnroll; ++u) {
                         const int i = i0 + u * kWarpSize + lane;
                         if (kk[j] >= 0 && i < n16) v[j][u] = ld_stream_v4(y + sr[j] * y_row16 + i);
                     }
 #pragma unroll
-                for (int j = 0; j < kLLCombineFanIn; ++j) {
+                for (int j = 0; j < kFanIn; ++j) {
                     if (kk[j] < 0) continue;
 #pragma unroll
                     for (int u = 0; u < kLLCombineUnroll; ++u) {
@@ -524,7 +526,8 @@ cudaError_t plan_ll(LaunchPlan* plan, int num_experts) {
     const int n = plan->num_sms;
     plan->ll_dispatch_blocks[0] = resident_blocks(ll_dispatch_kernel<false>, kLLDispatchThreads, n);
     plan->ll_dispatch_blocks[1] = resident_blocks(ll_dispatch_kernel<true>, kLLDispatchThreads, n);
-    plan->ll_combine_blocks = resident_blocks(ll_combine_kernel, kLLCombineThreads, n);
+    plan->ll_combine_blocks = resident_blocks(ll_combine_kernel<kLLCombineFanIn>, kLLCombineThreads, n);
+    plan->ll_combine_blocks_small_k = resident_blocks(ll_combine_kernel<kLLCombineFanInSmallK>, kLLCombineThreads, n);
     cudaError_t err = cudaFuncSetAttribute(ll_dispatch_bulk_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(kLLBulkMaxSmem));
     if (err == cudaSuccess)
@@ -591,8 +594,11 @@ cudaError_t launch_ll_combine(const LaunchPlan& plan, int R, int T, int maxT, in
                               const int32_t* slot, void* out, cudaStream_t stream) {
     const int64_t n_tokens = static_cast<int64_t>(R) * T;
     if (n_tokens == 0) return cudaSuccess;
-    const int grid = clamp_grid(plan.ll_combine_blocks, n_tokens, kLLCombineThreads / kWarpSize);
-    return launch_kernel(ll_combine_kernel, dim3(grid), dim3(kLLCombineThreads), 0, stream, 1, R, T, maxT, H, K, E,
+    const bool small_k = K <= kLLCombineFanInSmallK;
+    const int grid = clamp_grid(small_k ? plan.ll_combine_blocks_small_k : plan.ll_combine_blocks, n_tokens,
+                                kLLCombineThreads / kWarpSize);
+    auto kernel = small_k ? ll_combine_kernel<kLLCombineFanInSmallK> : ll_combine_kernel<kLLCombineFanIn>;
+    return launch_kernel(kernel, dim3(grid), dim3(kLLCombineThreads), 0, stream, 1, R, T, maxT, H, K, E,
                          static_cast<const int4*>(y), y_row_bytes / 16, topk_idx, topk_weights, slot,
                          static_cast<int4*>(out));
 }
