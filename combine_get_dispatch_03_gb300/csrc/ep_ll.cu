@@ -546,17 +546,16 @@ cudaError_t launch_ll_dispatch(const LaunchPlan& plan, int R, int T, int maxT, i
                                bool use_ue8m0, const int32_t* rank_mask, int32_t* slot, int32_t* cnt,
                                void* recv_msgs, int32_t* packed_recv_count, int64_t* layout_range,
                                int32_t* stats, int32_t* status, cudaStream_t stream) {
-    cudaError_t err = launch_kernel(ll_count_kernel, dim3(R), dim3(kLLCountThreads), ll_count_smem(E), stream, 1,
-            R, T, maxT, K, E, topk_idx, rank_mask, slot, cnt,
-                                                                      status);
+    cudaError_t err = launch_kernel(ll_count_kernel, dim3(R), dim3(kLLCountThreads), ll_count_smem(E), stream, 1, R, T,
+                                    maxT, K, E, topk_idx, rank_mask, slot, cnt, status);
     if (err != cudaSuccess) return err;
     const int fin_threads = 256;
     const int expert_blocks = (E + fin_threads / kWarpSize - 1) / (fin_threads / kWarpSize);
     const int64_t n_slots = static_cast<int64_t>(R) * T * K;
     const int slot_blocks = static_cast<int>((n_slots + fin_threads - 1) / fin_threads);
-    err = launch_kernel(ll_finish_kernel, dim3(expert_blocks + slot_blocks), dim3(fin_threads), 0, stream, 1,
-            
-        R, T, maxT, K, E, expert_blocks, topk_idx, cnt, slot, packed_recv_count, layout_range, stats, status);
+    err = launch_kernel(ll_finish_kernel, dim3(expert_blocks + slot_blocks), dim3(fin_threads), 0, stream, 1, R, T,
+                        maxT, K, E, expert_blocks, topk_idx, static_cast<const int32_t*>(cnt), slot,
+                        packed_recv_count, layout_range, stats, status);
     if (err != cudaSuccess) return err;
     const int64_t n_tokens = static_cast<int64_t>(R) * T;
     if (n_tokens == 0) return cudaSuccess;
