@@ -170,10 +170,11 @@ __global__ void __launch_bounds__(kDispatchThreads)
 // covers all tokens, so the rows in flight on the GPU stay a contiguous window
 // of the token order (a grid-stride walk spreads them out as CTAs drift apart,
 // and measured about 10 % slower on HBM).  Warp 0 lane 0 loads a row with
-// one bulk copy (completion counted on the stage's mbarrier) stages-1 tokens
-// ahead, and writes it to every destination row with one bulk store each; the
-// stores of token j form one bulk group, and a stage is refilled only after
-// the group that read it has finished reading.  In cast mode all warps of the
+// one bulk copy (completion counted on the stage's mbarrier), all stages at
+// the start, and writes it to every destination row with one bulk store each;
+// the stores of token j form one bulk group, and a stage is refilled (only
+// when a CTA has more tokens than stages) one token later, after its group has
+// read it and a block barrier has ordered its metadata's last use.  In cast mode all warps of the
 // CTA turn the staged bf16 row into e4m3 codes + fp32 scales in a second
 // buffer first.  A wait that reaches its iteration cap reports
 // EP_ERR_TIMEOUT, lets the loads already issued land, and leaves.
@@ -248,7 +249,7 @@ __global__ void dispatch_bulk_kernel(int R, int T, int H, int K, int EL, int64_t
     };
 
     if (warp0) {
-        const int64_t pro = n_local < S - 1 ? n_local : S - 1;
+        const int64_t pro = n_local < S ? n_local : S;  // every stage starts full
         for (int64_t j = 0; j < pro; ++j) produce(j);
     }
     int64_t j = 0;
@@ -324,18 +325,21 @@ __global__ void dispatch_bulk_kernel(int R, int T, int H, int K, int EL, int64_t
                 }
                 bulk_commit();
             }
-            // Refill the stage that token j-1 used once its stores have read it.
-            if (j + S - 1 < n_local) {
+            // Refill the stage that token j-1 used with token j-1+S, once its stores have read
+            // it; its metadata was read before this iteration's block barrier.  (A CTA takes at
+            // most S tokens unless max_sms caps the grid, so this is rare.)
+            if (j >= 1 && j - 1 + S < n_local) {
                 if (lane == 0) bulk_wait_read<1>();
                 __syncwarp();
-                produce(j + S - 1);
+                produce(j - 1 + S);
             }
         }
     }
     if (j < n_local && tid == 0) {
         report(status, EP_ERR_TIMEOUT);
         // Let the row loads already issued land before this CTA's shared memory is released.
-        const int64_t issued = (j + S - 1 < n_local) ? j + S - 1 : n_local;
+        const int64_t last = j + S - 1 > S ? j + S - 1 : S;  // tokens loaded so far
+        const int64_t issued = last < n_local ? last : n_local;
         for (int64_t k = j + 1; k < issued; ++k) mbar_wait_bounded(&bars[k % S], static_cast<uint32_t>((k / S) & 1));
     }
     if (tid == 0) bulk_wait_all();

@@ -221,7 +221,7 @@ __global__ void ll_dispatch_bulk_kernel(int R, int T, int maxT, int H, int K, in
     };
 
     if (warp0) {
-        const int64_t pro = n_local < S - 1 ? n_local : S - 1;
+        const int64_t pro = n_local < S ? n_local : S;  // every stage starts full
         for (int64_t j = 0; j < pro; ++j) produce(j);
     }
     int64_t j = 0;
@@ -273,16 +273,16 @@ __global__ void ll_dispatch_bulk_kernel(int R, int T, int maxT, int H, int K, in
                 if (lane == 0) bulk_store(recv_msgs + r * msg_bytes, msg, static_cast<uint32_t>(msg_bytes));
             }
             if (lane == 0) bulk_commit();
-            if (j + S - 1 < n_local) {
-                if (lane == 0) bulk_wait_read<1>();
+            if (j + S < n_local) {  // refill this token's stage once its stores have read it
+                if (lane == 0) bulk_wait_read<0>();
                 __syncwarp();
-                produce(j + S - 1);
+                produce(j + S);
             }
         }
     }
     if (j < n_local && tid == 0) {
         report(status, EP_ERR_TIMEOUT);
-        const int64_t issued = (j + S - 1 < n_local) ? j + S - 1 : n_local;
+        const int64_t issued = (j + S < n_local) ? j + S : n_local;
         for (int64_t k = j + 1; k < issued; ++k) mbar_wait_bounded(&bars[k % S], static_cast<uint32_t>((k / S) & 1));
     }
     if (tid == 0) bulk_wait_all();
