@@ -314,7 +314,7 @@ def run_ours(args):
              for j, name in enumerate(STEP_OPS)}
 
     # the layout and the record as one launch against the two separate calls (same outputs)
-    layout_notify = None
+    layout_notify_times = None
     if not args.no_ops:
         ln_one = None if args.layout_two_launches else \
             timed(lambda: ep.ep_layout_notify(h, idx_d, num_recv_tokens_per_expert=nrpe, **lay), 10, stream)
@@ -326,7 +326,7 @@ def run_ours(args):
 
         ln_two = timed(two_calls, 10, stream)
         h.check()
-        layout_notify = {"one_launch_us": round(ln_one * 1e3, 2) if ln_one else None,
+        layout_notify_times = {"one_launch_us": round(ln_one * 1e3, 2) if ln_one else None,
                          "two_launches_us": round(ln_two * 1e3, 2),
                          "step_uses": "two launches" if args.layout_two_launches else "one launch"}
 
@@ -341,7 +341,8 @@ def run_ours(args):
     dom = max(("dispatch", "combine"), key=lambda k: op_ms[k])
     dom_bytes = total(bm[dom])
     achieved = dom_bytes / (op_ms[dom] / 1e3) / 1e9
-    kernel_name = "dispatch_bulk_kernel<0>" if dom == "dispatch" else "combine_kernel<false>"
+    kernel_name = "dispatch_bulk_kernel<0>" if dom == "dispatch" else \
+        ("combine_kernel<false, 8>" if R <= 8 else "combine_kernel<false, 4>")  # all rows in one batch at R <= 8
     traffic = recorded_traffic(kernel_name)
 
     # End to end through the binding: every step copies its inputs from pinned host memory and its
@@ -435,7 +436,7 @@ def run_ours(args):
         "config": headline_config(T, R * cap * H * 2 / 1e9, world),
         "tokens_per_s": round(R * T * world / (elapsed / args.steps), 1),
         "launch_model": launch_model,
-        "layout_notify": layout_notify,
+        "layout_notify": layout_notify_times,
         "hbm_frac_step": round(alg / (step_ms / 1e3) / 1e9 / peak, 4),
         "op_ms": {k: round(v, 4) for k, v in op_ms.items()},
         "roofline": {"bound": "hbm", "kernel": kernel_name, "achieved": round(achieved, 1), "peak": peak,
