@@ -469,6 +469,29 @@ def timed(fn, reps, stream, warmup=3, batches=5):
     return statistics.median(times)
 
 
+def l2_bytes(dev):
+    """The device's L2 size (129 MB on GB300 if the property is missing)."""
+    return int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 129 << 20))
+
+
+def timed_cold(fn, reps, stream, flush, warmup=3):
+    """Time of one call that starts with a cold L2: `flush` (a buffer twice the L2) is written
+    before each call, outside the events; median over `reps` calls."""
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    times = []
+    for _ in range(reps):
+        flush.zero_()
+        a.record(stream)
+        fn()
+        b.record(stream)
+        b.synchronize()
+        times.append(a.elapsed_time(b))
+    return statistics.median(times)
+
+
 def measure_launch_model(ep, dev, peak, st, reps=10, probe_sms=(16, 32)):
     """The SM-count model on the headline workload: per-SM rates of the dispatch (writes) and the
     combine (reads) measured with max_sms capping the data kernels, the SM counts the model then
@@ -662,14 +685,21 @@ def measure_other_ops(ep, dev, peak, reps=10):
     fn = lambda: ep.ep_ll_dispatch(h, x_d, idx_d, use_fp8=True, use_ue8m0=True, recv_msgs=msgs,
                                    packed_recv_count=cnt, packed_recv_layout_range=rng_)
     ms_d = timed(fn, reps, stream)
+    flush = torch.empty(2 * l2_bytes(dev), dtype=torch.uint8, device=dev)
+    cold_d = timed_cold(fn, 2 * reps, stream, flush)
     y = W.normal_bf16((shape.R, shape.EL, shape.R * shape.max_tokens, shape.H), shape.seed, "lly", device=dev)
     out = torch.empty((shape.R, shape.T, shape.H), dtype=torch.bfloat16, device=dev)
     ms_c = timed(lambda: ep.ep_ll_combine(h, y, idx_d, w_d, combined_x=out), reps, stream)
+    cold_c = timed_cold(lambda: ep.ep_ll_combine(h, y, idx_d, w_d, combined_x=out), 2 * reps, stream, flush)
     h.check()
     n_valid = int((idx >= 0).sum())
     b = ll_bytes(shape.R, shape.T, shape.H, shape.K, n_valid, msg)
-    report("ll_v3.ll_dispatch_fp8_ue8m0", ms_d, b["ll_dispatch"])
-    report("ll_v3.ll_combine", ms_c, b["ll_combine"])
+    warm = "calls back to back (the 58.7 MB of tokens can stay in the 129 MB L2)"
+    report("ll_v3.ll_dispatch_fp8_ue8m0", ms_d, b["ll_dispatch"],
+           {"note": warm, "cold_us": round(cold_d * 1e3, 2), "cold_note": "L2 written over before each call"})
+    report("ll_v3.ll_combine", ms_c, b["ll_combine"],
+           {"note": warm, "cold_us": round(cold_c * 1e3, 2), "cold_note": "L2 written over before each call"})
+    del flush
     h.destroy()
     del msgs, y, out
     torch.cuda.empty_cache()
@@ -702,7 +732,12 @@ def measure_other_ops(ep, dev, peak, reps=10):
     b = normal_bytes(R, T, H, K, st["hits"])
     step_b = {"payload": b["dispatch"]["payload"] + b["combine"]["payload"],
               "meta": sum(v["meta"] for v in b.values())}
-    report("normal_small.step", ms, step_b, {"note": "L2-resident; eager calls, launch-bound"})
+    flush = torch.empty(2 * l2_bytes(dev), dtype=torch.uint8, device=dev)
+    cold = timed_cold(small_step, 2 * reps, stream, flush)
+    del flush
+    report("normal_small.step", ms, step_b, {"note": "L2-resident; eager calls, launch-bound",
+                                             "cold_us": round(cold * 1e3, 2),
+                                             "cold_note": "L2 written over before each step"})
     side = torch.cuda.Stream(dev)
     side.wait_stream(stream)
     with torch.cuda.stream(side):
