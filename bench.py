@@ -637,8 +637,20 @@ def measure_other_ops(ep, dev, peak, reps=10):
     report("fp8_zipf.dispatch_fp8", ms, {"payload": b["dispatch"]["payload"],
                                          "meta": b["dispatch"]["meta"] + total(b["notify"])},
            {"rho": round(st["hits"] / (shape.R * shape.T), 3)})
+    # FP8 input (already cast: e4m3 codes and fp32 scales), cached record: bytes are moved as they are
+    n, G = shape.R * shape.T, shape.H // 128
+    x8 = torch.randint(0, 126, (shape.R, shape.T, shape.H), dtype=torch.uint8, device=dev).view(torch.float8_e4m3fn)
+    xs = torch.rand((shape.R, shape.T, G), dtype=torch.float32, device=dev)
+    fn8 = lambda: ep.ep_dispatch(h, x8, x_scales=xs, cached=True, recv_x=bufs["recv_x"],
+                                 recv_x_scales=bufs["recv_x_scales"])
+    ms8 = timed(fn8, reps, stream)
+    h.check()
+    row8 = shape.H + 4 * G
+    report("fp8_zipf.dispatch_fp8_input_cached", ms8,
+           {"payload": n * row8 + st["hits"] * row8, "meta": n * shape.R * 4},
+           {"note": "e4m3 codes + fp32 scales in, moved unchanged; record of the cast dispatch reused"})
     h.destroy()
-    del bufs, st, lay
+    del bufs, st, lay, x8, xs
     torch.cuda.empty_cache()
 
     # combine-heavy: cached record, fresh expert outputs, two biases, weight reduction
