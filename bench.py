@@ -407,10 +407,41 @@ def run_ours(args):
         barrier(world)
         e2e_ms = e0.elapsed_time(e1) / e2e_steps
         el, un = reduce_replicas(e2e_ms * e2e_steps / 1e3, payload * e2e_steps, world)
+        h2d_b = x_h[0].numel() * 2 + idx_h[0].numel() * 8 + w_h[0].numel() * 4
+        d2h_b = out_h[0].numel() * 2 + outw_h[0].numel() * 4
+
+        # the host link alone: the same copies with no compute, each way and both ways at once
+        def copies(do_up, do_down, reps=5):
+            a_, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize(dev)
+            a_.record(up)
+            down.wait_event(a_)
+            for r in range(reps):
+                b = r % n_in
+                if do_up:
+                    with torch.cuda.stream(up):
+                        x_in[b].copy_(x_h[b], non_blocking=True)
+                        idx_in[b].copy_(idx_h[b], non_blocking=True)
+                        w_in[b].copy_(w_h[b], non_blocking=True)
+                if do_down:
+                    with torch.cuda.stream(down):
+                        out_h[b].copy_(outs[b], non_blocking=True)
+                        outw_h[b].copy_(outws[b], non_blocking=True)
+            up.wait_stream(down)
+            b_.record(up)
+            torch.cuda.synchronize(dev)
+            return a_.elapsed_time(b_) / reps
+
+        up_ms, down_ms, both_ms = copies(True, False), copies(False, True), copies(True, True)
         e2e = {"value": round(un / el / 1e9, 2), "unit": "GB/s", "ms_per_step": round(e2e_ms, 4),
                "steps": e2e_steps, "pipelined": "upload / compute / download on three streams, two buffer sets",
-               "h2d_bytes_per_step": x_h[0].numel() * 2 + idx_h[0].numel() * 8 + w_h[0].numel() * 4,
-               "d2h_bytes_per_step": out_h[0].numel() * 2 + outw_h[0].numel() * 4}
+               "h2d_bytes_per_step": h2d_b, "d2h_bytes_per_step": d2h_b,
+               "host_link": {"h2d_gbs": round(h2d_b / up_ms / 1e6, 1), "d2h_gbs": round(d2h_b / down_ms / 1e6, 1),
+                             "both_ways_gbs": round((h2d_b + d2h_b) / both_ms / 1e6, 1),
+                             "copies_ms_per_step": round(both_ms, 4),
+                             "frac": round(both_ms / e2e_ms, 4),
+                             "note": "one step's copies with no compute, both ways at once; frac = that time / "
+                                     "the e2e step: the e2e number is bound by the host link"}}
         h.check()
         del x_in, idx_in, w_in, outs, outws
 
