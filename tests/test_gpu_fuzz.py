@@ -1,9 +1,11 @@
 """Seeded random shapes across the ABI's limits, every output against the oracle.
 
 Each case draws R, experts per rank, top-k, tokens (0 included), hidden (down to 8 channels),
-channels, alignment, routing and masking; runs the one-call layout + record, the prepared
-dispatch (bf16, and the FP8 cast when H allows), the combine with biases and fp32 output, and
-the LL dispatch (bf16 and, when H allows, FP8 + UE8M0) and combine."""
+channels, alignment, routing, masked slots, an SM cap for the data kernels and a masked rank for
+the LL path.  It runs the one-call layout + record (with the node-level record when the ranks
+form whole nodes of 8), the prepared bf16 dispatch, the combine with biases and fp32 output, the
+cached FP8 cast and FP8-input dispatches when H allows, and the LL dispatch (bf16 and, when H
+allows, FP8 + UE8M0) and combine."""
 import numpy as np
 import pytest
 import torch
@@ -32,18 +34,21 @@ def draw(i):
     A = int(g.choice([1, 4, 128]))
     routing = str(g.choice(["uniform", "zipf", "gumbel"]))
     mask_p = float(g.choice([0.0, 0.1, 0.5]))
-    return W.Shape(f"fuzz{i}", R=R, T=T, H=H, E=E, K=K, routing=routing, C=C, A=A, mask_p=mask_p,
-                   max_tokens=max(T, 1) + int(g.integers(0, 4)), seed=30000 + i)
+    shape = W.Shape(f"fuzz{i}", R=R, T=T, H=H, E=E, K=K, routing=routing, C=C, A=A, mask_p=mask_p,
+                    max_tokens=max(T, 1) + int(g.integers(0, 4)), seed=30000 + i)
+    max_sms = int(g.choice([0, 0, 0, 1, 3, 16]))     # data kernels capped to this many SMs' worth
+    ll_masked = int(g.integers(-1, R)) if R > 1 else -1  # a rank masked in the LL path, or none
+    return shape, max_sms, ll_masked
 
 
 @pytest.mark.parametrize("i", range(N_CASES))
 def test_fuzz_normal_and_ll(i):
-    shape = draw(i)
+    shape, max_sms, ll_masked = draw(i)
     idx, w = W.routing(shape)
     x = W.tokens_x(shape)
     xb = W.bf16_bits(x)
     cap = max(P.needed_capacity(idx, shape.E), 1)
-    h = ep.Handle(P.config_of(shape, cap))
+    h = ep.Handle(P.config_of(shape, cap, max_sms))
     idx_d, w_d, x_d = torch.from_numpy(idx).to(P.DEV), torch.from_numpy(w).to(P.DEV), x.to(P.DEV)
 
     # layout and record in one call, then the prepared dispatch and the combine
@@ -55,6 +60,10 @@ def test_fuzz_normal_and_ll(i):
     P.compare_layout(lay, ora_lay)
     P.compare_record(h, ora_n, shape.T)
     np.testing.assert_array_equal(P.host(lay["num_recv_tokens_per_expert"]), ora_n["num_recv_tokens_per_expert"])
+    if shape.R > 8 and shape.R % 8 == 0:  # whole nodes of 8: the node-level record
+        ora_rdma = O.rdma_prefix(ora_lay["is_token_in_rank"], shape.C)
+        for key in ("rdma_channel_prefix_matrix", "recv_rdma_rank_prefix_sum"):
+            np.testing.assert_array_equal(P.host(h.export(key)), ora_rdma[key], err_msg=f"{key} {shape}")
     d = ep.ep_dispatch(h, x_d, topk_idx=idx_d, topk_weights=w_d, prepared=True)
     assert h.status() == 0, shape
     ora_d = O.dispatch(xb, ora_n["send_head"], cap, shape.E, topk_idx=idx, topk_weights=w)
@@ -77,15 +86,32 @@ def test_fuzz_normal_and_ll(i):
         ora8 = O.dispatch(xb, ora_n["send_head"], cap, shape.E, mode=O.MODE_CAST_FP8)
         np.testing.assert_array_equal(P.host(d8["recv_x"])[rows], ora8["recv_x"][rows], err_msg=str(shape))
         np.testing.assert_array_equal(P.host(d8["recv_x_scales"])[rows], ora8["recv_x_scales"][rows])
+        # FP8 input: e4m3 codes (no NaN codes) and fp32 scales moved unchanged
+        g = np.random.default_rng(shape.seed + 11)
+        codes = g.integers(0, 256, (shape.R, shape.T, shape.H), dtype=np.uint8)
+        codes[(codes & 0x7F) == 0x7F] = 0
+        xs = g.random((shape.R, shape.T, shape.H // 128), dtype=np.float32)
+        dq = ep.ep_dispatch(h, torch.from_numpy(codes).to(P.DEV).view(torch.float8_e4m3fn), cached=True,
+                            x_scales=torch.from_numpy(xs).to(P.DEV))
+        assert h.status() == 0, shape
+        oraq = O.dispatch(codes, ora_n["send_head"], cap, shape.E, mode=O.MODE_FP8_IN, x_scales=xs)
+        np.testing.assert_array_equal(P.host(dq["recv_x"])[rows], oraq["recv_x"][rows], err_msg=str(shape))
+        np.testing.assert_array_equal(P.host(dq["recv_x_scales"])[rows], oraq["recv_x_scales"][rows])
     h.destroy()
 
     # low-latency dispatch and combine
     maxT = shape.max_tokens
+    mask = None
+    if ll_masked >= 0:
+        mask = np.zeros(shape.R, np.int32)
+        mask[ll_masked] = 1
     for use_fp8 in ([False, True] if shape.H % 512 == 0 else [False]):
-        hl = ep.Handle(P.config_of(shape, 0))
+        hl = ep.Handle(P.config_of(shape, 0, max_sms))
+        if mask is not None:
+            ep.ep_update_mask_buffer(hl, ll_masked, True)
         out = ep.ep_ll_dispatch(hl, x_d, idx_d, use_fp8=use_fp8, use_ue8m0=use_fp8)
         assert hl.status() == 0, shape
-        ora = O.ll_dispatch(xb, idx, maxT, shape.E, use_fp8=use_fp8, use_ue8m0=use_fp8)
+        ora = O.ll_dispatch(xb, idx, maxT, shape.E, use_fp8=use_fp8, use_ue8m0=use_fp8, rank_mask=mask)
         np.testing.assert_array_equal(P.host(out["packed_recv_count"]), ora["packed_recv_count"])
         np.testing.assert_array_equal(P.host(out["packed_recv_layout_range"]), ora["packed_recv_layout_range"])
         np.testing.assert_array_equal(P.host(hl.export("ll_slot_row"))[:, :shape.T], ora["slot_row"])
