@@ -457,8 +457,7 @@ def run_ours(args):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
-        cpu = cpu_baseline(W.WORKLOADS[HEADLINE], tokens=max(64, W.WORKLOADS[HEADLINE].T // args.cpu_fraction),
-                           reps=2)
+        cpu = cpu_baseline(W.WORKLOADS[HEADLINE], args.cpu_seconds)
 
     result = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
@@ -825,18 +824,29 @@ def cpu_describe(shape, tokens):
             "layout + notify + dispatch + combine, single-threaded C oracle")
 
 
-def cpu_baseline(shape, tokens: int, reps: int = 1):
-    """The CPU oracle, as it stands, timed on a bounded sample of the workload (best of reps)."""
+def cpu_tokens(shape, budget_s: float, passes: int) -> int:
+    """Tokens per rank of the oracle sample so that `passes` passes take about budget_s seconds: one
+    pass over 64 tokens per rank gives the oracle's cost per token (its work is linear in tokens)."""
+    sub, idx, w, x = cpu_sample(shape, 64)
+    dt, _ = cpu_step(sub, idx, w, x)
+    t = int(budget_s / passes / (dt / 64)) // 64 * 64
+    return max(64, min(shape.T, t))
+
+
+def cpu_baseline(shape, budget_s: float, passes: int = 3):
+    """The CPU oracle, as it stands, timed over `passes` passes of a sample of the workload sized to
+    about budget_s seconds of CPU work in all."""
+    tokens = cpu_tokens(shape, budget_s, passes)
     sub, idx, w, x = cpu_sample(shape, tokens)
-    best, hits = None, 0
-    for _ in range(reps):
+    total, hits = 0.0, 0
+    for _ in range(passes):
         dt, hits = cpu_step(sub, idx, w, x)
-        best = dt if best is None else min(best, dt)
+        total += dt
     b = normal_bytes(sub.R, tokens, sub.H, sub.K, hits)
     payload = b["dispatch"]["payload"] + b["combine"]["payload"]
-    return {"value": round(payload / best / 1e9, 3), "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": cpu_describe(shape, tokens), "seconds": round(best, 3),
-            "tokens_per_s": round(sub.R * tokens / best, 1)}
+    return {"value": round(payload * passes / total / 1e9, 3), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{cpu_describe(shape, tokens)}; {passes} passes", "seconds": round(total, 3),
+            "tokens_per_s": round(sub.R * tokens * passes / total, 1)}
 
 
 def run_reference(args):
@@ -845,7 +855,7 @@ def run_reference(args):
     if rank != 0:
         return
     shape = W.WORKLOADS[HEADLINE]
-    tokens = max(64, shape.T // args.cpu_fraction)
+    tokens = cpu_tokens(shape, args.reference_seconds, args.warmup + args.steps)
     sub, idx, w, x = cpu_sample(shape, tokens)
     for _ in range(args.warmup):
         cpu_step(sub, idx, w, x)
@@ -873,7 +883,10 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--e2e-steps", type=int, default=50)
-    ap.add_argument("--cpu-fraction", type=int, default=8, help="oracle sample = T / this many tokens per rank")
+    ap.add_argument("--cpu-seconds", type=float, default=24.0,
+                    help="CPU work of the oracle baseline (three passes of a sample sized to it)")
+    ap.add_argument("--reference-seconds", type=float, default=120.0,
+                    help="--impl reference: the warm-up and timed steps together take about this long")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-ops", action="store_true")
     ap.add_argument("--ll-calls", type=int, default=0,
