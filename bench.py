@@ -455,9 +455,10 @@ def run_ours(args):
         torch.cuda.empty_cache()
         ops = measure_other_ops(ep, dev, peak)
 
-    cpu = None
+    cpu = cpu_all = None
     if rank == 0 and world == 1 and not args.no_cpu:
         cpu = cpu_baseline(W.WORKLOADS[HEADLINE], args.cpu_seconds)
+        cpu_all = cpu_baseline_all_cores(W.WORKLOADS[HEADLINE], args.cpu_seconds)
 
     result = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
@@ -472,7 +473,7 @@ def run_ours(args):
         "roofline": {"bound": "hbm", "kernel": kernel_name, "achieved": round(achieved, 1), "peak": peak,
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "traffic": traffic, "algorithmic_bytes": dom_bytes},
-        "cpu_baseline": cpu, "clocks": clocks.summary(), "e2e": e2e,
+        "cpu_baseline": cpu, "cpu_baseline_all_cores": cpu_all, "clocks": clocks.summary(), "e2e": e2e,
         "gpu_launches": (4 if args.layout_two_launches else 3) * args.steps,  # per step: layout + notify
                                                                               # (one or two), dispatch, combine
         "wall_s_timed": round(wall, 3), "ops": ops,
@@ -819,9 +820,36 @@ def cpu_step(sub, idx, w, x):
     return time.perf_counter() - t0, int(lay["num_tokens_per_rank"].sum())
 
 
-def cpu_describe(shape, tokens):
+def cpu_step_threads(sub, idx, w, x, threads: int):
+    """The same oracle pass with the dispatch and combine token loops split over `threads` host
+    threads, contiguous token blocks each (the oracle's C calls release the interpreter lock; the
+    blocks write disjoint rows of the shared outputs).  Layout and notify stay single-threaded."""
+    import oracle as O
+    from concurrent.futures import ThreadPoolExecutor
+    t0 = time.perf_counter()
+    lay = O.get_dispatch_layout(idx, sub.E, with_rdma=sub.R > 8)
+    cap = int(lay["num_tokens_per_rank"].sum(axis=0).max())
+    n = O.dispatch_notify(lay["num_tokens_per_rank"], lay["is_token_in_rank"], lay["num_tokens_per_expert"],
+                          sub.C, sub.A, cap)
+    blocks = np.array_split(np.arange(sub.R * sub.T, dtype=np.int64), threads)
+    d = dict(recv_x=np.zeros((sub.R, cap, sub.H), np.uint16),
+             recv_topk_idx=np.full((sub.R, cap, sub.K), -2, np.int64),
+             recv_topk_weights=np.full((sub.R, cap, sub.K), np.nan, np.float32))
+    c = dict(out=np.zeros((sub.R, sub.T, sub.H), np.uint16),
+             combined_topk_weights=np.zeros((sub.R, sub.T, sub.K), np.float32))
+    with ThreadPoolExecutor(threads) as ex:
+        list(ex.map(lambda b: O.dispatch(x, n["send_head"], cap, sub.E, topk_idx=idx, topk_weights=w, tokens=b,
+                                         out=d), blocks))
+        list(ex.map(lambda b: O.combine(d["recv_x"], n["send_head"], recv_topk_weights=d["recv_topk_weights"],
+                                        tokens=b, out=c), blocks))
+    return time.perf_counter() - t0, int(lay["num_tokens_per_rank"].sum())
+
+
+def cpu_describe(shape, tokens, threads: int = 1):
+    how = "single-threaded C oracle" if threads == 1 else \
+        f"C oracle with its dispatch and combine token loops over {threads} threads"
     return (f"{HEADLINE} restricted to the first {tokens} of {shape.T} tokens of each of the {shape.R} ranks: "
-            "layout + notify + dispatch + combine, single-threaded C oracle")
+            f"layout + notify + dispatch + combine, {how}")
 
 
 def cpu_tokens(shape, budget_s: float, passes: int) -> int:
@@ -846,6 +874,24 @@ def cpu_baseline(shape, budget_s: float, passes: int = 3):
     payload = b["dispatch"]["payload"] + b["combine"]["payload"]
     return {"value": round(payload * passes / total / 1e9, 3), "unit": "GB/s", "cores": 1, "kind": "oracle",
             "sample": f"{cpu_describe(shape, tokens)}; {passes} passes", "seconds": round(total, 3),
+            "tokens_per_s": round(sub.R * tokens * passes / total, 1)}
+
+
+def cpu_baseline_all_cores(shape, budget_s: float, passes: int = 3):
+    """The same oracle with its dispatch and combine token loops split over every host core the
+    process may run on; the sample is sized like cpu_baseline's, scaled by the core count."""
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+    tokens = cpu_tokens(shape, budget_s * cores, passes)
+    sub, idx, w, x = cpu_sample(shape, tokens)
+    total, hits = 0.0, 0
+    for _ in range(passes):
+        dt, hits = cpu_step_threads(sub, idx, w, x, cores)
+        total += dt
+    b = normal_bytes(sub.R, tokens, sub.H, sub.K, hits)
+    payload = b["dispatch"]["payload"] + b["combine"]["payload"]
+    return {"value": round(payload * passes / total / 1e9, 3), "unit": "GB/s", "cores": cores,
+            "kind": "oracle",
+            "sample": f"{cpu_describe(shape, tokens, cores)}; {passes} passes", "seconds": round(total, 3),
             "tokens_per_s": round(sub.R * tokens * passes / total, 1)}
 
 

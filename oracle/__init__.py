@@ -241,13 +241,24 @@ def dispatch(x, send_head, capacity: int, num_experts: int, mode: int = MODE_BF1
 
 
 def combine(y, send_head, recv_topk_weights=None, bias0=None, bias1=None, out_fp32=False,
-            tokens=None, num_topk: int = 1):
-    """Normal combine: fp32 sum of every receiving rank's row (+ biases)."""
+            tokens=None, num_topk: int = 1, out=None):
+    """Normal combine: fp32 sum of every receiving rank's row (+ biases).
+    out: optional dict of preallocated outputs (out, combined_topk_weights) that the listed
+    tokens' rows are written into."""
     R, cap, H = y.shape
     T = send_head.shape[1]
     K = recv_topk_weights.shape[2] if recv_topk_weights is not None else num_topk
-    out = np.zeros((R, T, H), np.float32 if out_fp32 else np.uint16)
-    cw = np.zeros((R, T, K), np.float32) if recv_topk_weights is not None else None
+    pre = out or {}
+    out = pre.get("out")
+    if out is None:
+        out = np.zeros((R, T, H), np.float32 if out_fp32 else np.uint16)
+    if out.shape != (R, T, H) or out.dtype != (np.float32 if out_fp32 else np.uint16) or not out.flags.c_contiguous:
+        raise ValueError("out['out'] does not match the combine output")
+    cw = pre.get("combined_topk_weights")
+    if cw is None and recv_topk_weights is not None:
+        cw = np.zeros((R, T, K), np.float32)
+    if cw is not None and (cw.shape != (R, T, K) or cw.dtype != np.float32 or not cw.flags.c_contiguous):
+        raise ValueError("out['combined_topk_weights'] does not match the weight output")
     tok = _c(tokens, np.int64)
     _check(_load().oracle_combine(
         R, T, H, K, cap, _p(_c(send_head, np.int32)), _p(_c(y, np.uint16)),

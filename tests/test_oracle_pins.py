@@ -522,6 +522,32 @@ def test_sampled_tokens_match_full():
     np.testing.assert_array_equal(cp["out"].reshape(-1, shape.H)[toks], cf["out"].reshape(-1, shape.H)[toks])
 
 
+def test_token_blocks_into_shared_outputs_match_full():
+    """Dispatch and combine over disjoint token blocks into one set of preallocated outputs (the
+    all-cores CPU baseline) give the full evaluation's outputs."""
+    shape, idx, w, x = _case(4, 25, 16, 4, "uniform", 0.1, 3, 1)
+    lay = O.get_dispatch_layout(idx, shape.E)
+    cap = int(lay["num_tokens_per_rank"].sum(axis=0).max())
+    n = O.dispatch_notify(lay["num_tokens_per_rank"], lay["is_token_in_rank"], lay["num_tokens_per_expert"],
+                          shape.C, 1, cap)
+    full = O.dispatch(x, n["send_head"], cap, shape.E, topk_idx=idx, topk_weights=w)
+    d = dict(recv_x=np.zeros_like(full["recv_x"]), recv_topk_idx=np.full_like(full["recv_topk_idx"], -2),
+             recv_topk_weights=np.full_like(full["recv_topk_weights"], np.nan))
+    blocks = np.array_split(np.arange(shape.R * shape.T, dtype=np.int64), 3)
+    for b in blocks:
+        O.dispatch(x, n["send_head"], cap, shape.E, topk_idx=idx, topk_weights=w, tokens=b, out=d)
+    for key in d:
+        np.testing.assert_array_equal(d[key], full[key], err_msg=key)
+    cf = O.combine(full["recv_x"], n["send_head"], recv_topk_weights=full["recv_topk_weights"])
+    c = dict(out=np.zeros_like(cf["out"]), combined_topk_weights=np.zeros_like(cf["combined_topk_weights"]))
+    for b in blocks:
+        O.combine(full["recv_x"], n["send_head"], recv_topk_weights=full["recv_topk_weights"], tokens=b, out=c)
+    np.testing.assert_array_equal(c["out"], cf["out"])
+    np.testing.assert_array_equal(c["combined_topk_weights"], cf["combined_topk_weights"])
+    with pytest.raises(ValueError):
+        O.combine(full["recv_x"], n["send_head"], out=dict(out=np.zeros((1, 1, 1), np.uint16)))
+
+
 @pytest.mark.parametrize("case", CASES[1:6])
 def test_low_latency_rank_mask(case):
     """Masking a rank equals removing every slot that starts or ends on it (both sides agree)."""
