@@ -609,9 +609,18 @@ def run_ll_calls(n):
                       "ll_combine_us": round(a.elapsed_time(b) * 1e3 / n, 2)}))
 
 
-def run_fp8_calls(n, tokens=0):
+def fp8_inputs(shape, dev):
+    """Already-cast tokens for the FP8-input dispatch: e4m3 codes (no NaN codes) and fp32 scales."""
+    x8 = torch.randint(0, 126, (shape.R, shape.T, shape.H), dtype=torch.uint8, device=dev).view(torch.float8_e4m3fn)
+    xs = torch.rand((shape.R, shape.T, shape.H // 128), dtype=torch.float32, device=dev)
+    return x8, xs
+
+
+def run_fp8_calls(n, tokens=0, fp8_input=False):
     """The FP8 dispatch of fp8_zipf alone (fresh record, fused cast, top-k metadata), n calls back to
-    back for profilers (tokens per rank cut to `tokens` if given); prints the CUDA-event time per call."""
+    back for profilers (tokens per rank cut to `tokens` if given); prints the CUDA-event time per call.
+    fp8_input: one cast dispatch builds the record, then n cached dispatches move e4m3 codes and
+    fp32 scales unchanged."""
     from combine_get_dispatch_03_gb300 import ep
     dev = torch.device("cuda", 0)
     shape = W.WORKLOADS["fp8_zipf"]
@@ -624,15 +633,24 @@ def run_fp8_calls(n, tokens=0):
                 recv_x_scales=torch.empty((shape.R, cap, shape.H // 128), dtype=torch.float32, device=dev))
     s = torch.cuda.current_stream(dev)
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record(s)
-    for _ in range(n):
+
+    def cast_call():
         ep.ep_dispatch(h, st["x_d"], topk_idx=st["idx_d"], topk_weights=st["w_d"], cast_to_fp8=True,
                        num_tokens_per_rank=lay["num_tokens_per_rank"], is_token_in_rank=lay["is_token_in_rank"],
                        num_tokens_per_expert=lay["num_tokens_per_expert"], **bufs)
+
+    call = cast_call
+    if fp8_input:
+        cast_call()
+        codes, scales = fp8_inputs(shape, dev)
+        call = lambda: ep.ep_dispatch(h, codes, x_scales=scales, cached=True, **bufs)  # noqa: E731
+    a.record(s)
+    for _ in range(n):
+        call()
     b.record(s)
     b.synchronize()
     h.check()
-    print(json.dumps({"fp8_calls": n, "tokens_per_rank": shape.T,
+    print(json.dumps({"fp8_calls": n, "tokens_per_rank": shape.T, "fp8_input": fp8_input,
                       "fp8_dispatch_us": round(a.elapsed_time(b) * 1e3 / n, 2)}))
 
 
@@ -670,8 +688,7 @@ def measure_other_ops(ep, dev, peak, reps=10):
            {"rho": round(st["hits"] / (shape.R * shape.T), 3)})
     # FP8 input (already cast: e4m3 codes and fp32 scales), cached record: bytes are moved as they are
     n, G = shape.R * shape.T, shape.H // 128
-    x8 = torch.randint(0, 126, (shape.R, shape.T, shape.H), dtype=torch.uint8, device=dev).view(torch.float8_e4m3fn)
-    xs = torch.rand((shape.R, shape.T, G), dtype=torch.float32, device=dev)
+    x8, xs = fp8_inputs(shape, dev)
     fn8 = lambda: ep.ep_dispatch(h, x8, x_scales=xs, cached=True, recv_x=bufs["recv_x"],
                                  recv_x_scales=bufs["recv_x_scales"])
     ms8 = timed(fn8, reps, stream)
@@ -939,6 +956,8 @@ def main():
                     help="only run the ll_v3 low-latency dispatch and combine this many times each (profiling)")
     ap.add_argument("--fp8-calls", type=int, default=0,
                     help="only run the fp8_zipf FP8 dispatch (fresh record, cast) this many times (profiling)")
+    ap.add_argument("--fp8-input", action="store_true",
+                    help="with --fp8-calls: time cached dispatches of already-cast e4m3 tokens and scales")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--layout-two-launches", action="store_true",
                     help="run the step's layout and notify as two launches (for profilers, which cannot launch "
@@ -951,7 +970,7 @@ def main():
     if args.ll_calls:
         run_ll_calls(args.ll_calls)
     elif args.fp8_calls:
-        run_fp8_calls(args.fp8_calls, args.tokens)
+        run_fp8_calls(args.fp8_calls, args.tokens, args.fp8_input)
     elif args.impl == "reference":
         run_reference(args)
     else:
