@@ -115,9 +115,10 @@ def _raise(rc: int):
         raise EPError(rc, lib().ep_last_error().decode(errors="replace"))
 
 
-def _stream(stream):
+def _stream(stream, device):
+    """The raw stream handle: `stream`, else the current stream of the handle's device."""
     if stream is None:
-        stream = torch.cuda.current_stream()
+        stream = torch.cuda.current_stream(device)
     return ctypes.c_void_p(stream.cuda_stream)
 
 
@@ -210,14 +211,15 @@ class Handle:
 
     def status(self, reset: bool = True, stream=None) -> int:
         """Synchronise and return the first device-detected error code (0 = none)."""
-        return lib().ep_handle_status(self.ptr, _stream(stream), int(reset))
+        return lib().ep_handle_status(self.ptr, _stream(stream, self.device), int(reset))
 
     def check(self, stream=None):
         _raise(self.status(True, stream))
 
     def num_recv(self, stream=None) -> torch.Tensor:
         out = torch.zeros(self.cfg.num_ranks, dtype=torch.int32)
-        _raise(lib().ep_handle_num_recv(self.ptr, ctypes.c_void_p(out.data_ptr()), _stream(stream)))
+        _raise(lib().ep_handle_num_recv(self.ptr, ctypes.c_void_p(out.data_ptr()),
+                                        _stream(stream, self.device)))
         return out
 
     def export(self, field: str, stream=None) -> torch.Tensor:
@@ -239,7 +241,7 @@ class Handle:
         assert nbytes == out.numel() * 4
         if nbytes:
             _raise(lib().ep_handle_export(self.ptr, FIELDS[field], ctypes.c_void_p(out.data_ptr()), nbytes,
-                                          _stream(stream)))
+                                          _stream(stream, self.device)))
         if field == "send_head":
             # rows are packed for the T of the last fresh dispatch: [R][T][R]
             T = self.normal_tokens or 0
@@ -248,21 +250,21 @@ class Handle:
 
 
 def ep_update_mask_buffer(h: Handle, rank: int, masked: bool = True, stream=None):
-    _raise(lib().ep_update_mask_buffer(h.ptr, rank, int(bool(masked)), _stream(stream)))
+    _raise(lib().ep_update_mask_buffer(h.ptr, rank, int(bool(masked)), _stream(stream, h.device)))
 
 
 def ep_query_mask_buffer(h: Handle, stream=None) -> torch.Tensor:
     out = torch.zeros(h.cfg.num_ranks, dtype=torch.int32)
-    _raise(lib().ep_query_mask_buffer(h.ptr, ctypes.c_void_p(out.data_ptr()), _stream(stream)))
+    _raise(lib().ep_query_mask_buffer(h.ptr, ctypes.c_void_p(out.data_ptr()), _stream(stream, h.device)))
     return out
 
 
 def ep_clean_mask_buffer(h: Handle, stream=None):
-    _raise(lib().ep_clean_mask_buffer(h.ptr, _stream(stream)))
+    _raise(lib().ep_clean_mask_buffer(h.ptr, _stream(stream, h.device)))
 
 
 def ep_selftest_bounded_wait(h: Handle, max_iterations: int, rank: int, stream=None):
-    _raise(lib().ep_selftest_bounded_wait(h.ptr, max_iterations, rank, _stream(stream)))
+    _raise(lib().ep_selftest_bounded_wait(h.ptr, max_iterations, rank, _stream(stream, h.device)))
 
 
 def ep_handle_create(cfg: Config, device=None) -> Handle:
@@ -300,7 +302,7 @@ def ep_get_dispatch_layout(h: Handle, topk_idx: torch.Tensor, num_tokens_per_ran
         _ptr(tpr, "num_tokens_per_rank", torch.int32, (R, R), d),
         _ptr(tprdma, "num_tokens_per_rdma_rank", torch.int32, (R, nn), d),
         _ptr(tpe, "num_tokens_per_expert", torch.int32, (R, E), d),
-        _ptr(itr, "is_token_in_rank", None, (R, T, R), d), _stream(stream)))
+        _ptr(itr, "is_token_in_rank", None, (R, T, R), d), _stream(stream, h.device)))
     if itr.dtype not in (torch.bool, torch.uint8):
         raise TypeError("is_token_in_rank must be bool or uint8")
     return dict(num_tokens_per_rank=tpr, num_tokens_per_rdma_rank=tprdma, num_tokens_per_expert=tpe,
@@ -322,7 +324,7 @@ def ep_notify_dispatch(h: Handle, num_tokens_per_rank, is_token_in_rank, num_tok
         _ptr(is_token_in_rank, "is_token_in_rank", None, (R, T, R), d),
         _ptr(num_tokens_per_expert, "num_tokens_per_expert", torch.int32, (R, c.num_experts), d),
         _ptr(num_recv_tokens_per_expert, "num_recv_tokens_per_expert", torch.int32, (R, c.num_local_experts), d),
-        _stream(stream)))
+        _stream(stream, h.device)))
     h.normal_tokens = T
     return num_recv_tokens_per_expert
 
@@ -356,7 +358,8 @@ def ep_layout_notify(h: Handle, topk_idx: torch.Tensor, num_tokens_per_rank=None
         _ptr(tprdma, "num_tokens_per_rdma_rank", torch.int32, (R, nn), d),
         _ptr(tpe, "num_tokens_per_expert", torch.int32, (R, E), d),
         _ptr(itr, "is_token_in_rank", None, (R, T, R), d),
-        _ptr(nrpe, "num_recv_tokens_per_expert", torch.int32, (R, c.num_local_experts), d), _stream(stream)))
+        _ptr(nrpe, "num_recv_tokens_per_expert", torch.int32, (R, c.num_local_experts), d),
+        _stream(stream, h.device)))
     h.normal_tokens = T
     return dict(num_tokens_per_rank=tpr, num_tokens_per_rdma_rank=tprdma, num_tokens_per_expert=tpe,
                 is_token_in_rank=itr, num_recv_tokens_per_expert=nrpe)
@@ -407,7 +410,7 @@ def ep_dispatch(h: Handle, x: torch.Tensor, topk_idx=None, topk_weights=None, nu
         _ptr(recv_topk_idx, "recv_topk_idx", torch.int64, (R, cap, K), d),
         _ptr(recv_topk_weights, "recv_topk_weights", torch.float32, (R, cap, K), d),
         _ptr(num_recv_tokens_per_expert, "num_recv_tokens_per_expert", torch.int32, (R, c.num_local_experts), d),
-        mode, _stream(stream)))
+        mode, _stream(stream, h.device)))
     if mode == EP_DISPATCH_FRESH:
         h.normal_tokens = T
     return dict(recv_x=recv_x, recv_x_scales=recv_x_scales, recv_topk_idx=recv_topk_idx,
@@ -432,7 +435,8 @@ def ep_combine(h: Handle, x: torch.Tensor, topk_weights=None, bias_0=None, bias_
         _ptr(bias_0, "bias_0", torch.bfloat16, (R, T, H), d), _ptr(bias_1, "bias_1", torch.bfloat16, (R, T, H), d),
         _ptr(combined_x, "combined_x", out_dtype, (R, T, H), d),
         EP_FP32 if out_dtype == torch.float32 else EP_BF16,
-        _ptr(combined_topk_weights, "combined_topk_weights", torch.float32, (R, T, K), d), _stream(stream)))
+        _ptr(combined_topk_weights, "combined_topk_weights", torch.float32, (R, T, K), d),
+        _stream(stream, h.device)))
     return dict(combined_x=combined_x, combined_topk_weights=combined_topk_weights)
 
 
@@ -457,7 +461,7 @@ def ep_ll_dispatch(h: Handle, x: torch.Tensor, topk_idx: torch.Tensor, use_fp8: 
         _ptr(packed_recv_count, "packed_recv_count", torch.int32, (R, EL), d),
         _ptr(packed_recv_layout_range, "packed_recv_layout_range", torch.int64, (R, EL, R), d),
         _ptr(cumulative_local_expert_recv_stats, "cumulative_local_expert_recv_stats", torch.int32, (R, EL), d),
-        _stream(stream)))
+        _stream(stream, h.device)))
     h.ll_tokens = T
     return dict(recv_msgs=recv_msgs, packed_recv_count=packed_recv_count,
                 packed_recv_layout_range=packed_recv_layout_range)
@@ -518,7 +522,7 @@ def ep_ll_combine(h: Handle, x: torch.Tensor, topk_idx: torch.Tensor, topk_weigh
         h.ptr, ctypes.c_void_p(x.data_ptr()), row_bytes,
         _ptr(topk_idx, "topk_idx", torch.int64, (R, T, K), d),
         _ptr(topk_weights, "topk_weights", torch.float32, (R, T, K), d),
-        _ptr(combined_x, "combined_x", torch.bfloat16, (R, T, H), d), _stream(stream)))
+        _ptr(combined_x, "combined_x", torch.bfloat16, (R, T, H), d), _stream(stream, h.device)))
     return combined_x
 
 
