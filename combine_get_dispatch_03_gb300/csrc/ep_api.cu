@@ -38,7 +38,8 @@ struct ep_handle {
     int32_t* rank_mask = nullptr;            // [R], nonzero = masked
     int32_t* rdma_channel_prefix = nullptr;    // [R][NN][C], NN = R / 8 whole nodes (see has_nodes)
     int32_t* recv_rdma_rank_prefix = nullptr;  // [R][NN]
-    int32_t* barrier = nullptr;                // [2]: count and generation of the layout + notify grid barrier
+    int32_t* barrier = nullptr;                // [4]: count and generation of the layout + notify grid barrier;
+                                               // the combine's next token and finished warps
     int normal_tokens = -1;                  // T of the current dispatch record, -1 = none
     bool prepared = false;                   // record built by ep_notify_dispatch, not yet used
     int ll_tokens = -1;                      // T of the last LL dispatch, -1 = none
@@ -193,7 +194,7 @@ ep_status ep_handle_create(const ep_config* cfg, ep_handle** out) {
     const size_t E = cfg->num_experts, cap = static_cast<size_t>(cfg->recv_capacity);
     const size_t NN = (R + 7) / 8;
     const size_t sizes[] = {1, R * R, R * R * C, R * R * C, R, R * cap, R * T * R, R * T * K, R * E, R,
-                            R * NN * C, R * NN, 2};
+                            R * NN * C, R * NN, 4};
     int32_t** slots[] = {&h->status,   &h->rank_prefix,  &h->channel_prefix, &h->recv_channel_prefix,
                          &h->num_recv, &h->recv_src_idx, &h->send_head,      &h->ll_slot,
                          &h->ll_cnt,   &h->rank_mask,    &h->rdma_channel_prefix, &h->recv_rdma_rank_prefix,
@@ -502,7 +503,7 @@ ep_status ep_combine(ep_handle* h, const void* x, const float* topk_weights, con
     DeviceGuard guard(h->device);
     cudaError_t err = ep::launch_combine(h->plan, out_dtype == EP_FP32, c.num_ranks, T, c.hidden, c.num_topk,
                                          c.recv_capacity, h->send_head, x, topk_weights, bias_0, bias_1, combined_x,
-                                         combined_topk_weights, stream);
+                                         combined_topk_weights, reinterpret_cast<uint32_t*>(h->barrier) + 2, stream);
     if (err != cudaSuccess) return cuda_fail(err, "combine launch");
     return EP_OK;
 }

@@ -64,10 +64,12 @@ cudaError_t launch_dispatch(const LaunchPlan& plan, int mode, int R, int T, int 
                             float* recv_x_scales, int64_t* recv_topk_idx, float* recv_topk_weights,
                             int32_t* status, cudaStream_t stream);
 
+// work: two words of device memory, zero before the first launch, through which the combine's
+// warps claim tokens; each launch leaves them zero again.  Launches sharing them must be ordered.
 cudaError_t launch_combine(const LaunchPlan& plan, bool out_fp32, int R, int T, int H, int K, int64_t cap,
                            const int32_t* send_head, const void* y, const float* recv_topk_weights,
                            const void* bias0, const void* bias1, void* out, float* combined_topk_weights,
-                           cudaStream_t stream);
+                           uint32_t* work, cudaStream_t stream);
 
 cudaError_t launch_ll_dispatch(const LaunchPlan& plan, int R, int T, int maxT, int H, int K, int E,
                                const void* x, const int64_t* topk_idx, bool use_fp8, bool round_scale,

@@ -25,6 +25,9 @@
  *    ids in [0, E) or -1 for a masked slot.
  *  - Every call is asynchronous on `stream` (a cudaStream_t; NULL is the
  *    legacy default stream) and returns after enqueueing its kernels.
+ *    Calls on one handle must not overlap on the GPU -- issue them on one
+ *    stream, or order them with events: the handle holds the dispatch record,
+ *    the status word and the counters its kernels share.
  *  - Argument errors found on the host are returned at once and nothing is
  *    enqueued.  Errors found by the kernels (an expert id out of range,
  *    counts that disagree with is_token_in_rank, a receive buffer that is
