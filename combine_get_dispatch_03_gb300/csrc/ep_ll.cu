@@ -31,6 +31,7 @@ namespace ep {
 namespace {
 
 constexpr int kLLCountThreadsLarge = 1024;  // the count kernel's block while its histograms fit in smem
+constexpr int kFinishThreads = 256;
 constexpr int kLLUnroll = 4;
 constexpr int kLLCombineUnroll = 2;
 constexpr int kLLCombineFanIn = 4;         // slots loaded together before accumulation
@@ -43,6 +44,8 @@ __global__ void __launch_bounds__(kThreads)
                     int32_t* status) {
     pdl_enter();
     constexpr int kWarps = kThreads / kWarpSize;
+    constexpr int kScanChunk = kWarps < 16 ? kWarps : 16;
+    static_assert(kWarps % kScanChunk == 0, "whole scan chunks");
     extern __shared__ int32_t smem[];
     int32_t* s_warp = smem;                   // [kWarps][E]: per-warp count -> exclusive prefix
     int32_t* s_run = smem + kWarps * E;  // [E]: slots of this source seen so far
@@ -75,12 +78,20 @@ __global__ void __launch_bounds__(kThreads)
         const int before = __popc(peers & lanemask_lt());
         if (e >= 0 && before == 0) s_warp[warp * E + e] = __popc(peers);
         __syncthreads();
+        // per expert: exclusive prefix over the warps, in chunks of 16 whose loads are all issued
+        // before the stores (a load after a store to the same array would wait for it)
         for (int x = tid; x < E; x += kThreads) {
             int32_t run = s_run[x];
-            for (int w = 0; w < kWarps; ++w) {
-                const int32_t c = s_warp[w * E + x];
-                s_warp[w * E + x] = run;
-                run += c;
+#pragma unroll
+            for (int w0 = 0; w0 < kWarps; w0 += kScanChunk) {
+                int32_t c[kScanChunk];
+#pragma unroll
+                for (int u = 0; u < kScanChunk; ++u) c[u] = s_warp[(w0 + u) * E + x];
+#pragma unroll
+                for (int u = 0; u < kScanChunk; ++u) {
+                    s_warp[(w0 + u) * E + x] = run;
+                    run += c[u];
+                }
             }
             s_run[x] = run;
         }
@@ -127,23 +138,57 @@ __global__ void ll_finish_kernel(int R, int T, int maxT, int K, int E, int exper
         }
         return;
     }
-    const int64_t i = static_cast<int64_t>(blockIdx.x - expert_blocks) * blockDim.x + threadIdx.x;
-    if (i >= static_cast<int64_t>(R) * T * K) return;
-    const int s = static_cast<int>(i / (static_cast<int64_t>(T) * K));
-    const int64_t tk = i - static_cast<int64_t>(s) * T * K;
-    const int64_t v = __ldg(topk_idx + i);
-    int32_t* sp = slot + static_cast<int64_t>(s) * maxT * K + tk;
-    const int32_t pos = *sp;
+    const int64_t n_slots = static_cast<int64_t>(R) * T * K;
+    const int64_t i0 = static_cast<int64_t>(blockIdx.x - expert_blocks) * blockDim.x;
+    const int64_t i = i0 + threadIdx.x;
+    // With E <= blockDim and every slot of the CTA from one source, the CTA sums the begins of
+    // that source's blocks for all experts into shared memory while its slots' expert ids and
+    // positions load: loads that need no expert id, so a slot waits for one round of loads
+    // instead of two.
+    __shared__ int32_t s_begin[kFinishThreads];
+    const int64_t i_last = (i0 + blockDim.x < n_slots ? i0 + blockDim.x : n_slots) - 1;
+    const int s_first = static_cast<int>(i0 / (static_cast<int64_t>(T) * K));
+    const bool table = E <= static_cast<int>(blockDim.x) && i0 < n_slots &&
+                       s_first == static_cast<int>(i_last / (static_cast<int64_t>(T) * K));
+    const bool live = i < n_slots;
+    int s = 0;
+    int64_t v = -1;
+    int32_t pos = -1;
+    int32_t* sp = nullptr;
+    if (live) {
+        s = static_cast<int>(i / (static_cast<int64_t>(T) * K));
+        v = __ldg(topk_idx + i);
+        sp = slot + static_cast<int64_t>(s) * maxT * K + (i - static_cast<int64_t>(s) * T * K);
+        pos = *sp;
+    }
+    if (table) {
+        const int e = threadIdx.x;
+        if (e < E) {
+            int32_t part[kMaxRanks];
+#pragma unroll
+            for (int q = 0; q < kMaxRanks; ++q) part[q] = q < s_first ? __ldg(cnt + static_cast<int64_t>(q) * E + e) : 0;
+            int32_t b = 0;
+#pragma unroll
+            for (int q = 0; q < kMaxRanks; ++q) b += part[q];
+            s_begin[e] = b;
+        }
+        __syncthreads();
+    }
+    if (!live) return;
     int32_t row = -1;
     if (v >= 0 && v < E && pos >= 0) {
-        // the counts of the earlier sources, all loads in flight at once (R <= kMaxRanks)
-        int32_t part[kMaxRanks];
-#pragma unroll
-        for (int sp2 = 0; sp2 < kMaxRanks; ++sp2)
-            part[sp2] = sp2 < s ? __ldg(cnt + static_cast<int64_t>(sp2) * E + v) : 0;
         int64_t begin = 0;
+        if (table) {
+            begin = s_begin[v];
+        } else {
+            // the counts of the earlier sources, all loads in flight at once (R <= kMaxRanks)
+            int32_t part[kMaxRanks];
 #pragma unroll
-        for (int sp2 = 0; sp2 < kMaxRanks; ++sp2) begin += part[sp2];
+            for (int sp2 = 0; sp2 < kMaxRanks; ++sp2)
+                part[sp2] = sp2 < s ? __ldg(cnt + static_cast<int64_t>(sp2) * E + v) : 0;
+#pragma unroll
+            for (int sp2 = 0; sp2 < kMaxRanks; ++sp2) begin += part[sp2];
+        }
         if (begin + pos < slots) row = static_cast<int32_t>(begin + pos);
     }
     *sp = row;
@@ -567,7 +612,7 @@ cudaError_t launch_ll_dispatch(const LaunchPlan& plan, int R, int T, int maxT, i
     cudaError_t err = launch_kernel(count_kernel, dim3(R), dim3(count_threads), ll_count_smem(E, count_threads), stream,
                                     1, R, T, maxT, K, E, topk_idx, rank_mask, slot, cnt, status);
     if (err != cudaSuccess) return err;
-    const int fin_threads = 256;
+    const int fin_threads = kFinishThreads;
     const int expert_blocks = (E + fin_threads / kWarpSize - 1) / (fin_threads / kWarpSize);
     const int64_t n_slots = static_cast<int64_t>(R) * T * K;
     const int slot_blocks = static_cast<int>((n_slots + fin_threads - 1) / fin_threads);
