@@ -14,6 +14,7 @@
 
 #include "ep_common.cuh"
 #include "ep_kernels.h"
+#include "ep_trace.h"
 
 namespace ep {
 cudaError_t plan_dispatch_combine(LaunchPlan* plan, int hidden);
@@ -165,6 +166,7 @@ int64_t ep_ll_msg_bytes(int32_t hidden, int32_t use_fp8) {
 }
 
 ep_status ep_handle_create(const ep_config* cfg, ep_handle** out) {
+    EP_TRACE();
     if (out == nullptr) return fail(EP_ERR_INVALID_ARG, "out is NULL");
     *out = nullptr;
     ep_status st = check_config(cfg);
@@ -223,6 +225,7 @@ ep_status ep_handle_create(const ep_config* cfg, ep_handle** out) {
 }
 
 void ep_handle_destroy(ep_handle* h) {
+    EP_TRACE();
     if (h == nullptr) return;
     DeviceGuard guard(h->device);
     cudaDeviceSynchronize();
@@ -231,6 +234,7 @@ void ep_handle_destroy(ep_handle* h) {
 }
 
 ep_status ep_handle_status(ep_handle* h, ep_stream_t stream, int32_t reset) {
+    EP_TRACE();
     if (h == nullptr) return fail(EP_ERR_INVALID_ARG, "handle is NULL");
     DeviceGuard guard(h->device);
     cudaError_t err = cudaStreamSynchronize(stream);
@@ -247,6 +251,7 @@ ep_status ep_handle_status(ep_handle* h, ep_stream_t stream, int32_t reset) {
 }
 
 ep_status ep_handle_num_recv(ep_handle* h, int32_t* host_num_recv, ep_stream_t stream) {
+    EP_TRACE();
     if (h == nullptr || host_num_recv == nullptr) return fail(EP_ERR_INVALID_ARG, "NULL argument");
     if (h->normal_tokens < 0) return fail(EP_ERR_STATE, "no normal dispatch on this handle yet");
     DeviceGuard guard(h->device);
@@ -277,6 +282,7 @@ size_t ep_handle_field_bytes(const ep_handle* h, ep_handle_field field) {
 
 ep_status ep_handle_export(const ep_handle* h, ep_handle_field field, void* dst, size_t bytes,
                            ep_stream_t stream) {
+    EP_TRACE();
     if (h == nullptr || dst == nullptr) return fail(EP_ERR_INVALID_ARG, "NULL argument");
     const bool node_field =
         field == EP_FIELD_RDMA_CHANNEL_PREFIX_MATRIX || field == EP_FIELD_RECV_RDMA_RANK_PREFIX_SUM;
@@ -311,6 +317,7 @@ ep_status ep_handle_export(const ep_handle* h, ep_handle_field field, void* dst,
 ep_status ep_get_dispatch_layout(ep_handle* h, int32_t num_tokens, const int64_t* topk_idx,
                                  int32_t* num_tokens_per_rank, int32_t* num_tokens_per_rdma_rank,
                                  int32_t* num_tokens_per_expert, uint8_t* is_token_in_rank, ep_stream_t stream) {
+    EP_TRACE();
     if (h == nullptr) return fail(EP_ERR_INVALID_ARG, "handle is NULL");
     ep_status st = check_tokens(h, num_tokens);
     if (st != EP_OK) return st;
@@ -334,6 +341,7 @@ ep_status ep_dispatch(ep_handle* h, int32_t num_tokens, const void* x, ep_dtype 
                       const int32_t* num_tokens_per_expert, void* recv_x, float* recv_x_scales,
                       int64_t* recv_topk_idx, float* recv_topk_weights, int32_t* num_recv_tokens_per_expert,
                       int32_t cached, ep_stream_t stream) {
+    EP_TRACE();
     if (h == nullptr) return fail(EP_ERR_INVALID_ARG, "handle is NULL");
     ep_status st = check_tokens(h, num_tokens);
     if (st != EP_OK) return st;
@@ -421,6 +429,7 @@ ep_status ep_dispatch(ep_handle* h, int32_t num_tokens, const void* x, ep_dtype 
 ep_status ep_notify_dispatch(ep_handle* h, int32_t num_tokens, const int32_t* num_tokens_per_rank,
                              const uint8_t* is_token_in_rank, const int32_t* num_tokens_per_expert,
                              int32_t* num_recv_tokens_per_expert, ep_stream_t stream) {
+    EP_TRACE();
     if (h == nullptr) return fail(EP_ERR_INVALID_ARG, "handle is NULL");
     ep_status st = check_tokens(h, num_tokens);
     if (st != EP_OK) return st;
@@ -446,6 +455,7 @@ ep_status ep_notify_dispatch(ep_handle* h, int32_t num_tokens, const int32_t* nu
 ep_status ep_layout_notify(ep_handle* h, int32_t num_tokens, const int64_t* topk_idx, int32_t* num_tokens_per_rank,
                            int32_t* num_tokens_per_rdma_rank, int32_t* num_tokens_per_expert,
                            uint8_t* is_token_in_rank, int32_t* num_recv_tokens_per_expert, ep_stream_t stream) {
+    EP_TRACE();
     if (h == nullptr) return fail(EP_ERR_INVALID_ARG, "handle is NULL");
     ep_status st = check_tokens(h, num_tokens);
     if (st != EP_OK) return st;
@@ -488,6 +498,7 @@ ep_status ep_layout_notify(ep_handle* h, int32_t num_tokens, const int64_t* topk
 ep_status ep_combine(ep_handle* h, const void* x, const float* topk_weights, const void* bias_0,
                      const void* bias_1, void* combined_x, ep_dtype out_dtype, float* combined_topk_weights,
                      ep_stream_t stream) {
+    EP_TRACE();
     if (h == nullptr) return fail(EP_ERR_INVALID_ARG, "handle is NULL");
     if (h->normal_tokens < 0) return fail(EP_ERR_STATE, "combine without a prior dispatch");
     const ep_config& c = h->cfg;
@@ -512,6 +523,7 @@ ep_status ep_ll_dispatch(ep_handle* h, int32_t num_tokens, const void* x, const 
                          int32_t round_scale, int32_t use_ue8m0, void* recv_msgs, int32_t* packed_recv_count,
                          int64_t* packed_recv_layout_range, int32_t* cumulative_local_expert_recv_stats,
                          ep_stream_t stream) {
+    EP_TRACE();
     if (h == nullptr) return fail(EP_ERR_INVALID_ARG, "handle is NULL");
     ep_status st = check_tokens(h, num_tokens);
     if (st != EP_OK) return st;
@@ -538,6 +550,7 @@ ep_status ep_ll_dispatch(ep_handle* h, int32_t num_tokens, const void* x, const 
 
 ep_status ep_ll_combine_strided(ep_handle* h, const void* x, int64_t x_row_bytes, const int64_t* topk_idx,
                                 const float* topk_weights, void* combined_x, ep_stream_t stream) {
+    EP_TRACE();
     if (h == nullptr) return fail(EP_ERR_INVALID_ARG, "handle is NULL");
     if (h->ll_tokens < 0) return fail(EP_ERR_STATE, "low-latency combine without a prior low-latency dispatch");
     const ep_config& c = h->cfg;
@@ -559,12 +572,14 @@ ep_status ep_ll_combine_strided(ep_handle* h, const void* x, int64_t x_row_bytes
 
 ep_status ep_ll_combine(ep_handle* h, const void* x, const int64_t* topk_idx, const float* topk_weights,
                         void* combined_x, ep_stream_t stream) {
+    EP_TRACE();
     if (h == nullptr) return fail(EP_ERR_INVALID_ARG, "handle is NULL");
     return ep_ll_combine_strided(h, x, 2 * static_cast<int64_t>(h->cfg.hidden), topk_idx, topk_weights, combined_x,
                                  stream);
 }
 
 ep_status ep_update_mask_buffer(ep_handle* h, int32_t rank, int32_t masked, ep_stream_t stream) {
+    EP_TRACE();
     if (h == nullptr) return fail(EP_ERR_INVALID_ARG, "handle is NULL");
     EP_CHECK_ARG(rank >= 0 && rank < h->cfg.num_ranks, "rank %d outside [0, %d)", rank, h->cfg.num_ranks);
     DeviceGuard guard(h->device);
@@ -575,6 +590,7 @@ ep_status ep_update_mask_buffer(ep_handle* h, int32_t rank, int32_t masked, ep_s
 }
 
 ep_status ep_query_mask_buffer(ep_handle* h, int32_t* host_mask, ep_stream_t stream) {
+    EP_TRACE();
     if (h == nullptr || host_mask == nullptr) return fail(EP_ERR_INVALID_ARG, "NULL argument");
     DeviceGuard guard(h->device);
     cudaError_t err = cudaMemcpyAsync(host_mask, h->rank_mask, sizeof(int32_t) * h->cfg.num_ranks, cudaMemcpyDefault,
@@ -585,6 +601,7 @@ ep_status ep_query_mask_buffer(ep_handle* h, int32_t* host_mask, ep_stream_t str
 }
 
 ep_status ep_clean_mask_buffer(ep_handle* h, ep_stream_t stream) {
+    EP_TRACE();
     if (h == nullptr) return fail(EP_ERR_INVALID_ARG, "handle is NULL");
     DeviceGuard guard(h->device);
     cudaError_t err = cudaMemsetAsync(h->rank_mask, 0, sizeof(int32_t) * h->cfg.num_ranks, stream);
@@ -593,6 +610,7 @@ ep_status ep_clean_mask_buffer(ep_handle* h, ep_stream_t stream) {
 }
 
 ep_status ep_selftest_bounded_wait(ep_handle* h, uint32_t max_iterations, int32_t rank, ep_stream_t stream) {
+    EP_TRACE();
     if (h == nullptr) return fail(EP_ERR_INVALID_ARG, "handle is NULL");
     EP_CHECK_ARG(rank >= 0 && rank < h->cfg.num_ranks, "rank %d outside [0, %d)", rank, h->cfg.num_ranks);
     EP_CHECK_ARG(max_iterations >= 1 && max_iterations <= (1u << 20), "max_iterations must lie in [1, 2^20]");

@@ -19,6 +19,7 @@
 
 #include "ep_common.cuh"
 #include "ep_kernels.h"
+#include "ep_trace.h"
 
 namespace ep {
 cudaError_t plan_ll(LaunchPlan* plan, int num_experts);
@@ -78,6 +79,7 @@ extern "C" ep_status ep_ll_dispatch_noalloc(int32_t num_ranks, int32_t num_token
                                             int64_t* packed_recv_layout_range,
                                             int32_t* cumulative_local_expert_recv_stats, int32_t* slot_row,
                                             int32_t* status, ep_stream_t stream) {
+    EP_TRACE();
     const int R = num_ranks, T = num_tokens, maxT = num_max_tokens, H = hidden, E = num_experts, K = num_topk;
     if (R < 1 || R > ep::kMaxRanks) return reject(EP_ERR_UNSUPPORTED, "num_ranks outside [1, 32]");
     if (E < 1 || E % R != 0 || E > ep::kMaxExperts)
