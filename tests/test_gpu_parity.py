@@ -465,6 +465,44 @@ def test_max_sms_keeps_every_result(max_sms):
     np.testing.assert_array_equal(P.host(got), want)
 
 
+@pytest.mark.parametrize("R", [8, 16])
+def test_claimed_token_combines_back_to_back(R):
+    """With several tokens per warp the combine's warps claim tokens from a counter in the handle,
+    which each launch must leave at zero: three combines on one handle (fresh outputs each, fp32
+    and bf16, with and without weights and biases) all equal the oracle."""
+    shape = S(f"claims{R}", R, 2048 if R == 8 else 1024, 128, 4 * R, 6, routing="gumbel", mask_p=0.05, seed=70 + R)
+    n_tokens = shape.R * shape.T
+    warps = torch.cuda.get_device_properties(0).multi_processor_count * 24  # at most 24 resident warps/SM
+    assert n_tokens >= 2 * warps, "the shape must put several tokens on every warp"
+    idx, w = W.routing(shape)
+    x = W.tokens_x(shape)
+    cap = P.needed_capacity(idx, shape.E)
+    h = ep.Handle(P.config_of(shape, cap))
+    idx_d, w_d = torch.from_numpy(idx).to(P.DEV), torch.from_numpy(w).to(P.DEV)
+    ep.ep_layout_notify(h, idx_d)
+    d = ep.ep_dispatch(h, x.to(P.DEV), topk_idx=idx_d, topk_weights=w_d, prepared=True)
+    assert h.status() == 0
+    lay = O.get_dispatch_layout(idx, shape.E)
+    n = O.dispatch_notify(lay["num_tokens_per_rank"], lay["is_token_in_rank"], lay["num_tokens_per_expert"],
+                          shape.C, shape.A, cap)
+    ora_d = O.dispatch(W.bf16_bits(x), n["send_head"], cap, shape.E, topk_idx=idx, topk_weights=w)
+    for i, (out_f32, weights, biases) in enumerate([(True, True, False), (False, False, True), (False, True, True)]):
+        y = W.normal_bf16((shape.R, cap, shape.H), shape.seed, f"cy{i}")
+        b0 = W.normal_bf16((shape.R, shape.T, shape.H), shape.seed, f"cb0{i}", std=0.1) if biases else None
+        b1 = W.normal_bf16((shape.R, shape.T, shape.H), shape.seed, f"cb1{i}", std=0.1) if biases else None
+        c = ep.ep_combine(h, y.to(P.DEV), topk_weights=d["recv_topk_weights"] if weights else None,
+                          bias_0=None if b0 is None else b0.to(P.DEV), bias_1=None if b1 is None else b1.to(P.DEV),
+                          out_dtype=torch.float32 if out_f32 else torch.bfloat16)
+        assert h.status() == 0
+        ora = O.combine(W.bf16_bits(y), n["send_head"],
+                        recv_topk_weights=ora_d["recv_topk_weights"] if weights else None,
+                        bias0=None if b0 is None else W.bf16_bits(b0), bias1=None if b1 is None else W.bf16_bits(b1),
+                        out_fp32=out_f32, num_topk=shape.K)
+        np.testing.assert_array_equal(P.host(c["combined_x"]), ora["out"], err_msg=f"combine {i}")
+        if weights:
+            np.testing.assert_array_equal(P.host(c["combined_topk_weights"]), ora["combined_topk_weights"])
+
+
 def test_bounded_wait_times_out_and_masks():
     """A wait on an mbarrier that nothing completes gives up, reports EP_ERR_TIMEOUT and masks the
     rank; the context stays usable and the next dispatch leaves that rank out."""
