@@ -966,8 +966,8 @@ def main():
                     help="with --fp8-calls: time cached dispatches of already-cast e4m3 tokens and scales")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--layout-two-launches", action="store_true",
-                    help="run the step's layout and notify as two launches (for profilers, which cannot launch "
-                         "the one-launch cooperative kernel)")
+                    help="run the step's layout and notify as the two separate calls (ep_get_dispatch_layout, "
+                         "ep_notify_dispatch) instead of ep_layout_notify")
     ap.add_argument("--tokens", type=int, default=0,
                     help="tokens per rank of the headline workload (0 = its full 4096; smaller only for profiling)")
     args = ap.parse_args()

@@ -41,6 +41,7 @@ struct ep_handle {
     int32_t* recv_rdma_rank_prefix = nullptr;  // [R][NN]
     int32_t* barrier = nullptr;                // [4]: count and generation of the layout + notify grid barrier;
                                                // the combine's next token and finished warps
+    int32_t* layout_scratch = nullptr;         // tile states of the one-pass layout + record scan
     int normal_tokens = -1;                  // T of the current dispatch record, -1 = none
     bool prepared = false;                   // record built by ep_notify_dispatch, not yet used
     int ll_tokens = -1;                      // T of the last LL dispatch, -1 = none
@@ -195,12 +196,13 @@ ep_status ep_handle_create(const ep_config* cfg, ep_handle** out) {
     const size_t R = cfg->num_ranks, C = cfg->num_channels, T = cfg->num_max_tokens, K = cfg->num_topk;
     const size_t E = cfg->num_experts, cap = static_cast<size_t>(cfg->recv_capacity);
     const size_t NN = (R + 7) / 8;
+    const size_t scan_words = ep::layout_scan_scratch_words(cfg->num_ranks, cfg->num_experts, cfg->num_max_tokens);
     const size_t sizes[] = {1, R * R, R * R * C, R * R * C, R, R * cap, R * T * R, R * T * K, R * E, R,
-                            R * NN * C, R * NN, 4};
+                            R * NN * C, R * NN, 4, scan_words};
     int32_t** slots[] = {&h->status,   &h->rank_prefix,  &h->channel_prefix, &h->recv_channel_prefix,
                          &h->num_recv, &h->recv_src_idx, &h->send_head,      &h->ll_slot,
                          &h->ll_cnt,   &h->rank_mask,    &h->rdma_channel_prefix, &h->recv_rdma_rank_prefix,
-                         &h->barrier};
+                         &h->barrier,  &h->layout_scratch};
     size_t total = 0;
     for (size_t s : sizes) total += align_up(s * sizeof(int32_t), 256);
     err = cudaMalloc(&h->dmem, total);
@@ -470,7 +472,16 @@ ep_status ep_layout_notify(ep_handle* h, int32_t num_tokens, const int64_t* topk
                  "misaligned layout pointer");
     DeviceGuard guard(h->device);
     cudaError_t err;
-    if (h->plan.layout_notify_fused) {
+    if (node_record(h, 0) == nullptr && ep::layout_scan_fits(num_tokens)) {
+        // one pass: a decoupled look-back scan over token tiles in receive order
+        err = ep::launch_layout_scan(topk_idx, c.num_ranks, num_tokens, c.num_topk, c.num_experts, c.num_channels,
+                                     c.expert_alignment, c.recv_capacity, num_tokens_per_rank,
+                                     num_tokens_per_rdma_rank, num_tokens_per_expert, is_token_in_rank,
+                                     h->rank_prefix, h->channel_prefix, h->recv_channel_prefix, h->num_recv,
+                                     h->send_head, h->recv_src_idx, num_recv_tokens_per_expert,
+                                     reinterpret_cast<uint32_t*>(h->layout_scratch), h->status, stream);
+        if (err != cudaSuccess) return cuda_fail(err, "layout scan launch");
+    } else if (h->plan.layout_notify_fused) {
         err = ep::launch_layout_notify(topk_idx, c.num_ranks, num_tokens, c.num_topk, c.num_experts, c.num_channels,
                                        c.expert_alignment, c.recv_capacity, num_tokens_per_rank,
                                        num_tokens_per_rdma_rank, num_tokens_per_expert, is_token_in_rank,

@@ -50,6 +50,18 @@ cudaError_t launch_dispatch_notify(int R, int T, int E, int C, int A, int64_t ca
 // a cooperative launch needs.
 bool layout_notify_fits(int R, int E);
 
+// Layout and the dispatch record in one pass (a decoupled look-back scan over token tiles) when
+// the ranks do not form whole nodes and layout_scan_fits(T) (1 <= T <= 32 tiles of 512 tokens).
+// scratch: layout_scan_scratch_words(R, E, maxT) words of device memory, zero before the first
+// launch; launches sharing it must be ordered.
+bool layout_scan_fits(int T);
+size_t layout_scan_scratch_words(int R, int E, int max_tokens);
+cudaError_t launch_layout_scan(const int64_t* topk_idx, int R, int T, int K, int E, int C, int A, int64_t cap,
+                               int32_t* tpr, int32_t* tprdma, int32_t* tpe, uint8_t* itr, int32_t* rank_prefix,
+                               int32_t* channel_prefix, int32_t* recv_channel_prefix, int32_t* num_recv,
+                               int32_t* send_head, int32_t* recv_src_idx, int32_t* num_recv_per_expert,
+                               uint32_t* scratch, int32_t* status, cudaStream_t stream);
+
 // get_dispatch_layout and dispatch_notify in one cooperative launch (layout_notify_fits).
 cudaError_t launch_layout_notify(const int64_t* topk_idx, int R, int T, int K, int E, int C, int A, int64_t cap,
                                  int32_t* tpr, int32_t* tprdma, int32_t* tpe, uint8_t* itr, int32_t* rank_prefix,

@@ -179,17 +179,19 @@ ep_status ep_notify_dispatch(ep_handle* h, int32_t num_tokens, const int32_t* nu
                              int32_t* num_recv_tokens_per_expert, ep_stream_t stream);
 
 /* ep_get_dispatch_layout() followed by ep_notify_dispatch(), in one launch
- * where the device holds the whole grid at once ([P3] §4.1: the layout, then
- * the notify step of the dispatch).  The layout outputs are written as by
- * ep_get_dispatch_layout() (num_tokens_per_rdma_rank optional) and the
- * dispatch record and num_recv_tokens_per_expert [R][EL] as by
- * ep_notify_dispatch(); follow with ep_dispatch() in EP_DISPATCH_PREPARED
- * mode with the same num_tokens.  The record needs every source's counts, so
- * the CTAs of the launch (R + 1 clusters of 8) meet at one grid barrier, which
- * the cooperative launch makes safe; the barrier's wait is bounded and a
- * timeout sets EP_ERR_TIMEOUT in the status word.  Where the grid does not fit
- * at once, the two steps are launched one after the other.  Errors as the two
- * calls it stands for. */
+ * ([P3] §4.1: the layout, then the notify step of the dispatch).  The layout
+ * outputs are written as by ep_get_dispatch_layout() (num_tokens_per_rdma_rank
+ * optional) and the dispatch record and num_recv_tokens_per_expert [R][EL] as
+ * by ep_notify_dispatch(); follow with ep_dispatch() in EP_DISPATCH_PREPARED
+ * mode with the same num_tokens.
+ * Without the node-level record and with 1 <= num_tokens <= 16384, one pass of a
+ * decoupled look-back scan: CTAs take tiles of 512 tokens in (source, token)
+ * order -- the receive order of every destination rank -- publish their
+ * per-rank hit counts and add up those of the earlier tiles.  Otherwise the
+ * CTAs of one cooperative launch (R + 1 clusters of 8) meet at a grid barrier,
+ * or, where that grid does not fit at once, the two steps run one after the
+ * other.  Every wait is bounded and a timeout sets EP_ERR_TIMEOUT in the
+ * status word.  Errors as the two calls it stands for. */
 ep_status ep_layout_notify(ep_handle* h, int32_t num_tokens, const int64_t* topk_idx, int32_t* num_tokens_per_rank,
                            int32_t* num_tokens_per_rdma_rank, int32_t* num_tokens_per_expert,
                            uint8_t* is_token_in_rank, int32_t* num_recv_tokens_per_expert, ep_stream_t stream);
