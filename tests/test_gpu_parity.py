@@ -140,8 +140,27 @@ def test_notify_then_prepared_dispatch_equals_fresh():
 
 @pytest.mark.parametrize("shape", NORMAL_CASES, ids=lambda s: s.name)
 def test_layout_notify_in_one_launch(shape):
-    """ep_layout_notify (layout and record in one cooperative launch) then a prepared dispatch and a
-    combine: every output equals the oracle, as with the separate calls."""
+    """ep_layout_notify (layout and record in one launch) then a prepared dispatch and a combine:
+    every output equals the oracle, as with the separate calls."""
+    _layout_notify_round(shape)
+
+
+# The one-pass scan takes up to 32 tiles of 512 tokens per source (its look-back window): T = 16384
+# is the last size it serves, T = 16385 goes to the cluster kernels; the third shape has a single
+# tile with a 1-token tail.
+SCAN_EDGE_CASES = [S("scan_max_tiles", 2, 16384, 16, 8, 2, routing="gumbel", mask_p=0.05, C=7, seed=80),
+                   S("scan_fallback", 3, 16385, 16, 12, 3, routing="zipf", C=5, A=4, seed=81),
+                   S("scan_tail", 5, 513, 16, 20, 4, mask_p=0.2, C=3, seed=82)]
+
+
+@pytest.mark.parametrize("shape", SCAN_EDGE_CASES, ids=lambda s: s.name)
+def test_layout_notify_scan_edges(shape):
+    """The one-pass layout + record at the edges of its tiling (32 tiles per source, the first size
+    past it, a 1-token last tile) equals the oracle."""
+    _layout_notify_round(shape)
+
+
+def _layout_notify_round(shape):
     idx, w = W.routing(shape)
     cap = max(P.needed_capacity(idx, shape.E), 1)
     h = ep.Handle(P.config_of(shape, cap))
