@@ -272,7 +272,7 @@ def run_ours(args):
     out = torch.empty((R, T, H), dtype=torch.bfloat16, device=dev)
     out_w = torch.empty((R, T, K), dtype=torch.float32, device=dev)
 
-    # The layout and the dispatch record come from one call (one cooperative launch); the
+    # The layout and the dispatch record come from one call (one launch); the
     # prepared dispatch then moves the rows, so the data kernel has its own pair of events.
     def layout_notify(idx_in):
         if args.layout_two_launches:
