@@ -124,6 +124,9 @@ ep_status check_config(const ep_config* c) {
                     static_cast<long long>(c->recv_capacity));
     const int64_t ll_rows = static_cast<int64_t>(c->num_ranks) * c->num_max_tokens;
     if (ll_rows > INT32_MAX) return fail(EP_ERR_UNSUPPORTED, "num_ranks * num_max_tokens exceeds 2^31");
+    // the top-k slots of one rank are indexed in int32
+    if (static_cast<int64_t>(c->num_max_tokens) * c->num_topk > INT32_MAX)
+        return fail(EP_ERR_UNSUPPORTED, "num_max_tokens * num_topk exceeds 2^31");
     return EP_OK;
 }
 

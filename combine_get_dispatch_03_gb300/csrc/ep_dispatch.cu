@@ -216,7 +216,7 @@ __global__ void dispatch_bulk_kernel(int R, int T, int H, int K, int EL, int64_t
     int32_t* s_row = reinterpret_cast<int32_t*>(smem + 64);                   // [S][32]
     int64_t* s_idx = reinterpret_cast<int64_t*>(smem + 64 + S * 128);         // [S][32]
     float* s_w = reinterpret_cast<float*>(smem + 64 + S * 384);               // [S][32]
-    int32_t* s_flag = reinterpret_cast<int32_t*>(smem + 64 + S * 512);
+    int32_t* s_flag = reinterpret_cast<int32_t*>(smem + 64 + S * 512);          // [2]
     uint8_t* in_base = smem + lay.meta_bytes;
     uint8_t* out_base = in_base + S * lay.in_stride;
 
@@ -255,9 +255,11 @@ __global__ void dispatch_bulk_kernel(int R, int T, int H, int K, int EL, int64_t
     int64_t j = 0;
     for (; j < n_local; ++j) {
         const int s = static_cast<int>(j % S);
-        if (tid == 0) *s_flag = mbar_wait_bounded(&bars[s], static_cast<uint32_t>((j / S) & 1)) ? 1 : 0;
+        // One flag per token parity: thread 0 may write token j+1's flag while a slower warp still
+        // reads token j's, but not token j+2's before every warp has passed token j+1's barrier.
+        if (tid == 0) s_flag[j & 1] = mbar_wait_bounded(&bars[s], static_cast<uint32_t>((j / S) & 1)) ? 1 : 0;
         __syncthreads();
-        if (*s_flag == 0) break;
+        if (s_flag[j & 1] == 0) break;
         const uint8_t* payload = in_base + s * lay.in_stride;
         if constexpr (kMode == kModeCastFp8) {
             const int4* xin = reinterpret_cast<const int4*>(payload);

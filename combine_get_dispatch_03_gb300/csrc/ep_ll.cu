@@ -236,7 +236,7 @@ __global__ void ll_dispatch_bulk_kernel(int R, int T, int maxT, int H, int K, in
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
     int32_t* s_row = reinterpret_cast<int32_t*>(smem + 64);            // [S][32]
     int64_t* s_idx = reinterpret_cast<int64_t*>(smem + 64 + S * 128);  // [S][32]
-    int32_t* s_flag = reinterpret_cast<int32_t*>(smem + 64 + S * 384);
+    int32_t* s_flag = reinterpret_cast<int32_t*>(smem + 64 + S * 384);            // [2]
     uint8_t* msg_base = smem + lay.meta_bytes;
     uint8_t* in_base = msg_base + S * lay.msg_stride;
     const int64_t slots = static_cast<int64_t>(R) * maxT;
@@ -274,9 +274,10 @@ __global__ void ll_dispatch_bulk_kernel(int R, int T, int maxT, int H, int K, in
     int64_t j = 0;
     for (; j < n_local; ++j) {
         const int st = static_cast<int>(j % S);
-        if (tid == 0) *s_flag = mbar_wait_bounded(&bars[st], static_cast<uint32_t>((j / S) & 1)) ? 1 : 0;
+        // one flag per token parity, as in the normal bulk dispatch
+        if (tid == 0) s_flag[j & 1] = mbar_wait_bounded(&bars[st], static_cast<uint32_t>((j / S) & 1)) ? 1 : 0;
         __syncthreads();
-        if (*s_flag == 0) break;
+        if (s_flag[j & 1] == 0) break;
         uint8_t* msg = msg_base + st * lay.msg_stride;
         const int64_t g = first + j;
         if constexpr (kFp8) {

@@ -6,9 +6,10 @@
 // not allocate, a server that reserves all device memory once at start-up and
 // forbids later allocations, or a latency-critical loop that cannot afford
 // the device-wide synchronisation cudaMalloc/cudaFree may cause.  For them,
-// ep_ll_dispatch_noalloc() runs the same three kernels with that count array
-// in a fixed-size file-scope __device__ array instead, and takes every other
-// buffer (slot map, status word included) from the caller.
+// ep_ll_dispatch_noalloc() runs the same kernels with that count array in a
+// fixed-size file-scope __device__ array instead, and takes every other
+// buffer (slot map, status word included) from the caller.  It has no handle,
+// so no rank mask applies.
 //
 // The array lives in the library image, so every GPU that loads the library
 // holds its 64 KiB until the process exits.  All calls on a device share it:
@@ -89,8 +90,9 @@ extern "C" ep_status ep_ll_dispatch_noalloc(int32_t num_ranks, int32_t num_token
                       "num_ranks * num_experts exceeds the fixed count scratch of ep_ll_dispatch_noalloc "
                       "(EP_LL_NOALLOC_MAX_COUNTS entries); use ep_ll_dispatch with a handle");
     if (K < 1 || K > ep::kMaxTopk) return reject(EP_ERR_UNSUPPORTED, "num_topk outside [1, 32]");
-    if (maxT < 0 || T < 0 || T > maxT || static_cast<int64_t>(R) * maxT > INT32_MAX)
-        return reject(EP_ERR_INVALID_ARG, "num_tokens must lie in [0, num_max_tokens]");
+    if (maxT < 0 || T < 0 || T > maxT) return reject(EP_ERR_INVALID_ARG, "num_tokens must lie in [0, num_max_tokens]");
+    if (static_cast<int64_t>(R) * maxT > INT32_MAX || static_cast<int64_t>(maxT) * K > INT32_MAX)
+        return reject(EP_ERR_UNSUPPORTED, "num_ranks * num_max_tokens or num_max_tokens * num_topk exceeds 2^31");
     if (H < 8 || H % 8 != 0) return reject(EP_ERR_INVALID_ARG, "hidden must be a positive multiple of 8");
     if (use_ue8m0 && !use_fp8) return reject(EP_ERR_INVALID_ARG, "use_ue8m0 needs use_fp8");
     if (use_fp8 && H % 512 != 0)

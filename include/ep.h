@@ -353,12 +353,21 @@ ep_status ep_selftest_bounded_wait(ep_handle* h, uint32_t max_iterations, int32_
  * callers that must not allocate device memory -- an engine plugin whose
  * enqueue path may not allocate, a server that reserves all device memory at
  * start-up, or a latency-critical loop that cannot take the synchronisation
- * cudaMalloc/cudaFree may cause.  It computes exactly what ep_ll_dispatch()
- * computes, without a handle: every buffer is the caller's, including the
- * slot map slot_row (int32 [R][maxT][K], row of each valid slot in its
- * expert's packed rows, -1 otherwise; ep_ll_dispatch() keeps it in the
- * handle) and the status word `status` (one device int32 that the kernels
- * set to the first error code and never clear; the caller zeroes it).
+ * cudaMalloc/cudaFree may cause.  It computes what ep_ll_dispatch() computes
+ * on a handle with no rank masked -- there is no handle, so no mask buffer
+ * applies and every rank sends and receives -- and every buffer is the
+ * caller's, including the slot map and the status word:
+ *   slot_row (int32 [R][maxT][K]): slot_row[s][t][k] is the row of slot
+ *     (s, t, k) among the packed rows of its expert e = topk_idx[s][t][k],
+ *     i.e. its message is recv_msgs[e / EL][e % EL][slot_row[s][t][k]]; -1
+ *     for a masked slot or a row past R*maxT.  Entries of tokens t >=
+ *     num_tokens are not written.  ep_ll_dispatch() keeps the same map in
+ *     its handle (EP_FIELD_LL_SLOT_ROW), and ep_ll_combine() reads only that
+ *     copy: no entry point of this library combines from a caller's
+ *     slot_row, so a caller of this function gathers the expert outputs back
+ *     with the map itself.
+ *   status (one device int32): the kernels set it to the first error code and
+ *     never clear it; the caller zeroes it.
  * The per-(source, expert) counts the kernels pass between them live in a
  * file-scope __device__ array of EP_LL_NOALLOC_MAX_COUNTS entries, so
  * num_ranks * num_experts beyond that is rejected with EP_ERR_UNSUPPORTED
