@@ -247,6 +247,93 @@ def prepare_normal(ep, shape, dev, with_e2e=True):
     return dict(idx=idx, w=w, idx_d=idx_d, w_d=w_d, x_d=x_d, cap=cap, hits=hits, h=h)
 
 
+# ----------------------------------------------------------------------------- parity capture
+# After each timed region the outputs of its last call are copied to host memory: the layout and
+# the dispatch record whole, payload rows and combined tokens on a seeded sample of tokens.  The
+# CPU-oracle leg (cpu_parity) later runs the oracle on the same inputs and compares.
+
+PARITY_TOKENS = 1024  # sampled tokens per checked call (plus the first and the last)
+
+
+def _host(t):
+    t = t.detach().to("cpu").contiguous()
+    if t.dtype == torch.bfloat16:
+        return t.view(torch.int16).numpy().view(np.uint16)
+    if t.dtype == torch.float8_e4m3fn:
+        return t.view(torch.uint8).numpy()
+    if t.dtype == torch.bool:
+        return t.numpy().astype(np.uint8)
+    return t.numpy()
+
+
+def _pairs(send_head_host, toks, R):
+    """(rank, row) of every destination of the sampled tokens."""
+    sh = send_head_host.reshape(-1, R)[toks]
+    i, r = np.nonzero(sh >= 0)
+    return np.stack([r, sh[i, r]], axis=1).astype(np.int64)
+
+
+def _rows(t, pairs):
+    idx = torch.from_numpy(pairs).to(t.device)
+    return _host(t[idx[:, 0], idx[:, 1]])
+
+
+def capture_normal(name, shape, h, idx, w, x_d, cap, *, mode=0, layout=None, nrpe=None, recv=None,
+                   x_scales=None, combine=None):
+    """Host copies of one normal-mode call's outputs for the oracle check.
+
+    layout: the four layout outputs (or None); nrpe: num_recv_tokens_per_expert (or None);
+    recv: receive buffers of the dispatch (recv_x, and optionally recv_x_scales, recv_topk_idx,
+    recv_topk_weights); combine: dict(y, out, and optionally out_w, b0, b1) of a combine (or None)."""
+    toks = W.sample_tokens(shape, PARITY_TOKENS, field="bench_parity")
+    t_idx = torch.from_numpy(toks).to(x_d.device)
+    rec = dict(kind="normal", name=name, shape=shape, idx=idx, w=w, cap=cap, mode=mode, toks=toks,
+               x_rows=_host(x_d.reshape(-1, shape.H)[t_idx]))
+    if x_scales is not None:
+        rec["x_scale_rows"] = _host(x_scales.reshape(-1, shape.H // 128)[t_idx])
+    rec["record"] = {k: _host(h.export(k)) for k in
+                     ("rank_prefix_matrix", "channel_prefix_matrix", "recv_channel_prefix_matrix", "num_recv",
+                      "send_head", "recv_src_idx")}
+    if layout is not None:
+        rec["layout"] = {k: (_host(v) if v is not None else None) for k, v in layout.items()}
+    if nrpe is not None:
+        rec["nrpe"] = _host(nrpe)
+    pairs = _pairs(rec["record"]["send_head"], toks, shape.R)
+    rec["pairs"] = pairs
+    if recv is not None:
+        rec["recv"] = {k: _rows(v, pairs) for k, v in recv.items() if v is not None}
+    if combine is not None:
+        c = dict(out_rows=_host(combine["out"].reshape(-1, shape.H)[t_idx]), y_rows=_rows(combine["y"], pairs))
+        if combine.get("out_w") is not None:
+            c["out_w"] = _host(combine["out_w"])
+        for b in ("b0", "b1"):
+            if combine.get(b) is not None:
+                c[b + "_rows"] = _host(combine[b].reshape(-1, shape.H)[t_idx])
+        rec["combine"] = c
+    return rec
+
+
+def capture_ll(name, shape, h, idx, w, x_d, out):
+    """Host copies of one low-latency dispatch (messages of the sampled tokens' slots, counts, layout
+    range, the slot map whole) and combine (the sampled tokens' outputs and the rows they read)."""
+    toks = W.sample_tokens(shape, PARITY_TOKENS, field="bench_parity")
+    t_idx = torch.from_numpy(toks).to(x_d.device)
+    rec = dict(kind="ll", name=name, shape=shape, idx=idx, w=w, toks=toks,
+               x_rows=_host(x_d.reshape(-1, shape.H)[t_idx]), slot_row=_host(h.export("ll_slot_row"))[:, :shape.T])
+    rec.update({k: _host(v) for k, v in out.items() if k in ("packed_recv_count", "packed_recv_layout_range")})
+    sl = rec["slot_row"].reshape(-1, shape.K)[toks]          # [n][K]
+    e = idx.reshape(-1, shape.K)[toks]
+    ok = (e >= 0) & (sl >= 0)
+    flat = torch.from_numpy(np.where(ok, e * (shape.R * shape.max_tokens) + sl, 0).reshape(-1)).to(x_d.device)
+    msgs = out["recv_msgs"].reshape(-1, out["recv_msgs"].shape[-1])
+    rec["msg_rows"] = _host(msgs[flat]).reshape(len(toks), shape.K, -1)
+    rec["ok"] = ok
+    if "y" in out:
+        rec["y_rows"] = _host(out["y"].reshape(-1, shape.H)[flat]).reshape(len(toks), shape.K, shape.H)
+        rec["out_rows"] = _host(out["combined_x"].reshape(-1, shape.H)[t_idx])
+    return rec
+
+
 def run_ours(args):
     from combine_get_dispatch_03_gb300 import ep
     rank, world, local = dist_setup()
@@ -309,6 +396,10 @@ def run_ours(args):
         wall = time.perf_counter() - t0
     barrier(world)
     h.check()
+    # the last timed step's outputs, for the oracle check of the CPU leg
+    checks = [capture_normal(HEADLINE + ".step", shape, h, st["idx"], st["w"], x_d, cap, layout=lay, nrpe=nrpe,
+                             recv=dict(recv_x=recv_x, recv_topk_idx=recv_i, recv_topk_weights=recv_w),
+                             combine=dict(y=recv_x, out=out, out_w=out_w))]
     step_ms = ev.ms(0, EV_PER_STEP * args.steps) / args.steps
     op_ms = {name: statistics.mean(ev.ms(EV_PER_STEP * i + j, EV_PER_STEP * i + j + 1) for i in range(args.steps))
              for j, name in enumerate(STEP_OPS)}
@@ -458,10 +549,12 @@ def run_ours(args):
         launch_model = measure_launch_model(ep, dev, peak, st)
         del st
         torch.cuda.empty_cache()
-        ops = measure_other_ops(ep, dev, peak)
+        ops = measure_other_ops(ep, dev, peak, checks)
 
     cpu = cpu_all = None
+    parity = {"checked": False, "note": "the oracle check runs in the CPU leg (rank 0, one GPU, without --no-cpu)"}
     if rank == 0 and world == 1 and not args.no_cpu:
+        parity = cpu_parity(checks)
         cpu = cpu_baseline(W.WORKLOADS[HEADLINE], args.cpu_seconds)
         cpu_all = cpu_baseline_all_cores(W.WORKLOADS[HEADLINE], args.cpu_seconds)
 
@@ -481,10 +574,12 @@ def run_ours(args):
         "cpu_baseline": cpu, "cpu_baseline_all_cores": cpu_all, "clocks": clocks.summary(), "e2e": e2e,
         "gpu_launches": (4 if args.layout_two_launches else 3) * args.steps,  # per step: layout + notify
                                                                               # (one or two), dispatch, combine
-        "wall_s_timed": round(wall, 3), "ops": ops,
+        "wall_s_timed": round(wall, 3), "ops": ops, "parity": parity,
     }
     if rank == 0:
         print(json.dumps(result), flush=True)
+    if parity.get("checked") and not parity.get("ok"):
+        sys.exit(1)
 
 
 def timed(fn, reps, stream, warmup=3, batches=5):
@@ -664,8 +759,9 @@ def run_fp8_calls(n, tokens=0, fp8_input=False):
                       "fp8_dispatch_us": round(a.elapsed_time(b) * 1e3 / n, 2)}))
 
 
-def measure_other_ops(ep, dev, peak, reps=10):
-    """Per-op times of the other workloads (median of reps, after warm-up)."""
+def measure_other_ops(ep, dev, peak, checks, reps=10):
+    """Per-op times of the other workloads (median of reps, after warm-up); the outputs of each
+    timed op's last call are appended to `checks` for the oracle check."""
     stream = torch.cuda.current_stream(dev)
     res = {}
 
@@ -692,6 +788,10 @@ def measure_other_ops(ep, dev, peak, reps=10):
                                 num_tokens_per_expert=lay["num_tokens_per_expert"], **bufs)
     ms = timed(fn, reps, stream)
     h.check()
+    checks.append(capture_normal("fp8_zipf.dispatch_fp8", shape, h, st["idx"], st["w"], st["x_d"], st["cap"], mode=1,
+                                 layout=lay, nrpe=bufs["num_recv_tokens_per_expert"],
+                                 recv={k: bufs[k] for k in ("recv_x", "recv_x_scales", "recv_topk_idx",
+                                                            "recv_topk_weights")}))
     b = normal_bytes(shape.R, shape.T, shape.H, shape.K, st["hits"], fp8=True)
     report("fp8_zipf.dispatch_fp8", ms, {"payload": b["dispatch"]["payload"],
                                          "meta": b["dispatch"]["meta"] + total(b["notify"])},
@@ -703,6 +803,8 @@ def measure_other_ops(ep, dev, peak, reps=10):
                                  recv_x_scales=bufs["recv_x_scales"])
     ms8 = timed(fn8, reps, stream)
     h.check()
+    checks.append(capture_normal("fp8_zipf.dispatch_fp8_input_cached", shape, h, st["idx"], st["w"], x8, st["cap"],
+                                 mode=2, x_scales=xs, recv={k: bufs[k] for k in ("recv_x", "recv_x_scales")}))
     row8 = shape.H + 4 * G
     report("fp8_zipf.dispatch_fp8_input_cached", ms8,
            {"payload": n * row8 + st["hits"] * row8, "meta": n * shape.R * 4},
@@ -734,6 +836,9 @@ def measure_other_ops(ep, dev, peak, reps=10):
 
     ms = timed(comb, reps, stream)
     h.check()
+    checks.append(capture_normal("combine_heavy.combine", shape, h, st["idx"], st["w"], st["x_d"], st["cap"],
+                                 layout=lay, recv=dict(recv_x=d["recv_x"]),
+                                 combine=dict(y=ys[it[0] % 2], out=out, out_w=cw, b0=b0, b1=b1)))
     b = normal_bytes(shape.R, shape.T, shape.H, shape.K, st["hits"], biases=2)
     report("combine_heavy.combine", ms, b["combine"], {"rho": round(st["hits"] / (shape.R * shape.T), 3)})
     report("combine_heavy.dispatch_cached", ms_disp, {"payload": b["dispatch"]["payload"],
@@ -762,6 +867,9 @@ def measure_other_ops(ep, dev, peak, reps=10):
     ms_c = timed(lambda: ep.ep_ll_combine(h, y, idx_d, w_d, combined_x=out), reps, stream)
     cold_c = timed_cold(lambda: ep.ep_ll_combine(h, y, idx_d, w_d, combined_x=out), 2 * reps, stream, flush)
     h.check()
+    checks.append(capture_ll("ll_v3.ll_dispatch_fp8_ue8m0+ll_combine", shape, h, idx, w, x_d,
+                             dict(recv_msgs=msgs, packed_recv_count=cnt, packed_recv_layout_range=rng_, y=y,
+                                  combined_x=out)))
     n_valid = int((idx >= 0).sum())
     b = ll_bytes(shape.R, shape.T, shape.H, shape.K, n_valid, msg)
     warm = "calls back to back (the 58.7 MB of tokens can stay in the 129 MB L2)"
@@ -818,12 +926,123 @@ def measure_other_ops(ep, dev, peak, reps=10):
         small_step()
     ms = timed(graph.replay, reps, stream)
     h.check()
+    checks.append(capture_normal("normal_small.step_graph", shape, h, st["idx"], st["w"], st["x_d"], cap, layout=lay,
+                                 nrpe=bufs["num_recv_tokens_per_expert"],
+                                 recv={k: bufs[k] for k in ("recv_x", "recv_topk_idx", "recv_topk_weights")},
+                                 combine=dict(y=bufs["recv_x"], out=out, out_w=cw)))
     report("normal_small.step_graph", ms, step_b, {"note": "the same step captured once in a CUDA graph"})
     h.destroy()
     return res
 
 
 # ----------------------------------------------------------------------------- CPU oracle
+
+def _check_normal(O, rec):
+    """The oracle on one captured normal-mode call: layout and record whole, rows and tokens sampled."""
+    shape, cap, toks, pairs = rec["shape"], rec["cap"], rec["toks"], rec["pairs"]
+    R, T, H, E, K = shape.R, shape.T, shape.H, shape.E, shape.K
+    bad = []
+    lay = O.get_dispatch_layout(rec["idx"], E, with_rdma=True)
+    n = O.dispatch_notify(lay["num_tokens_per_rank"], lay["is_token_in_rank"], lay["num_tokens_per_expert"],
+                          shape.C, shape.A, cap)
+    for k, v in rec.get("layout", {}).items():
+        if v is not None and not np.array_equal(v, lay[k]):
+            bad.append(k)
+    for k, v in rec["record"].items():
+        want = n[k]
+        if k == "recv_src_idx":
+            m = np.arange(cap)[None, :] < np.minimum(n["num_recv"], cap)[:, None]
+            v, want = v[m], want[m]
+        if not np.array_equal(v, want):
+            bad.append(k)
+    if "nrpe" in rec and not np.array_equal(rec["nrpe"], n["num_recv_tokens_per_expert"]):
+        bad.append("num_recv_tokens_per_expert")
+    mode = rec["mode"]
+    x = np.zeros((R * T, H), np.uint8 if mode == 2 else np.uint16)  # only the sampled rows are touched
+    x[toks] = rec["x_rows"]
+    xs = None
+    if "x_scale_rows" in rec:
+        xs = np.zeros((R * T, H // 128), np.float32)
+        xs[toks] = rec["x_scale_rows"]
+        xs = xs.reshape(R, T, H // 128)
+    c = rec.get("combine")
+    with_topk = "recv_topk_idx" in rec.get("recv", {}) or (c is not None and "out_w" in c)
+    d = O.dispatch(x.reshape(R, T, H), n["send_head"], cap, E, mode=mode, x_scales=xs,
+                   topk_idx=rec["idx"] if with_topk else None, topk_weights=rec["w"] if with_topk else None,
+                   tokens=toks)
+    for k, v in rec.get("recv", {}).items():
+        if not np.array_equal(v, d[k][pairs[:, 0], pairs[:, 1]]):
+            bad.append(k)
+    if c is not None:
+        y = np.zeros((R, cap, H), np.uint16)
+        y[pairs[:, 0], pairs[:, 1]] = c["y_rows"]
+        rw = d["recv_topk_weights"] if "out_w" in c else None  # the oracle's own dispatched weights
+        bias = {}
+        for b in ("b0", "b1"):
+            if b + "_rows" in c:
+                a = np.zeros((R * T, H), np.uint16)
+                a[toks] = c[b + "_rows"]
+                bias[b] = a.reshape(R, T, H)
+        oc = O.combine(y, n["send_head"], recv_topk_weights=rw, bias0=bias.get("b0"), bias1=bias.get("b1"),
+                       num_topk=K, tokens=toks)
+        if not np.array_equal(c["out_rows"], oc["out"].reshape(-1, H)[toks]):
+            bad.append("combined_x")
+        if "out_w" in c:
+            # every token: one nonzero term per valid slot, so the reduction returns the routing's weights
+            want = np.where(rec["idx"] >= 0, rec["w"], 0).astype(np.float32)
+            if not np.array_equal(c["out_w"], want) or \
+                    not np.array_equal(c["out_w"].reshape(-1, K)[toks], oc["combined_topk_weights"].reshape(-1, K)[toks]):
+                bad.append("combined_topk_weights")
+    return bad, len(toks)
+
+
+def _check_ll(O, rec):
+    """The oracle on one captured low-latency dispatch + combine: counts, layout range and the slot map
+    whole, the sampled tokens' messages and combined outputs."""
+    shape, toks = rec["shape"], rec["toks"]
+    R, T, H, E, K, maxT = shape.R, shape.T, shape.H, shape.E, shape.K, shape.max_tokens
+    bad = []
+    x = np.zeros((R * T, H), np.uint16)
+    x[toks] = rec["x_rows"]
+    o = O.ll_dispatch(x.reshape(R, T, H), rec["idx"], maxT, E, use_fp8=True, use_ue8m0=True)
+    for k in ("packed_recv_count", "packed_recv_layout_range", "slot_row"):
+        if not np.array_equal(rec[k], o[k]):
+            bad.append(k)
+    want = o["msgs_by_slot"].reshape(R * T, K, -1)[toks]
+    ok = rec["ok"]
+    if not np.array_equal(rec["msg_rows"][ok], want[ok]):
+        bad.append("messages")
+    if "y_rows" in rec:
+        y = np.zeros((R, E // R, R * maxT, H), np.uint16)
+        e = rec["idx"].reshape(-1, K)[toks]
+        sl = o["slot_row"].reshape(-1, K)[toks]
+        for i in range(len(toks)):
+            for k in range(K):
+                if ok[i, k]:
+                    y[e[i, k] // (E // R), e[i, k] % (E // R), sl[i, k]] = rec["y_rows"][i, k]
+        got = O.ll_combine(y, rec["idx"], rec["w"], o["slot_row"], maxT, E, tokens=toks)
+        if not np.array_equal(rec["out_rows"], got.reshape(-1, H)[toks]):
+            bad.append("ll combined_x")
+    return bad, len(toks)
+
+
+def cpu_parity(checks):
+    """The CPU-oracle leg's check of the timed calls: each captured call against the oracle."""
+    import oracle as O
+    t0 = time.perf_counter()
+    res, ok = {}, True
+    for rec in checks:
+        bad, n = (_check_ll if rec["kind"] == "ll" else _check_normal)(O, rec)
+        res[rec["name"]] = {"status": "ok" if not bad else "MISMATCH: " + ", ".join(bad), "tokens_sampled": n}
+        ok = ok and not bad
+    return {"checked": True, "ok": ok, "calls": res,
+            "whole": "layout outputs, the dispatch record, num_recv_tokens_per_expert, the combined top-k weights, "
+                     "LL counts / layout range / slot map",
+            "sampled": "receive rows and scales of the sampled tokens' destinations, their combined tokens, "
+                       "their LL messages",
+            "what": "the outputs of the last timed call of each line, against the CPU oracle on the same inputs",
+            "seconds": round(time.perf_counter() - t0, 2)}
+
 
 def cpu_sample(shape, tokens: int):
     """Inputs of the oracle sample: the first `tokens` tokens of every rank of the workload."""

@@ -174,3 +174,53 @@ def rel_err(a: np.ndarray, b: np.ndarray) -> float:
         return 0.0
     floor = 1e-3 * max(np.sqrt(np.mean(b * b)), 1e-30)
     return float(np.max(np.abs(a - b) / np.maximum(np.abs(b), floor)))
+
+
+def host_threads() -> int:
+    import os
+    return len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+
+
+def oracle_dispatch_all(x, send_head, cap, E, mode=O.MODE_BF16, x_scales=None, topk_idx=None, topk_weights=None):
+    """oracle.dispatch over every token, its token loop split into contiguous blocks over the host cores
+    (the C calls release the interpreter lock; the blocks write disjoint receive rows)."""
+    from concurrent.futures import ThreadPoolExecutor
+    R, T, H = x.shape
+    K = topk_idx.shape[2] if topk_idx is not None else 1
+    pay = np.uint16 if mode == O.MODE_BF16 else np.uint8
+    out = dict(recv_x=np.zeros((R, cap, H), pay))
+    if mode != O.MODE_BF16:
+        out["recv_x_scales"] = np.zeros((R, cap, H // 128), np.float32)
+    if topk_idx is not None:
+        out["recv_topk_idx"] = np.full((R, cap, K), -2, np.int64)
+        if topk_weights is not None:
+            out["recv_topk_weights"] = np.full((R, cap, K), np.nan, np.float32)
+    n = host_threads()
+    blocks = np.array_split(np.arange(R * T, dtype=np.int64), n)
+    with ThreadPoolExecutor(n) as ex:
+        list(ex.map(lambda b: O.dispatch(x, send_head, cap, E, mode=mode, x_scales=x_scales, topk_idx=topk_idx,
+                                         topk_weights=topk_weights, tokens=b, out=out), blocks))
+    return out
+
+
+def oracle_combine_all(y, send_head, recv_topk_weights=None, bias0=None, bias1=None, out_fp32=False, num_topk=1):
+    """oracle.combine over every token, split over the host cores like oracle_dispatch_all."""
+    from concurrent.futures import ThreadPoolExecutor
+    R, T, _ = send_head.shape
+    H = y.shape[2]
+    K = recv_topk_weights.shape[2] if recv_topk_weights is not None else num_topk
+    out = dict(out=np.zeros((R, T, H), np.float32 if out_fp32 else np.uint16),
+               combined_topk_weights=np.zeros((R, T, K), np.float32) if recv_topk_weights is not None else None)
+    n = host_threads()
+    blocks = np.array_split(np.arange(R * T, dtype=np.int64), n)
+    with ThreadPoolExecutor(n) as ex:
+        list(ex.map(lambda b: O.combine(y, send_head, recv_topk_weights=recv_topk_weights, bias0=bias0, bias1=bias1,
+                                        out_fp32=out_fp32, num_topk=num_topk, tokens=b, out=out), blocks))
+    return out
+
+
+def assert_rows_equal(gpu: torch.Tensor, ora: np.ndarray, num_recv, name: str):
+    """Receive rows [0, num_recv[r]) of every rank r, whole, one rank at a time (bounded host memory)."""
+    for r, n in enumerate(num_recv):
+        n = int(min(n, ora.shape[1]))
+        np.testing.assert_array_equal(host(gpu[r, :n]), ora[r, :n], err_msg=f"{name}[{r}]")

@@ -1,8 +1,10 @@
 """The five named workloads at their full sizes, in the launch configuration bench.py times.
 
-Integer outputs (layout, dispatch record, LL packing) are compared whole with the
-oracle; payload rows and combine outputs on a seeded sample of tokens (the oracle
-evaluates exactly those tokens), plus properties over every token.
+The benchmark's own step and ops (test_*_timed_*) are compared whole with the
+oracle: every layout output, the whole dispatch record, every receive row and
+every combined token, with the oracle's token loops split over the host cores.
+The other tests compare integer outputs whole and payload rows and combine
+outputs on a seeded sample of tokens, plus properties over every token.
 """
 import numpy as np
 import pytest
@@ -187,3 +189,113 @@ def test_ll_v3_full():
     y_host.reshape(-1, shape.H)[flat.cpu().numpy()] = P.host(vals)
     want = O.ll_combine(y_host, idx, w, ora["slot_row"], maxT, shape.E)
     np.testing.assert_array_equal(P.host(got), want)
+
+
+def test_headline_step_timed_whole():
+    """normal_v3 exactly as the benchmark's timed step runs it: layout + record in one launch
+    (ep_layout_notify), the prepared bf16 dispatch with top-k metadata, then the combine of the
+    received rows with the top-k weight reduction.  Every output against the oracle, whole."""
+    shape = W.WORKLOADS["normal_v3"]
+    R, T, H, E, K = shape.R, shape.T, shape.H, shape.E, shape.K
+    idx, w = W.routing(shape)
+    ora_lay = O.get_dispatch_layout(idx, E, with_rdma=False)
+    cap = int(ora_lay["num_tokens_per_rank"].sum(axis=0).max())
+    ora_n = O.dispatch_notify(ora_lay["num_tokens_per_rank"], ora_lay["is_token_in_rank"],
+                              ora_lay["num_tokens_per_expert"], shape.C, shape.A, cap)
+    dev = torch.device("cuda")
+    idx_d, w_d = torch.from_numpy(idx).to(dev), torch.from_numpy(w).to(dev)
+    x_d = W.tokens_x(shape, device=dev)
+    h = ep.Handle(P.config_of(shape, cap), dev)
+    lay = dict(num_tokens_per_rank=torch.empty((R, R), dtype=torch.int32, device=dev), num_tokens_per_rdma_rank=None,
+               num_tokens_per_expert=torch.empty((R, E), dtype=torch.int32, device=dev),
+               is_token_in_rank=torch.empty((R, T, R), dtype=torch.bool, device=dev))
+    nrpe = torch.empty((R, E // R), dtype=torch.int32, device=dev)
+    recv_x = torch.empty((R, cap, H), dtype=torch.bfloat16, device=dev)
+    recv_i = torch.empty((R, cap, K), dtype=torch.int64, device=dev)
+    recv_w = torch.empty((R, cap, K), dtype=torch.float32, device=dev)
+    out = torch.empty((R, T, H), dtype=torch.bfloat16, device=dev)
+    out_w = torch.empty((R, T, K), dtype=torch.float32, device=dev)
+    for _ in range(2):  # the second step runs on a handle and buffers the first one used, as in the benchmark
+        ep.ep_layout_notify(h, idx_d, num_recv_tokens_per_expert=nrpe, **lay)
+        ep.ep_dispatch(h, x_d, topk_idx=idx_d, topk_weights=w_d, recv_x=recv_x, recv_topk_idx=recv_i,
+                       recv_topk_weights=recv_w, prepared=True)
+        ep.ep_combine(h, recv_x, topk_weights=recv_w, combined_x=out, combined_topk_weights=out_w)
+    assert h.status() == 0
+    P.compare_layout(lay, ora_lay)
+    P.compare_record(h, ora_n, T)
+    np.testing.assert_array_equal(P.host(nrpe), ora_n["num_recv_tokens_per_expert"])
+    ora_d = P.oracle_dispatch_all(P.host(x_d), ora_n["send_head"], cap, E, topk_idx=idx, topk_weights=w)
+    P.assert_rows_equal(recv_x, ora_d["recv_x"], ora_n["num_recv"], "recv_x")
+    P.assert_rows_equal(recv_i, ora_d["recv_topk_idx"], ora_n["num_recv"], "recv_topk_idx")
+    P.assert_rows_equal(recv_w, ora_d["recv_topk_weights"], ora_n["num_recv"], "recv_topk_weights")
+    ora_c = P.oracle_combine_all(ora_d["recv_x"], ora_n["send_head"], recv_topk_weights=ora_d["recv_topk_weights"])
+    np.testing.assert_array_equal(P.host(out), ora_c["out"])
+    np.testing.assert_array_equal(P.host(out_w), ora_c["combined_topk_weights"])
+    h.destroy()
+
+
+def test_fp8_zipf_timed_dispatch_whole():
+    """fp8_zipf as the benchmark times it: a fresh dispatch with the fused FP8 cast and top-k
+    metadata after ep_get_dispatch_layout, then the FP8-input dispatch (codes and scales moved
+    unchanged) on the cached record.  Every receive row, scale and top-k entry, whole."""
+    shape = W.WORKLOADS["fp8_zipf"]
+    R, T, H, E, K = shape.R, shape.T, shape.H, shape.E, shape.K
+    st = setup_normal(shape)
+    h, cap, ora_n = st["h"], st["cap"], st["ora_n"]
+    bufs = dict(recv_x=torch.empty((R, cap, H), dtype=torch.float8_e4m3fn, device="cuda"),
+                recv_x_scales=torch.empty((R, cap, H // 128), dtype=torch.float32, device="cuda"),
+                recv_topk_idx=torch.empty((R, cap, K), dtype=torch.int64, device="cuda"),
+                recv_topk_weights=torch.empty((R, cap, K), dtype=torch.float32, device="cuda"),
+                num_recv_tokens_per_expert=torch.empty((R, shape.EL), dtype=torch.int32, device="cuda"))
+    P.compare_layout(st["lay"], st["ora_lay"])
+    ep.ep_dispatch(h, st["x_d"], topk_idx=st["idx_d"], topk_weights=st["w_d"], cast_to_fp8=True,
+                   num_tokens_per_rank=st["lay"]["num_tokens_per_rank"], is_token_in_rank=st["lay"]["is_token_in_rank"],
+                   num_tokens_per_expert=st["lay"]["num_tokens_per_expert"], **bufs)
+    assert h.status() == 0
+    P.compare_record(h, ora_n, T)
+    np.testing.assert_array_equal(P.host(bufs["num_recv_tokens_per_expert"]), ora_n["num_recv_tokens_per_expert"])
+    ora = P.oracle_dispatch_all(P.host(st["x_d"]), ora_n["send_head"], cap, E, mode=O.MODE_CAST_FP8,
+                                topk_idx=st["idx"], topk_weights=st["w"])
+    for key in ("recv_x", "recv_x_scales", "recv_topk_idx", "recv_topk_weights"):
+        P.assert_rows_equal(bufs[key], ora[key], ora_n["num_recv"], key)
+    del ora
+    # FP8 input on the cached record: already-cast codes (no NaN codes) and scales
+    g = torch.Generator(device="cuda")
+    g.manual_seed(shape.seed + 11)
+    x8 = torch.randint(0, 126, (R, T, H), dtype=torch.uint8, device="cuda", generator=g).view(torch.float8_e4m3fn)
+    xs = torch.rand((R, T, H // 128), dtype=torch.float32, device="cuda", generator=g)
+    ep.ep_dispatch(h, x8, x_scales=xs, cached=True, recv_x=bufs["recv_x"], recv_x_scales=bufs["recv_x_scales"])
+    assert h.status() == 0
+    ora = P.oracle_dispatch_all(P.host(x8), ora_n["send_head"], cap, E, mode=O.MODE_FP8_IN, x_scales=P.host(xs))
+    for key in ("recv_x", "recv_x_scales"):
+        P.assert_rows_equal(bufs[key], ora[key], ora_n["num_recv"], key)
+    h.destroy()
+
+
+def test_combine_heavy_timed_combine_whole():
+    """combine_heavy as the benchmark times it: one fresh dispatch, then combines of fresh expert
+    outputs with two biases and the top-k weight reduction on the cached record.  The second
+    combine (it runs on the claim counters the first one left) against the oracle, whole."""
+    shape = W.WORKLOADS["combine_heavy"]
+    R, T, H, K = shape.R, shape.T, shape.H, shape.K
+    st = setup_normal(shape)
+    h, cap, ora_n = st["h"], st["cap"], st["ora_n"]
+    d = ep.ep_dispatch(h, st["x_d"], topk_idx=st["idx_d"], topk_weights=st["w_d"],
+                       num_tokens_per_rank=st["lay"]["num_tokens_per_rank"],
+                       is_token_in_rank=st["lay"]["is_token_in_rank"],
+                       num_tokens_per_expert=st["lay"]["num_tokens_per_expert"])
+    b0, b1 = W.biases(shape, device="cuda")
+    out = torch.empty((R, T, H), dtype=torch.bfloat16, device="cuda")
+    cw = torch.empty((R, T, K), dtype=torch.float32, device="cuda")
+    for i in range(2):
+        y = W.expert_outputs(shape, R * cap, i, device="cuda").view(R, cap, H)
+        ep.ep_combine(h, y, topk_weights=d["recv_topk_weights"], bias_0=b0, bias_1=b1, combined_x=out,
+                      combined_topk_weights=cw)
+    assert h.status() == 0
+    ora_w = P.oracle_dispatch_all(np.zeros((R, T, 8), np.uint16), ora_n["send_head"], cap, shape.E,
+                                  topk_idx=st["idx"], topk_weights=st["w"])["recv_topk_weights"]
+    ora_c = P.oracle_combine_all(P.host(y), ora_n["send_head"], recv_topk_weights=ora_w, bias0=P.host(b0),
+                                 bias1=P.host(b1))
+    np.testing.assert_array_equal(P.host(out), ora_c["out"])
+    np.testing.assert_array_equal(P.host(cw), ora_c["combined_topk_weights"])
+    h.destroy()
