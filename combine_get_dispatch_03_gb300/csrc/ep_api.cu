@@ -39,8 +39,7 @@ struct ep_handle {
     int32_t* rank_mask = nullptr;            // [R], nonzero = masked
     int32_t* rdma_channel_prefix = nullptr;    // [R][NN][C], NN = R / 8 whole nodes (see has_nodes)
     int32_t* recv_rdma_rank_prefix = nullptr;  // [R][NN]
-    int32_t* barrier = nullptr;                // [4]: count and generation of the layout + notify grid barrier;
-                                               // the combine's next token and finished warps
+    int32_t* claims = nullptr;                 // [2]: the combine's next token and finished warps
     int32_t* layout_scratch = nullptr;         // tile states of the one-pass layout + record scan
     int normal_tokens = -1;                  // T of the current dispatch record, -1 = none
     bool prepared = false;                   // record built by ep_notify_dispatch, not yet used
@@ -190,7 +189,6 @@ ep_status ep_handle_create(const ep_config* cfg, ep_handle** out) {
     }
     if (err == cudaSuccess) err = ep::plan_dispatch_combine(&h->plan, cfg->hidden);
     if (err == cudaSuccess) err = ep::plan_ll(&h->plan, cfg->num_experts);
-    if (err == cudaSuccess) h->plan.layout_notify_fused = ep::layout_notify_fits(cfg->num_ranks, cfg->num_experts);
     if (err != cudaSuccess) {
         delete h;
         return cuda_fail(err, "planning launches");
@@ -201,11 +199,11 @@ ep_status ep_handle_create(const ep_config* cfg, ep_handle** out) {
     const size_t NN = (R + 7) / 8;
     const size_t scan_words = ep::layout_scan_scratch_words(cfg->num_ranks, cfg->num_experts, cfg->num_max_tokens);
     const size_t sizes[] = {1, R * R, R * R * C, R * R * C, R, R * cap, R * T * R, R * T * K, R * E, R,
-                            R * NN * C, R * NN, 4, scan_words};
+                            R * NN * C, R * NN, 2, scan_words};
     int32_t** slots[] = {&h->status,   &h->rank_prefix,  &h->channel_prefix, &h->recv_channel_prefix,
                          &h->num_recv, &h->recv_src_idx, &h->send_head,      &h->ll_slot,
                          &h->ll_cnt,   &h->rank_mask,    &h->rdma_channel_prefix, &h->recv_rdma_rank_prefix,
-                         &h->barrier,  &h->layout_scratch};
+                         &h->claims,   &h->layout_scratch};
     size_t total = 0;
     for (size_t s : sizes) total += align_up(s * sizeof(int32_t), 256);
     err = cudaMalloc(&h->dmem, total);
@@ -219,7 +217,7 @@ ep_status ep_handle_create(const ep_config* cfg, ep_handle** out) {
         *slots[i] = reinterpret_cast<int32_t*>(static_cast<char*>(h->dmem) + off);
         off += align_up(sizes[i] * sizeof(int32_t), 256);
     }
-    err = cudaMemset(h->dmem, 0, total);
+    err = cudaMemset(h->dmem, 0, total);  // the status word, the claim counters and the scan's tickets start at 0
     if (err != cudaSuccess) {
         cudaFree(h->dmem);
         delete h;
@@ -333,8 +331,8 @@ ep_status ep_get_dispatch_layout(ep_handle* h, int32_t num_tokens, const int64_t
                      aligned4(num_tokens_per_rdma_rank) && aligned16(is_token_in_rank),
                  "misaligned layout pointer");
     DeviceGuard guard(h->device);
-    cudaError_t err = ep::launch_get_dispatch_layout(topk_idx, c.num_ranks, num_tokens, c.num_topk, c.num_experts,
-                                                     num_tokens_per_rank, num_tokens_per_rdma_rank,
+    cudaError_t err = ep::launch_get_dispatch_layout(topk_idx, h->rank_mask, c.num_ranks, num_tokens, c.num_topk,
+                                                     c.num_experts, num_tokens_per_rank, num_tokens_per_rdma_rank,
                                                      num_tokens_per_expert, is_token_in_rank, h->status, stream);
     if (err != cudaSuccess) return cuda_fail(err, "get_dispatch_layout launch");
     return EP_OK;
@@ -475,27 +473,21 @@ ep_status ep_layout_notify(ep_handle* h, int32_t num_tokens, const int64_t* topk
                  "misaligned layout pointer");
     DeviceGuard guard(h->device);
     cudaError_t err;
-    if (node_record(h, 0) == nullptr && ep::layout_scan_fits(num_tokens)) {
+    if (num_tokens >= 1) {
         // one pass: a decoupled look-back scan over token tiles in receive order
-        err = ep::launch_layout_scan(topk_idx, c.num_ranks, num_tokens, c.num_topk, c.num_experts, c.num_channels,
-                                     c.expert_alignment, c.recv_capacity, num_tokens_per_rank,
+        err = ep::launch_layout_scan(topk_idx, h->rank_mask, c.num_ranks, num_tokens, c.num_topk, c.num_experts,
+                                     c.num_channels, c.expert_alignment, c.recv_capacity, num_tokens_per_rank,
                                      num_tokens_per_rdma_rank, num_tokens_per_expert, is_token_in_rank,
                                      h->rank_prefix, h->channel_prefix, h->recv_channel_prefix, h->num_recv,
-                                     h->send_head, h->recv_src_idx, num_recv_tokens_per_expert,
-                                     reinterpret_cast<uint32_t*>(h->layout_scratch), h->status, stream);
+                                     h->send_head, h->recv_src_idx, num_recv_tokens_per_expert, node_record(h, 0),
+                                     node_record(h, 1), reinterpret_cast<uint32_t*>(h->layout_scratch), h->status,
+                                     stream);
         if (err != cudaSuccess) return cuda_fail(err, "layout scan launch");
-    } else if (h->plan.layout_notify_fused) {
-        err = ep::launch_layout_notify(topk_idx, c.num_ranks, num_tokens, c.num_topk, c.num_experts, c.num_channels,
-                                       c.expert_alignment, c.recv_capacity, num_tokens_per_rank,
-                                       num_tokens_per_rdma_rank, num_tokens_per_expert, is_token_in_rank,
-                                       h->rank_prefix, h->channel_prefix, h->recv_channel_prefix, h->num_recv,
-                                       h->send_head, h->recv_src_idx, num_recv_tokens_per_expert, node_record(h, 0),
-                                       node_record(h, 1), reinterpret_cast<uint32_t*>(h->barrier), h->status, stream);
-        if (err != cudaSuccess) return cuda_fail(err, "layout_notify launch");
     } else {
-        err = ep::launch_get_dispatch_layout(topk_idx, c.num_ranks, num_tokens, c.num_topk, c.num_experts,
-                                             num_tokens_per_rank, num_tokens_per_rdma_rank, num_tokens_per_expert,
-                                             is_token_in_rank, h->status, stream);
+        // no tokens: the two calls it stands for (their kernels write the empty record)
+        err = ep::launch_get_dispatch_layout(topk_idx, h->rank_mask, c.num_ranks, num_tokens, c.num_topk,
+                                             c.num_experts, num_tokens_per_rank, num_tokens_per_rdma_rank,
+                                             num_tokens_per_expert, is_token_in_rank, h->status, stream);
         if (err == cudaSuccess)
             err = ep::launch_dispatch_notify(
                 c.num_ranks, num_tokens, c.num_experts, c.num_channels, c.expert_alignment, c.recv_capacity,
@@ -528,7 +520,7 @@ ep_status ep_combine(ep_handle* h, const void* x, const float* topk_weights, con
     DeviceGuard guard(h->device);
     cudaError_t err = ep::launch_combine(h->plan, out_dtype == EP_FP32, c.num_ranks, T, c.hidden, c.num_topk,
                                          c.recv_capacity, h->send_head, x, topk_weights, bias_0, bias_1, combined_x,
-                                         combined_topk_weights, reinterpret_cast<uint32_t*>(h->barrier) + 2, stream);
+                                         combined_topk_weights, reinterpret_cast<uint32_t*>(h->claims), stream);
     if (err != cudaSuccess) return cuda_fail(err, "combine launch");
     return EP_OK;
 }

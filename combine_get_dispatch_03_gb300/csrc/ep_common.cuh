@@ -260,58 +260,4 @@ cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_
     return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 
-// Cooperative launch (every CTA resident at once, so CTAs may wait on one another) with a 1-D
-// cluster; ordinary stream order with the previous kernel.
-template <typename... KArgs, typename... Args>
-cudaError_t launch_kernel_cooperative(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
-                                      cudaStream_t stream, unsigned cluster_x, Args&&... args) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = grid;
-    cfg.blockDim = block;
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[2];
-    attr[0].id = cudaLaunchAttributeCooperative;
-    attr[0].val.cooperative = 1;
-    attr[1].id = cudaLaunchAttributeClusterDimension;
-    attr[1].val.clusterDim.x = cluster_x;
-    attr[1].val.clusterDim.y = 1;
-    attr[1].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
-}
-
-// Bounded barrier over every CTA of a cooperative launch: a generation counter that the last
-// CTA to arrive advances.  Writes made before the barrier are visible after it to loads that
-// bypass L1 (__ldcg).  Returns false (and reports EP_ERR_TIMEOUT) if the wait gave up.
-__device__ __forceinline__ bool grid_barrier(uint32_t* count, uint32_t* generation, uint32_t n_blocks,
-                                             int32_t* status) {
-    __shared__ int32_t s_ok;
-    __threadfence();
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        int32_t ok = 1;
-        const uint32_t gen = *reinterpret_cast<volatile uint32_t*>(generation);
-        __threadfence();
-        if (atomicAdd(count, 1u) == n_blocks - 1) {
-            atomicExch(count, 0u);
-            __threadfence();
-            atomicAdd(generation, 1u);
-        } else {
-            ok = 0;
-            for (uint32_t it = 0; it < kMaxWaitIterations; ++it)
-                if (*reinterpret_cast<volatile uint32_t*>(generation) != gen) {
-                    ok = 1;
-                    break;
-                }
-            if (!ok) report(status, EP_ERR_TIMEOUT);
-        }
-        __threadfence();
-        s_ok = ok;
-    }
-    __syncthreads();
-    return s_ok != 0;
-}
-
 }  // namespace ep

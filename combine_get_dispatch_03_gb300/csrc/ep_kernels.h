@@ -20,7 +20,6 @@ struct LaunchPlan {
     int bulk_stages[3] = {0, 0, 0};      // bulk-copy dispatch: stages per CTA (0 = not usable)
     unsigned bulk_smem[3] = {0, 0, 0};   // its dynamic shared memory
     int bulk_resident[3] = {1, 1, 1};    // its CTAs resident on the GPU at once
-    bool layout_notify_fused = false;    // layout + notify fit one cooperative launch
 };
 
 constexpr int kLayoutThreads = 1024;
@@ -35,8 +34,9 @@ enum DispatchMode { kModeBf16 = 0, kModeCastFp8 = 1, kModeFp8In = 2 };
 
 cudaError_t plan_launches(LaunchPlan* plan, int device, int num_experts);
 
-cudaError_t launch_get_dispatch_layout(const int64_t* topk_idx, int R, int T, int K, int E,
-                                       int32_t* tpr, int32_t* tprdma, int32_t* tpe, uint8_t* itr,
+// rank_mask: int32 [R] (nonzero = masked) or NULL; slots that start or end on a masked rank are left out.
+cudaError_t launch_get_dispatch_layout(const int64_t* topk_idx, const int32_t* rank_mask, int R, int T, int K,
+                                       int E, int32_t* tpr, int32_t* tprdma, int32_t* tpe, uint8_t* itr,
                                        int32_t* status, cudaStream_t stream);
 
 cudaError_t launch_dispatch_notify(int R, int T, int E, int C, int A, int64_t cap, const int32_t* tpr,
@@ -46,29 +46,18 @@ cudaError_t launch_dispatch_notify(int R, int T, int E, int C, int A, int64_t ca
                                    int32_t* rdma_channel_prefix, int32_t* recv_rdma_rank_prefix, int32_t* status,
                                    cudaStream_t stream);
 
-// Whether the layout + notify grid (R + 1 clusters of 8 CTAs) fits on the device at once, as
-// a cooperative launch needs.
-bool layout_notify_fits(int R, int E);
-
-// Layout and the dispatch record in one pass (a decoupled look-back scan over token tiles) when
-// the ranks do not form whole nodes and layout_scan_fits(T) (1 <= T <= 32 tiles of 512 tokens).
-// scratch: layout_scan_scratch_words(R, E, maxT) words of device memory, zero before the first
-// launch; launches sharing it must be ordered.
-bool layout_scan_fits(int T);
+// Layout and the dispatch record in one pass (a decoupled look-back scan over token tiles of 512),
+// for T >= 1; with rdma_channel_prefix and recv_rdma_rank_prefix (whole nodes of 8, R > 8) the
+// node-level record as well.  scratch: layout_scan_scratch_words(R, E, maxT) words of device
+// memory, zero before the first launch; launches sharing it must be ordered.
 size_t layout_scan_scratch_words(int R, int E, int max_tokens);
-cudaError_t launch_layout_scan(const int64_t* topk_idx, int R, int T, int K, int E, int C, int A, int64_t cap,
-                               int32_t* tpr, int32_t* tprdma, int32_t* tpe, uint8_t* itr, int32_t* rank_prefix,
-                               int32_t* channel_prefix, int32_t* recv_channel_prefix, int32_t* num_recv,
-                               int32_t* send_head, int32_t* recv_src_idx, int32_t* num_recv_per_expert,
-                               uint32_t* scratch, int32_t* status, cudaStream_t stream);
-
-// get_dispatch_layout and dispatch_notify in one cooperative launch (layout_notify_fits).
-cudaError_t launch_layout_notify(const int64_t* topk_idx, int R, int T, int K, int E, int C, int A, int64_t cap,
-                                 int32_t* tpr, int32_t* tprdma, int32_t* tpe, uint8_t* itr, int32_t* rank_prefix,
-                                 int32_t* channel_prefix, int32_t* recv_channel_prefix, int32_t* num_recv,
-                                 int32_t* send_head, int32_t* recv_src_idx, int32_t* num_recv_per_expert,
-                                 int32_t* rdma_channel_prefix, int32_t* recv_rdma_rank_prefix, uint32_t* barrier,
-                                 int32_t* status, cudaStream_t stream);
+cudaError_t launch_layout_scan(const int64_t* topk_idx, const int32_t* rank_mask, int R, int T, int K, int E, int C,
+                               int A, int64_t cap, int32_t* tpr, int32_t* tprdma, int32_t* tpe, uint8_t* itr,
+                               int32_t* rank_prefix, int32_t* channel_prefix, int32_t* recv_channel_prefix,
+                               int32_t* num_recv, int32_t* send_head, int32_t* recv_src_idx,
+                               int32_t* num_recv_per_expert, int32_t* rdma_channel_prefix,
+                               int32_t* recv_rdma_rank_prefix, uint32_t* scratch, int32_t* status,
+                               cudaStream_t stream);
 
 cudaError_t launch_dispatch(const LaunchPlan& plan, int mode, int R, int T, int H, int K, int EL, int64_t cap,
                             const void* x, const float* x_scales, const int64_t* topk_idx,

@@ -15,11 +15,16 @@
 // RDMA team is the ranks with the same GPU index ("DeepEP Normal vs
 // Low-Latency 双模式深度分析").
 //
-// Both kernels give each source rank one thread-block cluster of kClusterCtas
-// CTAs; CTA q of the cluster owns the q-th contiguous slice of that rank's
-// tokens.  Partial counts are exchanged through distributed shared memory
-// after a cluster barrier, so a kernel is one launch with no global scratch,
-// no atomics on global memory and no waiting on other launches.
+// The two separate kernels (ep_get_dispatch_layout, ep_notify_dispatch) give
+// each source rank one thread-block cluster of kClusterCtas CTAs; CTA q of the
+// cluster owns the q-th contiguous slice of that rank's tokens.  Partial
+// counts are exchanged through distributed shared memory after a cluster
+// barrier, so a kernel is one launch with no global scratch, no atomics on
+// global memory and no waiting on other launches.  ep_layout_notify runs both
+// steps as one pass of a decoupled look-back scan (layout_scan_kernel, below).
+// With ranks masked in the handle's mask buffer, the layout leaves out every
+// slot that starts or ends on a masked rank (the mask buffer of the
+// low-latency receive excerpt of the same page, applied to the normal path).
 #include <cooperative_groups.h>
 
 #include "ep_common.cuh"
@@ -86,18 +91,21 @@ __device__ __forceinline__ void cluster_slice(int T, int q, int& lo, int& hi) {
 }
 
 // Layout of source s by CTA q of its cluster: the slice's tokens are marked in is_token_in_rank,
-// counted per expert, per destination rank and per node.  Leaves the slice's hits per rank in
+// counted per expert, per destination rank and per node.  Slots that start or end on a rank of
+// `rmask` (bit r: rank r masked) are left out as if they were -1.  Leaves the slice's hits per rank in
 // s_cnt[0, R) and per node in s_cnt[R, R + ceil(R/8)) -- read by the rest of the cluster -- and
 // writes the source's totals (tpr, tprdma when given, tpe).  Ends with a cluster barrier.
 __device__ __forceinline__ void layout_source(const cg::cluster_group& cluster, int s, int q,
-                                              const int64_t* __restrict__ topk_idx, int R, int T, int K, int E,
-                                              int EL, int32_t* __restrict__ tpr, int32_t* __restrict__ tprdma,
-                                              int32_t* __restrict__ tpe, uint8_t* __restrict__ itr,
-                                              int32_t* status, int32_t* s_expert, int32_t* s_cnt) {
+                                              const int64_t* __restrict__ topk_idx, uint32_t rmask, int R, int T,
+                                              int K, int E, int EL, int32_t* __restrict__ tpr,
+                                              int32_t* __restrict__ tprdma, int32_t* __restrict__ tpe,
+                                              uint8_t* __restrict__ itr, int32_t* status, int32_t* s_expert,
+                                              int32_t* s_cnt) {
     __shared__ uint32_t s_mask[kLayoutRound];
     const int tid = threadIdx.x;
     const int lane = lane_id();
     const int NN = (R + kRanksPerNode - 1) / kRanksPerNode;
+    const bool src_masked = (rmask >> s) & 1u;
     for (int i = tid; i < E; i += kLayoutThreads) s_expert[i] = 0;
     if (tid < kMaxColumns) s_cnt[tid] = 0;
 
@@ -129,8 +137,10 @@ __device__ __forceinline__ void layout_source(const cg::cluster_group& cluster, 
                     report(status, EP_ERR_BAD_EXPERT);
                     continue;
                 }
+                const int d = static_cast<int>(e) / EL;
+                if (src_masked || ((rmask >> d) & 1u)) continue;  // a masked rank neither sends nor receives
                 atomicAdd(&s_expert[e], 1);
-                atomicOr(&s_mask[static_cast<int>(i / K) - round], 1u << (static_cast<int>(e) / EL));
+                atomicOr(&s_mask[static_cast<int>(i / K) - round], 1u << d);
             }
         }
         __syncthreads();
@@ -173,14 +183,16 @@ __device__ __forceinline__ void layout_source(const cg::cluster_group& cluster, 
 
 // grid (kClusterCtas, R), cluster (kClusterCtas, 1, 1).
 __global__ void __launch_bounds__(kLayoutThreads)
-    get_dispatch_layout_kernel(const int64_t* __restrict__ topk_idx, int R, int T, int K, int E, int EL,
-                               int32_t* __restrict__ tpr, int32_t* __restrict__ tprdma,
+    get_dispatch_layout_kernel(const int64_t* __restrict__ topk_idx, const int32_t* __restrict__ rank_mask, int R,
+                               int T, int K, int E, int EL, int32_t* __restrict__ tpr, int32_t* __restrict__ tprdma,
                                int32_t* __restrict__ tpe, uint8_t* __restrict__ itr, int32_t* status) {
     pdl_enter();
     extern __shared__ int32_t s_expert[];  // [E]
     __shared__ int32_t s_cnt[kMaxColumns];
     cg::cluster_group cluster = cg::this_cluster();
-    layout_source(cluster, blockIdx.y, static_cast<int>(cluster.block_rank()), topk_idx, R, T, K, E, EL, tpr,
+    const int lane = lane_id();
+    const uint32_t rmask = __ballot_sync(kFullMask, rank_mask != nullptr && lane < R && __ldg(rank_mask + lane) != 0);
+    layout_source(cluster, blockIdx.y, static_cast<int>(cluster.block_rank()), topk_idx, rmask, R, T, K, E, EL, tpr,
                   tprdma, tpe, itr, status, s_expert, s_cnt);
 }
 
@@ -402,56 +414,31 @@ __global__ void __launch_bounds__(kMaxRanks * kMaxNodes)
     recv_rdma_rank_prefix[i] = acc;
 }
 
-// Layout and notify in one cooperative launch: grid (kClusterCtas, R + 1), cluster
-// (kClusterCtas, 1, 1).  The source clusters compute the layout (and keep each slice's
-// hits per column in shared memory, which is what the notify's first pass would count),
-// every CTA meets at one grid barrier -- the record needs every source's counts -- and then
-// the source clusters write their rows while cluster R writes the summary.
-__global__ void __launch_bounds__(kLayoutThreads)
-    layout_notify_kernel(const int64_t* __restrict__ topk_idx, int R, int NN, int T, int K, int E, int C, int A,
-                         int64_t cap, int32_t* __restrict__ tpr, int32_t* __restrict__ tprdma,
-                         int32_t* __restrict__ tpe, uint8_t* __restrict__ itr, int32_t* __restrict__ rank_prefix,
-                         int32_t* __restrict__ channel_prefix, int32_t* __restrict__ recv_channel_prefix,
-                         int32_t* __restrict__ rdma_channel_prefix, int32_t* __restrict__ num_recv,
-                         int32_t* __restrict__ send_head, int32_t* __restrict__ recv_src_idx,
-                         int32_t* __restrict__ num_recv_per_expert, uint32_t* barrier, int32_t* status) {
-    static_assert(kLayoutThreads == kNotifyThreads, "one block size for both phases");
-    pdl_enter();
-    extern __shared__ int32_t s_expert[];  // [E]
-    __shared__ int32_t s_cnt[kMaxColumns];
-    cg::cluster_group cluster = cg::this_cluster();
-    const int q = static_cast<int>(cluster.block_rank());
-    const int s = blockIdx.y;
-    if (s < R)
-        layout_source(cluster, s, q, topk_idx, R, T, K, E, E / R, tpr, tprdma, tpe, itr, status, s_expert, s_cnt);
-    if (!grid_barrier(barrier, barrier + 1, gridDim.x * gridDim.y, status)) return;
-    if (s == R) {
-        notify_summary(q, R, E, A, cap, tpr, tpe, rank_prefix, num_recv, num_recv_per_expert, status);
-        return;
-    }
-    notify_source(cluster, s, q, R, NN, T, C, cap, tpr, itr, channel_prefix, recv_channel_prefix,
-                  rdma_channel_prefix, send_head, recv_src_idx, status, s_cnt);
-}
-
 // ---------------------------------------------------------------------------
-// Layout and record in one pass (ranks that do not form whole nodes): a single decoupled
-// look-back scan.  The receive rows of every destination rank follow the (source, token) order,
-// so one scan over the tokens of all sources, in that order, with one counter per destination
-// rank, gives every row.  CTAs take tiles of kScanTile tokens of one source by ticket, in
-// (source, token) order -- a CTA only ever waits for tiles whose CTAs started before it, so the
-// waits end -- and for its tile:
-//   1. marks is_token_in_rank, counts the slots per expert (and the tokens per node) and, per
-//      destination rank, the hits of each warp (ballots), then publishes the tile's per-rank
-//      totals with state "aggregate";
+// Layout and record in one pass: a single decoupled look-back scan.  The receive rows of every
+// destination rank follow the (source, token) order, so one scan over the tokens of all sources,
+// in that order, with one counter per destination rank, gives every row.  CTAs take tiles of
+// kScanTile tokens of one source by ticket, in (source, token) order -- a CTA only ever waits for
+// tiles whose CTAs started before it, so the waits end -- and for its tile:
+//   1. marks is_token_in_rank, counts the slots per expert and, per column -- R destination ranks,
+//      then ceil(R/8) nodes of 8 ranks -- the hits of each warp (ballots), then publishes the
+//      tile's per-column totals with state "aggregate";
 //   2. looks back over the earlier tiles, adding aggregates until one publishes state
-//      "inclusive", then publishes its own inclusive prefix;
+//      "inclusive", then publishes its own inclusive prefixes: over all earlier tiles (rank
+//      columns: the rows before the tile) and over this source's earlier tiles (every column:
+//      the channel prefix matrices).  A tile reaches "inclusive" only after every earlier tile
+//      published its aggregate, so the nearest inclusive tile ends both sums, however many
+//      tiles a source has;
 //   3. writes each token's send_head row (the exclusive prefix + the hits before the token in
-//      the tile), recv_src_idx and the channel prefix entries at channel starts.
+//      the tile), recv_src_idx and the channel prefix entries (rank and, with whole nodes, node
+//      columns) at channel starts.
 // The last tile of a source writes the source's totals; the last CTA to finish writes the
-// summary (num_recv, aligned per-expert receive counts) and resets the tickets for the next
-// launch.  Every wait is bounded (EP_ERR_TIMEOUT).  Published states carry the launch's epoch
-// (a counter in the scratch that each launch advances), so stale states of an earlier launch
-// never match.
+// summary (num_recv, aligned per-expert receive counts and, with whole nodes, the node receive
+// prefix) and resets the tickets for the next launch.  Every wait is bounded (EP_ERR_TIMEOUT).
+// Published states carry the launch's epoch (a counter in the scratch that each launch
+// advances), so stale states of an earlier launch never match and CUDA-graph replays need no
+// reset.  With a rank mask, slots that start or end on a masked rank are left out as if they
+// were -1 (a masked rank neither sends nor receives).
 constexpr int kScanTile = 512;   // tokens per tile = threads per CTA (1024 measured 0.3 % slower on the step)
 constexpr int kScanWarps = kScanTile / kWarpSize;
 static_assert(kScanWarps <= kWarpSize, "the column scan gives one lane per warp");
@@ -467,11 +454,24 @@ __device__ __forceinline__ void st_release_u32(uint32_t* p, uint32_t v) {
     asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
-// Scratch words: [0] next ticket, [1] finished tiles, [2] epoch, [3] unused; then per tile its
-// state word, its per-rank aggregate [R] and inclusive prefix [R], and its expert histogram [E]
-// followed by its per-node token counts [ceil(R/8)].
-__host__ __device__ __forceinline__ int64_t scan_tile_words(int R, int E) {
-    return 1 + 2 * static_cast<int64_t>(R) + E + (R + kRanksPerNode - 1) / kRanksPerNode;
+// Per-tile words of the scratch, NC = R + ceil(R/8) columns: the state word, then the tile's
+// per-column hits [NC], its inclusive prefix over all earlier tiles for the rank columns [R], its
+// inclusive prefix over this source's tiles for every column [NC], and its expert histogram [E].
+// The scratch starts with 4 words: [0] next ticket, [1] finished tiles, [2] epoch, [3] unused.
+struct ScanWords {
+    int NC, agg, incl, sincl, hist;
+    int64_t per_tile;
+};
+
+__host__ __device__ __forceinline__ ScanWords scan_words(int R, int E) {
+    ScanWords w;
+    w.NC = R + (R + kRanksPerNode - 1) / kRanksPerNode;
+    w.agg = 1;
+    w.incl = w.agg + w.NC;
+    w.sincl = w.incl + R;
+    w.hist = w.sincl + w.NC;
+    w.per_tile = w.hist + E;
+    return w;
 }
 
 // All lanes of the calling warp wait (bounded) until tile k published at least `state` in this
@@ -484,21 +484,29 @@ __device__ __forceinline__ uint32_t scan_wait(const uint32_t* word, uint32_t epo
     return 0u;
 }
 
+// Bit r set: rank r is masked (rank_mask may be NULL).  Every lane of the calling warp gets it.
+__device__ __forceinline__ uint32_t masked_ranks(const int32_t* rank_mask, int R) {
+    const int lane = lane_id();
+    return __ballot_sync(kFullMask, rank_mask != nullptr && lane < R && __ldg(rank_mask + lane) != 0);
+}
+
 __global__ void __launch_bounds__(kScanTile)
-    layout_scan_kernel(const int64_t* __restrict__ topk_idx, int R, int T, int K, int E, int C, int A, int64_t cap,
-                       int32_t* __restrict__ tpr, int32_t* __restrict__ tprdma, int32_t* __restrict__ tpe,
-                       uint8_t* __restrict__ itr, int32_t* __restrict__ rank_prefix,
-                       int32_t* __restrict__ channel_prefix, int32_t* __restrict__ recv_channel_prefix,
-                       int32_t* __restrict__ num_recv, int32_t* __restrict__ send_head,
-                       int32_t* __restrict__ recv_src_idx, int32_t* __restrict__ num_recv_per_expert,
-                       uint32_t* __restrict__ scratch, int32_t* status) {
+    layout_scan_kernel(const int64_t* __restrict__ topk_idx, const int32_t* __restrict__ rank_mask, int R, int T,
+                       int K, int E, int C, int A, int64_t cap, int32_t* __restrict__ tpr,
+                       int32_t* __restrict__ tprdma, int32_t* __restrict__ tpe, uint8_t* __restrict__ itr,
+                       int32_t* __restrict__ rank_prefix, int32_t* __restrict__ channel_prefix,
+                       int32_t* __restrict__ recv_channel_prefix, int32_t* __restrict__ num_recv,
+                       int32_t* __restrict__ send_head, int32_t* __restrict__ recv_src_idx,
+                       int32_t* __restrict__ num_recv_per_expert, int32_t* __restrict__ rdma_channel_prefix,
+                       int32_t* __restrict__ recv_rdma_rank_prefix, uint32_t* __restrict__ scratch,
+                       int32_t* status) {
     pdl_enter();
-    extern __shared__ int32_t s_hist[];                  // [E + NN]: slots per expert, then tokens per node
-    __shared__ uint32_t s_mask[kScanTile];               // destination ranks of each token of the tile
-    __shared__ int32_t s_wpre[kMaxRanks][kScanWarps];    // per-warp hits -> exclusive prefix in the tile
-    __shared__ int32_t s_agg[kMaxRanks];                 // the tile's hits per rank
-    __shared__ int32_t s_excl[kMaxRanks];                // hits of every earlier tile (rows before the tile)
-    __shared__ int32_t s_ws[kMaxRanks];                  // hits of this source's earlier tiles
+    extern __shared__ int32_t s_hist[];                    // [E]: slots per expert
+    __shared__ uint32_t s_mask[kScanTile];                 // destination ranks of each token of the tile
+    __shared__ int32_t s_wpre[kMaxColumns][kScanWarps];    // per-warp hits -> exclusive prefix in the tile
+    __shared__ int32_t s_agg[kMaxColumns];                 // the tile's hits per column
+    __shared__ int32_t s_excl[kMaxRanks];                  // hits of every earlier tile (rows before the tile)
+    __shared__ int32_t s_ws[kMaxColumns];                  // hits of this source's earlier tiles
     __shared__ int32_t s_tile, s_ok, s_last;
     __shared__ uint32_t s_epoch;
     const int tid = threadIdx.x;
@@ -506,9 +514,10 @@ __global__ void __launch_bounds__(kScanTile)
     const int warp = tid / kWarpSize;
     const int EL = E / R;
     const int NN = (R + kRanksPerNode - 1) / kRanksPerNode;
+    const ScanWords W = scan_words(R, E);
+    const int NC = W.NC;
     const int tiles_per_src = (T + kScanTile - 1) / kScanTile;
     const int n_tiles = R * tiles_per_src;
-    const int64_t words = scan_tile_words(R, E);
     uint32_t* tiles = scratch + 4;
 
     if (tid == 0) {
@@ -516,8 +525,9 @@ __global__ void __launch_bounds__(kScanTile)
         s_epoch = ld_acquire_u32(scratch + 2);
         s_ok = 1;
     }
-    for (int i = tid; i < E + NN; i += kScanTile) s_hist[i] = 0;
+    for (int i = tid; i < E; i += kScanTile) s_hist[i] = 0;
     s_mask[tid] = 0u;
+    const uint32_t rmask = masked_ranks(rank_mask, R);
     __syncthreads();
     const int tile = s_tile;
     const uint32_t epoch = s_epoch;
@@ -526,7 +536,8 @@ __global__ void __launch_bounds__(kScanTile)
     const int j = tile - s * tiles_per_src;
     const int t0 = j * kScanTile;
     const int len = min(kScanTile, T - t0);
-    uint32_t* my = tiles + static_cast<int64_t>(tile) * words;
+    uint32_t* my = tiles + static_cast<int64_t>(tile) * W.per_tile;
+    const bool src_masked = (rmask >> s) & 1u;
 
     // 1. the tile's layout: one flat walk over its top-k entries, several loads in flight
     const int64_t* idx_t = topk_idx + (static_cast<int64_t>(s) * T + t0) * K;
@@ -547,8 +558,10 @@ __global__ void __launch_bounds__(kScanTile)
                 report(status, EP_ERR_BAD_EXPERT);
                 continue;
             }
+            const int d = static_cast<int>(e) / EL;
+            if (src_masked || ((rmask >> d) & 1u)) continue;  // a masked rank neither sends nor receives
             atomicAdd(&s_hist[e], 1);
-            atomicOr(&s_mask[static_cast<int>(i / K)], 1u << (static_cast<int>(e) / EL));
+            atomicOr(&s_mask[static_cast<int>(i / K)], 1u << d);
         }
     }
     __syncthreads();
@@ -556,74 +569,78 @@ __global__ void __launch_bounds__(kScanTile)
     const int t = t0 + tid;
     const uint32_t m = live ? s_mask[tid] : 0u;
     if (live) store_rank_mask(itr + (static_cast<int64_t>(s) * T + t) * R, R, m);
-    for (int n = 0; n < NN; ++n) {
-        const unsigned b = __ballot_sync(kFullMask, column_bit(m, R + n, R));
-        if (lane == 0 && b) atomicAdd(&s_hist[E + n], __popc(b));
-    }
-    for (int r = 0; r < R; ++r) {
-        const unsigned b = __ballot_sync(kFullMask, (m >> r) & 1u);
-        if (lane == 0) s_wpre[r][warp] = __popc(b);
+    for (int c = 0; c < NC; ++c) {
+        const unsigned b = __ballot_sync(kFullMask, column_bit(m, c, R));
+        if (lane == 0) s_wpre[c][warp] = __popc(b);
     }
     __syncthreads();
-    for (int r = warp; r < R; r += kScanWarps) {  // exclusive prefix of rank r's hits over the warps of the tile
-        const int32_t v = lane < kScanWarps ? s_wpre[r][lane] : 0;
+    for (int c = warp; c < NC; c += kScanWarps) {  // exclusive prefix of column c's hits over the warps of the tile
+        const int32_t v = lane < kScanWarps ? s_wpre[c][lane] : 0;
         int32_t incl = v;
 #pragma unroll
         for (int off = 1; off < kWarpSize; off <<= 1) {
             const int32_t o = __shfl_up_sync(kFullMask, incl, off);
             if (lane >= off) incl += o;
         }
-        if (lane < kScanWarps) s_wpre[r][lane] = incl - v;
-        if (lane == kWarpSize - 1) s_agg[r] = incl;
+        if (lane < kScanWarps) s_wpre[c][lane] = incl - v;
+        if (lane == kWarpSize - 1) s_agg[c] = incl;
     }
     __syncthreads();
     // publish the aggregate (and the histogram the source's last tile sums)
-    if (tid < R) my[1 + tid] = static_cast<uint32_t>(s_agg[tid]);
-    for (int i = tid; i < E + NN; i += kScanTile) my[1 + 2 * R + i] = static_cast<uint32_t>(s_hist[i]);
+    if (tid < NC) my[W.agg + tid] = static_cast<uint32_t>(s_agg[tid]);
+    for (int i = tid; i < E; i += kScanTile) my[W.hist + i] = static_cast<uint32_t>(s_hist[i]);
     __threadfence();
     __syncthreads();
     if (tid == 0) st_release_u32(my, tag | kScanAggregate);
 
-    // 2. look back: warp r sums rank r's hits of the earlier tiles.  Lane i reads tile
-    //    (tile - 1 - i) of a window of 32, so one round of loads covers the window; the sum stops
-    //    at the nearest tile that published its inclusive prefix.  The same loads give the hits
-    //    of this source's earlier tiles (j <= 32 of them: T <= 32 tiles, checked at launch).
-    for (int r = warp; r < R; r += kScanWarps) {
+    // 2. look back: warp c sums column c's hits of the earlier tiles.  Lane i reads tile
+    //    (tile - 1 - i) of a window of 32, so one round of loads covers the window; the sums stop
+    //    at the nearest tile that published its inclusive prefixes -- for a rank column the prefix
+    //    over all tiles, and for every column the prefix over its own source's tiles.
+    for (int c = warp; c < NC; c += kScanWarps) {
+        const bool rank_col = c < R;
         int32_t excl = 0, ws = 0;
         bool ok = true;
         for (int k0 = tile - 1; k0 >= 0; k0 -= kWarpSize) {
             const int k = k0 - lane;
             uint32_t f = 1u;
-            int32_t agg = 0, inc = 0;
+            int32_t agg = 0, inc = 0, sinc = 0;
             if (k >= 0) {
-                const uint32_t* w = tiles + static_cast<int64_t>(k) * words;
+                const uint32_t* w = tiles + static_cast<int64_t>(k) * W.per_tile;
                 f = scan_wait(w, epoch, kScanAggregate);
                 if (f != 0u) {
-                    agg = static_cast<int32_t>(__ldcg(w + 1 + r));
-                    if ((f & 3u) == kScanInclusive) inc = static_cast<int32_t>(__ldcg(w + 1 + R + r));
+                    agg = static_cast<int32_t>(__ldcg(w + W.agg + c));
+                    if ((f & 3u) == kScanInclusive) {
+                        if (rank_col) inc = static_cast<int32_t>(__ldcg(w + W.incl + c));
+                        sinc = static_cast<int32_t>(__ldcg(w + W.sincl + c));
+                    }
                 }
             }
             if (__any_sync(kFullMask, f == 0u)) {
                 ok = false;
                 break;
             }
-            int32_t same = (k >= 0 && k >= tile - j) ? agg : 0;
+            const bool same = k >= 0 && k >= tile - j;  // tile k is an earlier tile of this source
             const unsigned inclusive = __ballot_sync(kFullMask, k >= 0 && (f & 3u) == kScanInclusive);
             const int first = inclusive ? __ffs(inclusive) - 1 : kWarpSize;
             int32_t part = lane < first ? agg : (lane == first ? inc : 0);
+            int32_t spart = same ? (lane < first ? agg : (lane == first ? sinc : 0)) : 0;
 #pragma unroll
             for (int off = kWarpSize / 2; off > 0; off >>= 1) {
                 part += __shfl_xor_sync(kFullMask, part, off);
-                same += __shfl_xor_sync(kFullMask, same, off);
+                spart += __shfl_xor_sync(kFullMask, spart, off);
             }
             excl += part;
-            ws += same;
+            ws += spart;
             if (inclusive) break;
         }
         if (lane == 0) {
-            s_excl[r] = excl;
-            s_ws[r] = ws;
-            my[1 + R + r] = static_cast<uint32_t>(excl + s_agg[r]);
+            if (rank_col) {
+                s_excl[c] = excl;
+                my[W.incl + c] = static_cast<uint32_t>(excl + s_agg[c]);
+            }
+            s_ws[c] = ws;
+            my[W.sincl + c] = static_cast<uint32_t>(ws + s_agg[c]);
             if (!ok) s_ok = 0;
         }
     }
@@ -638,6 +655,7 @@ __global__ void __launch_bounds__(kScanTile)
     if (s_ok) {
         const int chunk = max(1, (T + C - 1) / C);
         const unsigned lt = lanemask_lt();
+        const bool channel_start = live && (t % chunk) == 0;
         int32_t rows[kMaxRanks];
 #pragma unroll
         for (int r = 0; r < kMaxRanks; ++r) {
@@ -647,10 +665,18 @@ __global__ void __launch_bounds__(kScanTile)
             const int32_t before = s_wpre[r][warp] + __popc(b & lt);  // hits of (s -> r) in the tile before t
             const int32_t row = s_excl[r] + before;
             rows[r] = bit ? row : -1;
-            if (live && (t % chunk) == 0) {
+            if (channel_start) {
                 const int c = t / chunk;
                 recv_channel_prefix[(static_cast<int64_t>(r) * R + s) * C + c] = row;
                 if (c > 0) channel_prefix[(static_cast<int64_t>(s) * R + r) * C + c - 1] = s_ws[r] + before;
+            }
+        }
+        if (rdma_channel_prefix != nullptr) {  // node columns: tokens of s that reach node n, before t
+            for (int n = 0; n < NN; ++n) {
+                const unsigned b = __ballot_sync(kFullMask, column_bit(m, R + n, R));
+                if (channel_start && t > 0)
+                    rdma_channel_prefix[(static_cast<int64_t>(s) * NN + n) * C + t / chunk - 1] =
+                        s_ws[R + n] + s_wpre[R + n][warp] + __popc(b & lt);
             }
         }
         if (live) {
@@ -688,13 +714,22 @@ __global__ void __launch_bounds__(kScanTile)
                     if (end == T) channel_prefix[(static_cast<int64_t>(s) * R + r) * C + c] = total;
                     if (start == T) recv_channel_prefix[(static_cast<int64_t>(r) * R + s) * C + c] = base + total;
                 }
+            } else if (tid < NC) {
+                const int n = tid - R;
+                const int32_t total = s_ws[tid] + s_agg[tid];
+                if (tprdma != nullptr) tprdma[s * NN + n] = total;
+                if (rdma_channel_prefix != nullptr)
+                    for (int c = 0; c < C; ++c)
+                        if (min(static_cast<int64_t>(T), static_cast<int64_t>(c + 1) * chunk) == T)
+                            rdma_channel_prefix[(static_cast<int64_t>(s) * NN + n) * C + c] = total;
             }
-            for (int i = tid; i < E + NN; i += kScanTile) {
+            // every earlier tile of the source has published its histogram: the look-back above
+            // reached an inclusive tile, and a tile is inclusive only after all earlier ones
+            for (int i = tid; i < E; i += kScanTile) {
                 int32_t sum = s_hist[i];
                 for (int k = tile - j; k < tile; ++k)
-                    sum += static_cast<int32_t>(__ldcg(tiles + static_cast<int64_t>(k) * words + 1 + 2 * R + i));
-                if (i < E) tpe[static_cast<int64_t>(s) * E + i] = sum;
-                else if (tprdma != nullptr) tprdma[s * NN + (i - E)] = sum;
+                    sum += static_cast<int32_t>(__ldcg(tiles + static_cast<int64_t>(k) * W.per_tile + W.hist + i));
+                tpe[static_cast<int64_t>(s) * E + i] = sum;
             }
         }
     }
@@ -716,6 +751,15 @@ __global__ void __launch_bounds__(kScanTile)
         for (int sp = 0; sp < R; ++sp) sum += __ldcg(tpe + static_cast<int64_t>(sp) * E + e);
         num_recv_per_expert[e] = static_cast<int32_t>(((sum + A - 1) / A) * A);
     }
+    if (recv_rdma_rank_prefix != nullptr && tid < R * NN) {
+        // rank (n, l) receives over RDMA the tokens of the sources (m, l) that reach node n
+        const int r = tid / NN, mm = tid % NN;
+        const int n = r / kRanksPerNode, l = r % kRanksPerNode;
+        int32_t acc = 0;
+        for (int mp = 0; mp <= mm; ++mp)
+            acc += __ldcg(rdma_channel_prefix + (static_cast<int64_t>(kRanksPerNode * mp + l) * NN + n) * C + C - 1);
+        recv_rdma_rank_prefix[tid] = acc;
+    }
     if (tid == 0) {
         scratch[0] = 0u;
         scratch[1] = 0u;
@@ -726,12 +770,12 @@ __global__ void __launch_bounds__(kScanTile)
 
 }  // namespace
 
-cudaError_t launch_get_dispatch_layout(const int64_t* topk_idx, int R, int T, int K, int E, int32_t* tpr,
-                                       int32_t* tprdma, int32_t* tpe, uint8_t* itr, int32_t* status,
+cudaError_t launch_get_dispatch_layout(const int64_t* topk_idx, const int32_t* rank_mask, int R, int T, int K, int E,
+                                       int32_t* tpr, int32_t* tprdma, int32_t* tpe, uint8_t* itr, int32_t* status,
                                        cudaStream_t stream) {
     return launch_kernel(get_dispatch_layout_kernel, dim3(kClusterCtas, R, 1), dim3(kLayoutThreads, 1, 1),
-                         sizeof(int32_t) * static_cast<size_t>(E), stream, kClusterCtas, topk_idx, R, T, K, E, E / R,
-                         tpr, tprdma, tpe, itr, status);
+                         sizeof(int32_t) * static_cast<size_t>(E), stream, kClusterCtas, topk_idx, rank_mask, R, T, K,
+                         E, E / R, tpr, tprdma, tpe, itr, status);
 }
 
 cudaError_t launch_dispatch_notify(int R, int T, int E, int C, int A, int64_t cap, const int32_t* tpr,
@@ -752,63 +796,29 @@ cudaError_t launch_dispatch_notify(int R, int T, int E, int C, int A, int64_t ca
                          static_cast<const int32_t*>(rdma_channel_prefix), recv_rdma_rank_prefix);
 }
 
-bool layout_scan_fits(int T) { return T >= 1 && (T + kScanTile - 1) / kScanTile <= kWarpSize; }
-
 size_t layout_scan_scratch_words(int R, int E, int max_tokens) {
     const int64_t tiles = static_cast<int64_t>(R) * ((max_tokens + kScanTile - 1) / kScanTile);
-    return static_cast<size_t>(4 + tiles * scan_tile_words(R, E));
+    return static_cast<size_t>(4 + tiles * scan_words(R, E).per_tile);
 }
 
-cudaError_t launch_layout_scan(const int64_t* topk_idx, int R, int T, int K, int E, int C, int A, int64_t cap,
-                               int32_t* tpr, int32_t* tprdma, int32_t* tpe, uint8_t* itr, int32_t* rank_prefix,
-                               int32_t* channel_prefix, int32_t* recv_channel_prefix, int32_t* num_recv,
-                               int32_t* send_head, int32_t* recv_src_idx, int32_t* num_recv_per_expert,
-                               uint32_t* scratch, int32_t* status, cudaStream_t stream) {
-    if (!layout_scan_fits(T)) return cudaErrorInvalidValue;
-    const int n_tiles = R * ((T + kScanTile - 1) / kScanTile);
-    const size_t smem = sizeof(int32_t) * static_cast<size_t>(E + (R + kRanksPerNode - 1) / kRanksPerNode);
-    return launch_kernel(layout_scan_kernel, dim3(n_tiles), dim3(kScanTile), smem, stream, 1, topk_idx, R, T, K, E,
-                         C, A, cap, tpr, tprdma, tpe, itr, rank_prefix, channel_prefix, recv_channel_prefix, num_recv,
-                         send_head, recv_src_idx, num_recv_per_expert, scratch, status);
-}
-
-bool layout_notify_fits(int R, int E) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(kClusterCtas, R + 1, 1);
-    cfg.blockDim = dim3(kLayoutThreads, 1, 1);
-    cfg.dynamicSmemBytes = sizeof(int32_t) * static_cast<size_t>(E);
-    cudaLaunchAttribute attr;
-    attr.id = cudaLaunchAttributeClusterDimension;
-    attr.val.clusterDim.x = kClusterCtas;
-    attr.val.clusterDim.y = 1;
-    attr.val.clusterDim.z = 1;
-    cfg.attrs = &attr;
-    cfg.numAttrs = 1;
-    int clusters = 0;
-    if (cudaOccupancyMaxActiveClusters(&clusters, layout_notify_kernel, &cfg) != cudaSuccess) {
-        cudaGetLastError();
-        return false;
-    }
-    return clusters >= R + 1;
-}
-
-cudaError_t launch_layout_notify(const int64_t* topk_idx, int R, int T, int K, int E, int C, int A, int64_t cap,
-                                 int32_t* tpr, int32_t* tprdma, int32_t* tpe, uint8_t* itr, int32_t* rank_prefix,
-                                 int32_t* channel_prefix, int32_t* recv_channel_prefix, int32_t* num_recv,
-                                 int32_t* send_head, int32_t* recv_src_idx, int32_t* num_recv_per_expert,
-                                 int32_t* rdma_channel_prefix, int32_t* recv_rdma_rank_prefix, uint32_t* barrier,
-                                 int32_t* status, cudaStream_t stream) {
-    const bool nodes = rdma_channel_prefix != nullptr && recv_rdma_rank_prefix != nullptr;
-    if (nodes && (R <= kRanksPerNode || R % kRanksPerNode != 0)) return cudaErrorInvalidValue;
-    const int NN = nodes ? R / kRanksPerNode : 0;
-    cudaError_t err = launch_kernel_cooperative(
-        layout_notify_kernel, dim3(kClusterCtas, R + 1, 1), dim3(kLayoutThreads, 1, 1),
-        sizeof(int32_t) * static_cast<size_t>(E), stream, kClusterCtas, topk_idx, R, NN, T, K, E, C, A, cap, tpr,
-        tprdma, tpe, itr, rank_prefix, channel_prefix, recv_channel_prefix, rdma_channel_prefix, num_recv, send_head,
-        recv_src_idx, num_recv_per_expert, barrier, status);
-    if (err != cudaSuccess || !nodes) return err;
-    return launch_kernel(node_prefix_kernel, dim3(1, 1, 1), dim3(kMaxRanks * kMaxNodes, 1, 1), 0, stream, 1, R, NN, C,
-                         static_cast<const int32_t*>(rdma_channel_prefix), recv_rdma_rank_prefix);
+cudaError_t launch_layout_scan(const int64_t* topk_idx, const int32_t* rank_mask, int R, int T, int K, int E, int C,
+                               int A, int64_t cap, int32_t* tpr, int32_t* tprdma, int32_t* tpe, uint8_t* itr,
+                               int32_t* rank_prefix, int32_t* channel_prefix, int32_t* recv_channel_prefix,
+                               int32_t* num_recv, int32_t* send_head, int32_t* recv_src_idx,
+                               int32_t* num_recv_per_expert, int32_t* rdma_channel_prefix,
+                               int32_t* recv_rdma_rank_prefix, uint32_t* scratch, int32_t* status,
+                               cudaStream_t stream) {
+    const bool nodes = rdma_channel_prefix != nullptr || recv_rdma_rank_prefix != nullptr;
+    if (T < 1 || (nodes && (rdma_channel_prefix == nullptr || recv_rdma_rank_prefix == nullptr ||
+                            R <= kRanksPerNode || R % kRanksPerNode != 0)))
+        return cudaErrorInvalidValue;
+    const int64_t n_tiles = static_cast<int64_t>(R) * ((T + kScanTile - 1) / kScanTile);
+    if (n_tiles > INT32_MAX) return cudaErrorInvalidValue;
+    const size_t smem = sizeof(int32_t) * static_cast<size_t>(E);
+    return launch_kernel(layout_scan_kernel, dim3(static_cast<unsigned>(n_tiles)), dim3(kScanTile), smem, stream, 1,
+                         topk_idx, rank_mask, R, T, K, E, C, A, cap, tpr, tprdma, tpe, itr, rank_prefix, channel_prefix,
+                         recv_channel_prefix, num_recv, send_head, recv_src_idx, num_recv_per_expert,
+                         rdma_channel_prefix, recv_rdma_rank_prefix, scratch, status);
 }
 
 }  // namespace ep

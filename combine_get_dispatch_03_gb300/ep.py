@@ -179,7 +179,10 @@ class Handle:
 
     def __init__(self, cfg: Config, device=None):
         self.cfg = cfg
-        self.device = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+        d = torch.device("cuda") if device is None else torch.device(device)
+        if d.type == "cuda" and d.index is None:  # "cuda" means the current device
+            d = torch.device("cuda", torch.cuda.current_device())
+        self.device = d
         self._ptr = ctypes.c_void_p()
         with torch.cuda.device(self.device):
             _raise(lib().ep_handle_create(ctypes.byref(cfg.c()), ctypes.byref(self._ptr)))

@@ -149,7 +149,11 @@ const char* ep_last_error(void);
  *                                  (8 ranks per node, [P1] NVL peers); may be NULL
  *   num_tokens_per_expert[s][e]    int32 [R][E]    top-k slots of s that chose e
  *   is_token_in_rank[s][t][r]      uint8 [R][T][R] 1 iff token (s,t) has an expert on r
- * Every output element is written.  An id outside [-1, E) sets EP_ERR_BAD_EXPERT. */
+ * Every output element is written.  An id outside [-1, E) sets EP_ERR_BAD_EXPERT.
+ * With ranks masked in the handle's mask buffer (ep_update_mask_buffer), a
+ * slot whose source rank s or whose destination rank e / EL is masked counts
+ * as a masked slot (-1): a masked rank neither sends nor receives.  The
+ * record, dispatch and combine built from this layout then leave it out. */
 ep_status ep_get_dispatch_layout(ep_handle* h, int32_t num_tokens, const int64_t* topk_idx,
                                  int32_t* num_tokens_per_rank, int32_t* num_tokens_per_rdma_rank,
                                  int32_t* num_tokens_per_expert, uint8_t* is_token_in_rank,
@@ -184,14 +188,14 @@ ep_status ep_notify_dispatch(ep_handle* h, int32_t num_tokens, const int32_t* nu
  * optional) and the dispatch record and num_recv_tokens_per_expert [R][EL] as
  * by ep_notify_dispatch(); follow with ep_dispatch() in EP_DISPATCH_PREPARED
  * mode with the same num_tokens.
- * Without the node-level record and with 1 <= num_tokens <= 16384, one pass of a
- * decoupled look-back scan: CTAs take tiles of 512 tokens in (source, token)
- * order -- the receive order of every destination rank -- publish their
- * per-rank hit counts and add up those of the earlier tiles.  Otherwise the
- * CTAs of one cooperative launch (R + 1 clusters of 8) meet at a grid barrier,
- * or, where that grid does not fit at once, the two steps run one after the
- * other.  Every wait is bounded and a timeout sets EP_ERR_TIMEOUT in the
- * status word.  Errors as the two calls it stands for. */
+ * With num_tokens >= 1 this is one pass of a decoupled look-back scan: CTAs
+ * take tiles of 512 tokens in (source, token) order -- the receive order of
+ * every destination rank -- publish their per-rank and per-node hit counts,
+ * and add up those of the earlier tiles; with two or more whole nodes of 8
+ * ranks it also writes the node-level record.  With num_tokens == 0 the two
+ * steps run one after the other.  The rank mask applies as in
+ * ep_get_dispatch_layout().  Every wait is bounded and a timeout sets
+ * EP_ERR_TIMEOUT in the status word.  Errors as the two calls it stands for. */
 ep_status ep_layout_notify(ep_handle* h, int32_t num_tokens, const int64_t* topk_idx, int32_t* num_tokens_per_rank,
                            int32_t* num_tokens_per_rdma_rank, int32_t* num_tokens_per_expert,
                            uint8_t* is_token_in_rank, int32_t* num_recv_tokens_per_expert, ep_stream_t stream);
@@ -323,10 +327,20 @@ ep_status ep_ll_combine_strided(ep_handle* h, const void* x, int64_t x_row_bytes
 
 /* The handle's mask buffer ([P1] low-latency: mask_buffer, is_rank_masked,
  * query / update / clean_mask_buffer): one int32 per rank, all zero after
- * ep_handle_create().  ep_ll_dispatch() treats every slot whose source or
- * destination rank is masked as a masked slot (no message, not counted, no
- * contribution in ep_ll_combine()): a masked rank neither sends nor
- * receives.  The normal-mode path ignores the mask.
+ * ep_handle_create().  A masked rank neither sends nor receives:
+ *  - ep_ll_dispatch() treats every slot whose source or destination rank is
+ *    masked as a masked slot (no message, not counted, no contribution in
+ *    ep_ll_combine());
+ *  - the normal-mode layout (ep_get_dispatch_layout(), ep_layout_notify())
+ *    does the same, so such slots are not counted in num_tokens_per_expert,
+ *    the token does not go to that rank in is_token_in_rank and the counts,
+ *    and the record, dispatch and combine built from that layout leave the
+ *    rank out (it receives no row; its tokens go nowhere and combine to the
+ *    bias sum).  ep_notify_dispatch() and a fresh ep_dispatch() follow the
+ *    layout they are given; a cached dispatch or a combine follows its record,
+ *    i.e. the mask as it was when the layout was computed.
+ * The pages show the mask on the low-latency path only; the normal path
+ * applies it the same way.
  *   update: asynchronously set (masked != 0) or clear one rank's entry;
  *   query:  synchronise `stream` and copy the R entries to host_mask[R];
  *   clean:  asynchronously clear every entry. */

@@ -55,7 +55,7 @@ def _bind(lib):
     lib.oracle_e4m3_to_f32.restype = ctypes.c_float
     lib.oracle_fp8_quantize_group.argtypes = [P, I, I, P, P, P]
     lib.oracle_fp8_quantize_group.restype = None
-    lib.oracle_get_dispatch_layout.argtypes = [I, I, I, I, P, P, P, P, P]
+    lib.oracle_get_dispatch_layout.argtypes = [I, I, I, I, P, P, P, P, P, P]
     lib.oracle_dispatch_notify.argtypes = [I, I, I, I, I, L, P, P, P, P, P, P, P, P, P, P]
     lib.oracle_rdma_prefix.argtypes = [I, I, I, P, P, P]
     lib.oracle_dispatch.argtypes = [I, I, I, I, I, L, I, P, P, P, P, P, P, L, P, P, P, P]
@@ -151,15 +151,17 @@ def fp8_quantize_group(x_bits: np.ndarray, round_scale: bool = False):
 
 # ---------------------------------------------------------------- layout
 
-def get_dispatch_layout(topk_idx: np.ndarray, num_experts: int, with_rdma: bool = True):
-    """get_dispatch_layout: counts per rank / RDMA node / expert and is_token_in_rank."""
+def get_dispatch_layout(topk_idx: np.ndarray, num_experts: int, with_rdma: bool = True, rank_mask=None):
+    """get_dispatch_layout: counts per rank / RDMA node / expert and is_token_in_rank.
+    rank_mask: optional [R] ints, nonzero = the rank neither sends nor receives."""
     R, T, K = topk_idx.shape
     idx = _c(topk_idx, np.int64)
+    mask = _c(rank_mask, np.int32)
     tpr = np.zeros((R, R), np.int32)
     tprdma = np.zeros((R, (R + 7) // 8), np.int32) if with_rdma else None
     tpe = np.zeros((R, num_experts), np.int32)
     itr = np.zeros((R, T, R), np.uint8)
-    _check(_load().oracle_get_dispatch_layout(R, T, K, num_experts, _p(idx), _p(tpr), _p(tprdma),
+    _check(_load().oracle_get_dispatch_layout(R, T, K, num_experts, _p(idx), _p(mask), _p(tpr), _p(tprdma),
                                               _p(tpe), _p(itr)), "get_dispatch_layout")
     return dict(num_tokens_per_rank=tpr, num_tokens_per_rdma_rank=tprdma,
                 num_tokens_per_expert=tpe, is_token_in_rank=itr)

@@ -168,8 +168,17 @@ void oracle_fp8_quantize_group(const uint16_t* x, int n, int round_scale,
  *   num_tokens_per_rank[s][r]   = #t with is_token_in_rank[s][t][r]
  *   num_tokens_per_rdma_rank[s][n] = #t with a hit in node n (8 ranks per
  *     node), computed only when the pointer is non-NULL.
+ *
+ * Rank masking ([P1] low-latency receive excerpt: mask_buffer and
+ * is_rank_masked; the pages show it in the low-latency path only): when
+ * rank_mask is non-NULL, a slot whose source rank s or whose destination
+ * rank e / EL has rank_mask != 0 counts as a masked slot (-1).  Reading, the
+ * same as the low-latency dispatch's: a masked rank neither sends nor
+ * receives, so the layout -- and the record, dispatch and combine that
+ * follow from it -- leaves it out.  An expert id out of range is an error
+ * whatever the mask.
  * ---------------------------------------------------------------------- */
-int oracle_get_dispatch_layout(int R, int T, int K, int E, const int64_t* topk_idx,
+int oracle_get_dispatch_layout(int R, int T, int K, int E, const int64_t* topk_idx, const int32_t* rank_mask,
                                int32_t* num_tokens_per_rank, int32_t* num_tokens_per_rdma_rank,
                                int32_t* num_tokens_per_expert, uint8_t* is_token_in_rank) {
     if (R <= 0 || T < 0 || K <= 0 || E <= 0 || E % R != 0) return ORACLE_BAD_ARG;
@@ -186,6 +195,7 @@ int oracle_get_dispatch_layout(int R, int T, int K, int E, const int64_t* topk_i
                 int64_t e = topk_idx[((size_t)s * T + t) * K + k];
                 if (e == -1) continue;
                 if (e < 0 || e >= E) return ORACLE_BAD_EXPERT;
+                if (rank_mask && (rank_mask[s] != 0 || rank_mask[e / EL] != 0)) continue;
                 num_tokens_per_expert[(size_t)s * E + e] += 1;
                 hit[e / EL] = 1;
             }

@@ -1,8 +1,8 @@
 """Seeded random shapes across the ABI's limits, every output against the oracle.
 
 Each case draws R, experts per rank, top-k, tokens (0 included), hidden (down to 8 channels),
-channels, alignment, routing, masked slots, an SM cap for the data kernels and a masked rank for
-the LL path.  It runs the one-call layout + record (with the node-level record when the ranks
+channels, alignment, routing, masked slots, an SM cap for the data kernels and a masked rank (in
+the handle's mask buffer, for the normal and the LL path).  It runs the one-call layout + record (with the node-level record when the ranks
 form whole nodes of 8), the prepared bf16 dispatch, the combine with biases and fp32 output, the
 cached FP8 cast and FP8-input dispatches when H allows, and the LL dispatch (bf16 and, when H
 allows, FP8 + UE8M0) and combine."""
@@ -37,23 +37,29 @@ def draw(i):
     shape = W.Shape(f"fuzz{i}", R=R, T=T, H=H, E=E, K=K, routing=routing, C=C, A=A, mask_p=mask_p,
                     max_tokens=max(T, 1) + int(g.integers(0, 4)), seed=30000 + i)
     max_sms = int(g.choice([0, 0, 0, 1, 3, 16]))     # data kernels capped to this many SMs' worth
-    ll_masked = int(g.integers(-1, R)) if R > 1 else -1  # a rank masked in the LL path, or none
-    return shape, max_sms, ll_masked
+    masked = int(g.integers(-1, R)) if R > 1 else -1  # a rank masked in the mask buffer, or none
+    return shape, max_sms, masked
 
 
 @pytest.mark.parametrize("i", range(N_CASES))
 def test_fuzz_normal_and_ll(i):
-    shape, max_sms, ll_masked = draw(i)
+    shape, max_sms, masked = draw(i)
     idx, w = W.routing(shape)
     x = W.tokens_x(shape)
     xb = W.bf16_bits(x)
+    mask = None
+    if masked >= 0:
+        mask = np.zeros(shape.R, np.int32)
+        mask[masked] = 1
     cap = max(P.needed_capacity(idx, shape.E), 1)
     h = ep.Handle(P.config_of(shape, cap, max_sms))
+    if mask is not None:
+        ep.ep_update_mask_buffer(h, masked, True)
     idx_d, w_d, x_d = torch.from_numpy(idx).to(P.DEV), torch.from_numpy(w).to(P.DEV), x.to(P.DEV)
 
     # layout and record in one call, then the prepared dispatch and the combine
     lay = ep.ep_layout_notify(h, idx_d)
-    ora_lay = O.get_dispatch_layout(idx, shape.E)
+    ora_lay = O.get_dispatch_layout(idx, shape.E, rank_mask=mask)
     ora_n = O.dispatch_notify(ora_lay["num_tokens_per_rank"], ora_lay["is_token_in_rank"],
                               ora_lay["num_tokens_per_expert"], shape.C, shape.A, cap)
     assert h.status() == 0, shape
@@ -101,14 +107,10 @@ def test_fuzz_normal_and_ll(i):
 
     # low-latency dispatch and combine
     maxT = shape.max_tokens
-    mask = None
-    if ll_masked >= 0:
-        mask = np.zeros(shape.R, np.int32)
-        mask[ll_masked] = 1
     for use_fp8 in ([False, True] if shape.H % 512 == 0 else [False]):
         hl = ep.Handle(P.config_of(shape, 0, max_sms))
         if mask is not None:
-            ep.ep_update_mask_buffer(hl, ll_masked, True)
+            ep.ep_update_mask_buffer(hl, masked, True)
         out = ep.ep_ll_dispatch(hl, x_d, idx_d, use_fp8=use_fp8, use_ue8m0=use_fp8)
         assert hl.status() == 0, shape
         ora = O.ll_dispatch(xb, idx, maxT, shape.E, use_fp8=use_fp8, use_ue8m0=use_fp8, rank_mask=mask)

@@ -145,30 +145,72 @@ def test_layout_notify_in_one_launch(shape):
     _layout_notify_round(shape)
 
 
-# The one-pass scan takes up to 32 tiles of 512 tokens per source (its look-back window): T = 16384
-# is the last size it serves, T = 16385 goes to the cluster kernels; the third shape has a single
-# tile with a 1-token tail.
-SCAN_EDGE_CASES = [S("scan_max_tiles", 2, 16384, 16, 8, 2, routing="gumbel", mask_p=0.05, C=7, seed=80),
-                   S("scan_fallback", 3, 16385, 16, 12, 3, routing="zipf", C=5, A=4, seed=81),
+# The one-pass scan's look-back reads 32 tiles of 512 tokens per round of loads: T = 16384 is one
+# window per source, T = 16385 and 32768 need more (a source's same-source sum then stops at the
+# nearest inclusive tile of that source), the R = 16 shape adds the node-level record to many tiles
+# per source; the last shape has a single tile with a 1-token tail.
+SCAN_EDGE_CASES = [S("scan_32_tiles", 2, 16384, 16, 8, 2, routing="gumbel", mask_p=0.05, C=7, seed=80),
+                   S("scan_33_tiles", 3, 16385, 16, 12, 3, routing="zipf", C=5, A=4, seed=81),
+                   S("scan_64_tiles", 2, 32768, 16, 8, 2, routing="uniform", mask_p=0.1, C=12, seed=83),
+                   S("scan_nodes_40_tiles", 16, 20000, 16, 64, 4, routing="zipf", mask_p=0.05, C=9, seed=84),
                    S("scan_tail", 5, 513, 16, 20, 4, mask_p=0.2, C=3, seed=82)]
 
 
 @pytest.mark.parametrize("shape", SCAN_EDGE_CASES, ids=lambda s: s.name)
 def test_layout_notify_scan_edges(shape):
-    """The one-pass layout + record at the edges of its tiling (32 tiles per source, the first size
-    past it, a 1-token last tile) equals the oracle."""
+    """The one-pass layout + record at the edges of its tiling (one look-back window per source,
+    more than one, with the node-level record, a 1-token last tile) equals the oracle."""
     _layout_notify_round(shape)
 
 
-def _layout_notify_round(shape):
-    idx, w = W.routing(shape)
+# (shape, masked ranks): one or two ranks masked in the handle's mask buffer
+MASK_CASES = [(NORMAL_CASES[0], [NORMAL_CASES[0].R - 1]), (NORMAL_CASES[1], [0]),
+              (S("mask_r16_nodes", 16, 700, 256, 64, 6, routing="gumbel", mask_p=0.05, C=12, seed=85), [3, 12]),
+              (S("mask_r5_multitile", 5, 1500, 128, 20, 4, routing="zipf", C=7, A=4, seed=86), [2])]
+
+
+@pytest.mark.parametrize("case", MASK_CASES, ids=[c[0].name for c in MASK_CASES])
+def test_normal_rank_mask(case):
+    """Masked ranks in the mask buffer: the layout leaves out every slot that starts or ends on one,
+    through both layout paths (ep_get_dispatch_layout + fresh dispatch, ep_layout_notify + prepared
+    dispatch); record, rows and combine equal the oracle's masked layout; a masked rank receives no
+    row; cleaning the mask restores the unmasked layout."""
+    shape, masked = case
+    mask = np.zeros(shape.R, np.int32)
+    mask[masked] = 1
+    idx, _ = W.routing(shape)
     cap = max(P.needed_capacity(idx, shape.E), 1)
     h = ep.Handle(P.config_of(shape, cap))
+    for r in masked:
+        ep.ep_update_mask_buffer(h, r, True)
+    _layout_notify_round(shape, h=h, rank_mask=mask)
+    lay = ep.ep_get_dispatch_layout(h, torch.from_numpy(idx).to(P.DEV))
+    ora_lay = O.get_dispatch_layout(idx, shape.E, rank_mask=mask)
+    P.compare_layout(lay, ora_lay)
+    assert (ora_lay["num_tokens_per_rank"][:, masked] == 0).all()
+    x = W.tokens_x(shape).to(P.DEV)
+    ep.ep_dispatch(h, x, topk_idx=torch.from_numpy(idx).to(P.DEV), num_tokens_per_rank=lay["num_tokens_per_rank"],
+                   is_token_in_rank=lay["is_token_in_rank"], num_tokens_per_expert=lay["num_tokens_per_expert"])
+    assert h.status() == 0
+    ora_n = O.dispatch_notify(ora_lay["num_tokens_per_rank"], ora_lay["is_token_in_rank"],
+                              ora_lay["num_tokens_per_expert"], shape.C, shape.A, cap)
+    P.compare_record(h, ora_n, shape.T)
+    assert (P.host(h.export("num_recv"))[masked] == 0).all()
+    ep.ep_clean_mask_buffer(h)
+    P.compare_layout(ep.ep_get_dispatch_layout(h, torch.from_numpy(idx).to(P.DEV)), O.get_dispatch_layout(idx, shape.E))
+    h.destroy()
+
+
+def _layout_notify_round(shape, h=None, rank_mask=None):
+    idx, w = W.routing(shape)
+    cap = max(P.needed_capacity(idx, shape.E), 1)
+    if h is None:
+        h = ep.Handle(P.config_of(shape, cap))
     idx_d, w_d = torch.from_numpy(idx).to(P.DEV), torch.from_numpy(w).to(P.DEV)
     x = W.tokens_x(shape)
     lay = ep.ep_layout_notify(h, idx_d)
     assert h.status() == 0
-    ora_lay = O.get_dispatch_layout(idx, shape.E)
+    ora_lay = O.get_dispatch_layout(idx, shape.E, rank_mask=rank_mask)
     P.compare_layout(lay, ora_lay)
     ora_n = O.dispatch_notify(ora_lay["num_tokens_per_rank"], ora_lay["is_token_in_rank"],
                               ora_lay["num_tokens_per_expert"], shape.C, shape.A, cap)

@@ -87,3 +87,26 @@ def test_node_record_needs_whole_nodes(R):
             h.export(key)
         assert err.value.status == 5  # EP_ERR_UNSUPPORTED
     h.destroy()
+
+
+@pytest.mark.parametrize("case", CASES, ids=[f"R{c[0]}-T{c[1]}-C{c[6]}" for c in CASES])
+def test_layout_notify_builds_node_record(case):
+    """ep_layout_notify (the one-pass scan for T >= 1, the two separate kernels for T = 0) builds the
+    same node-level record as the separate calls: every array against the oracle."""
+    shape = _shape(*case)
+    idx, _ = W.routing(shape)
+    cap = max(P.needed_capacity(idx, shape.E), 1)
+    h = ep.Handle(P.config_of(shape, cap))
+    for _ in range(2):  # the second call runs on the scratch the first one left
+        lay = ep.ep_layout_notify(h, torch.from_numpy(idx).to(P.DEV))
+    assert h.status() == 0
+    ora_lay = O.get_dispatch_layout(idx, shape.E)
+    P.compare_layout(lay, ora_lay)
+    ora_n = O.dispatch_notify(ora_lay["num_tokens_per_rank"], ora_lay["is_token_in_rank"],
+                              ora_lay["num_tokens_per_expert"], shape.C, shape.A, cap)
+    P.compare_record(h, ora_n, shape.T)
+    np.testing.assert_array_equal(P.host(lay["num_recv_tokens_per_expert"]), ora_n["num_recv_tokens_per_expert"])
+    want = O.rdma_prefix(ora_lay["is_token_in_rank"], shape.C)
+    for key in ("rdma_channel_prefix_matrix", "recv_rdma_rank_prefix_sum"):
+        np.testing.assert_array_equal(_record(h, key), want[key], err_msg=key)
+    h.destroy()

@@ -53,6 +53,11 @@ MUTATIONS = [
      "const int l = r / 8, n = r % 8 % NN;"),
     ("ll mask ignores the source", "if (rank_mask && (rank_mask[s] != 0 || rank_mask[e / EL] != 0)) return -1;",
      "if (rank_mask && rank_mask[e / EL] != 0) return -1;"),
+    ("layout mask ignores the source", "if (rank_mask && (rank_mask[s] != 0 || rank_mask[e / EL] != 0)) continue;",
+     "if (rank_mask && rank_mask[e / EL] != 0) continue;"),
+    ("layout mask ignores the destination",
+     "if (rank_mask && (rank_mask[s] != 0 || rank_mask[e / EL] != 0)) continue;",
+     "if (rank_mask && rank_mask[s] != 0) continue;"),
 ]
 
 
@@ -64,6 +69,7 @@ def _pin_checks():
         ("p1 notify", lambda: pins.test_p1_notify(p1, 4)),
         ("p1 dispatch/combine", lambda: pins.test_p1_dispatch_combine(p1)),
         ("p1 low latency", lambda: pins.test_p1_low_latency(p1)),
+        ("p1 rank mask", pins.test_p1_rank_mask),
         ("bf16 vs torch", pins.test_bf16_rounding_matches_torch),
         ("e4m3 hand codes", pins.test_e4m3_hand_codes),
         ("e4m3 brute force", pins.test_e4m3_exhaustive_against_brute_force),
@@ -79,6 +85,7 @@ def _pin_checks():
         checks.append((f"ll invariants {case}", lambda c=case: pins.test_low_latency_invariants(c, "fp8_ue8m0")))
         checks.append((f"ll combine {case}", lambda c=case: pins.test_low_latency_combine(c)))
         checks.append((f"ll rank mask {case}", lambda c=case: pins.test_low_latency_rank_mask(c)))
+        checks.append((f"normal rank mask {case}", lambda c=case: pins.test_normal_rank_mask(c)))
     checks.append(("dispatch fp8 modes", pins.test_dispatch_fp8_modes))
     checks.append(("two-level hand case", pins.test_two_level_hand_case))
     for case in pins.TWO_LEVEL_CASES:

@@ -570,6 +570,73 @@ def test_low_latency_rank_mask(case):
     assert (masked["slot_row"][R // 2] == -1).all()
 
 
+def _mask_slots(idx, mask, EL):
+    """topk_idx with every slot that starts or ends on a masked rank set to -1 (numpy, no oracle)."""
+    R = idx.shape[0]
+    src = np.asarray(mask, bool)[:, None, None].repeat(idx.shape[1], 1).repeat(idx.shape[2], 2)
+    dst = np.where(idx >= 0, np.asarray(mask, bool)[np.clip(idx, 0, None) // EL], False)
+    out = idx.copy()
+    out[(idx >= 0) & (src | dst)] = -1
+    assert out.shape[0] == R
+    return out
+
+
+def test_p1_rank_mask():
+    """The hand case with rank 1 masked: layout, record, rows, combine multiplicity, weights."""
+    g = gold("p1_rank_mask_case.json")
+    idx = np.array(g["topk_idx"], np.int64)
+    R, T, K, E = g["R"], g["T"], g["K"], g["E"]
+    lay = O.get_dispatch_layout(idx, E, rank_mask=np.array(g["rank_mask"], np.int32))
+    for key in ("is_token_in_rank", "num_tokens_per_rank", "num_tokens_per_rdma_rank", "num_tokens_per_expert"):
+        np.testing.assert_array_equal(lay[key], g[key], err_msg=key)
+    n = O.dispatch_notify(lay["num_tokens_per_rank"], lay["is_token_in_rank"], lay["num_tokens_per_expert"],
+                          g["C"], 1, capacity=3)
+    assert n["status"] == O.OK
+    for key in ("rank_prefix_matrix", "num_recv", "channel_prefix_matrix", "recv_channel_prefix_matrix",
+                "send_head"):
+        np.testing.assert_array_equal(n[key], g[key], err_msg=key)
+    np.testing.assert_array_equal(n["recv_src_idx"][0, :2], g["recv_src_idx_rank0"])
+    np.testing.assert_array_equal(n["num_recv_tokens_per_expert"], g["num_recv_tokens_per_expert_align1"])
+    H = 128
+    x = np.stack([np.stack([bits_of([float(s * T + t + 1)] * H) for t in range(T)]) for s in range(R)])
+    w = np.arange(R * T * K, dtype=np.float32).reshape(R, T, K) + 0.5
+    d = O.dispatch(x, n["send_head"], 3, E, topk_idx=idx, topk_weights=w)
+    np.testing.assert_array_equal(d["recv_topk_idx"][0, :2], g["recv_topk_idx_rank0"])
+    c = O.combine(d["recv_x"], n["send_head"], recv_topk_weights=d["recv_topk_weights"], out_fp32=True)
+    mult = np.array(g["combine_multiplicity"], np.float32)
+    np.testing.assert_array_equal(c["out"], mult[:, :, None] * f32_of_bits(x))
+    np.testing.assert_array_equal(c["combined_topk_weights"],
+                                  np.where(np.array(g["combined_topk_weights_valid"], bool), w, 0).astype(np.float32))
+
+
+@pytest.mark.parametrize("case", CASES)
+def test_normal_rank_mask(case):
+    """Masking ranks in the layout equals removing every slot that starts or ends on them; the masked
+    ranks then receive no row and their tokens go nowhere."""
+    shape, idx, w, x = _case(*case)
+    R, T, E, EL = shape.R, shape.T, shape.E, shape.EL
+    for masked in ({R // 2}, {0, R - 1}):
+        mask = np.zeros(R, np.int32)
+        mask[list(masked)] = 1
+        got = O.get_dispatch_layout(idx, E, rank_mask=mask)
+        want = O.get_dispatch_layout(_mask_slots(idx, mask, EL), E)
+        for key in ("is_token_in_rank", "num_tokens_per_rank", "num_tokens_per_rdma_rank", "num_tokens_per_expert"):
+            np.testing.assert_array_equal(got[key], want[key], err_msg=key)
+        for r in masked:
+            assert not got["is_token_in_rank"][r].any() and not got["is_token_in_rank"][:, :, r].any()
+            assert not got["num_tokens_per_expert"][r].any()
+            assert not got["num_tokens_per_expert"][:, r * EL:(r + 1) * EL].any()
+        n = O.dispatch_notify(got["num_tokens_per_rank"], got["is_token_in_rank"], got["num_tokens_per_expert"],
+                              shape.C, shape.A, max(1, int(got["num_tokens_per_rank"].sum(axis=0).max())))
+        assert n["status"] == O.OK
+        for r in masked:
+            assert n["num_recv"][r] == 0 and (n["send_head"][:, :, r] == -1).all() and (n["send_head"][r] == -1).all()
+    no_mask = O.get_dispatch_layout(idx, E, rank_mask=np.zeros(R, np.int32))
+    plain = O.get_dispatch_layout(idx, E)
+    for key in plain:
+        np.testing.assert_array_equal(no_mask[key], plain[key], err_msg=key)
+
+
 # --------------------------------------------------------------------- two-level (node) record
 
 def _two_level_hand():
