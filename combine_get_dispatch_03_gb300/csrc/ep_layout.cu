@@ -444,16 +444,6 @@ constexpr int kScanWarps = kScanTile / kWarpSize;
 static_assert(kScanWarps <= kWarpSize, "the column scan gives one lane per warp");
 constexpr int kScanAggregate = 1, kScanInclusive = 2;
 
-__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
-    uint32_t v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
-
-__device__ __forceinline__ void st_release_u32(uint32_t* p, uint32_t v) {
-    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-
 // Per-tile words of the scratch, NC = R + ceil(R/8) columns: the state word, then the tile's
 // per-column hits [NC], its inclusive prefix over all earlier tiles for the rank columns [R], its
 // inclusive prefix over this source's tiles for every column [NC], and its expert histogram [E].

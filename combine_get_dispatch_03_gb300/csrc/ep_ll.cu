@@ -8,13 +8,14 @@
 // rows of its expert e: recv_msgs[e][row] with e = d*EL + j.  The pages take a
 // slot with an atomicAdd on a per-expert counter, whose order depends on
 // timing; here the rows are fixed beforehand so the layout is deterministic:
-//   1. ll_count (one CTA per source rank): stable rank of each slot among the
-//      slots of the same (source, expert), in (token, k) order, and the count;
-//   2. ll_finish: begin of each source block = prefix over sources (one warp
-//      per expert); packed_recv_count, packed_recv_layout_range, receive
-//      stats; and the final row of every slot, which stays in the handle for
-//      the combine;
-//   3. ll_dispatch: read + cast the row once into a complete message in
+//   1. ll_meta (one CTA per source rank, one launch): stable rank of each slot
+//      among the slots of the same (source, expert), in (token, k) order, and
+//      the per-expert count; the begin of each source block = the counts of
+//      the earlier sources, which their CTAs publish (bounded waits); the final
+//      row of every slot, which stays in the handle for the combine;
+//      packed_recv_layout_range, and from the last source's CTA
+//      packed_recv_count and the receive stats;
+//   2. ll_dispatch: read + cast the row once into a complete message in
 //      shared memory, then one bulk store per destination slot (a register
 //      kernel, one warp per token, serves messages too long to stage).
 // LL combine (§4.3): one warp per token gathers its K expert outputs and
@@ -30,41 +31,90 @@ namespace ep {
 
 namespace {
 
-constexpr int kLLCountThreadsLarge = 1024;  // the count kernel's block while its histograms fit in smem
-constexpr int kFinishThreads = 256;
+constexpr int kLLMetaThreadsLarge = 1024;  // the metadata kernel's block while its histograms fit in smem
 constexpr int kLLUnroll = 4;
 constexpr int kLLCombineUnroll = 2;
 constexpr int kLLCombineFanIn = 4;         // slots loaded together before accumulation
 constexpr int kLLCombineFanInSmallK = 8;   // ... with top-k up to 8: every slot in one batch
 
+// Per-source state word of the metadata kernel: the epoch tag (bits 2..31) and 1 once the
+// source's counts are published.
+constexpr uint32_t kLLPublished = 1;
+
+// All lanes of the calling warp: true once the word holds `want` (bounded wait).
+__device__ __forceinline__ bool ll_wait_word(const uint32_t* word, uint32_t want) {
+    for (uint32_t it = 0; it < kMaxWaitIterations; ++it)
+        if (ld_acquire_u32(word) == want) return true;
+    return false;
+}
+
+// The slot rows of every source in one launch, one CTA per source.  CTAs take their source by
+// ticket, so a CTA only ever waits for sources whose CTAs already started, and for source s:
+//   1. the stable position of each of its slots among the slots of the same (source, expert), in
+//      (token, k) order: per-warp histograms (__match_any_sync) and a prefix over the warps, one
+//      chunk of kThreads slots at a time; the counts cnt[s][e] come out of the same pass;
+//   2. publishes cnt[s][.] and its state word;
+//   3. waits (bounded) for the earlier sources' state words and sums their counts: begin[e][s];
+//   4. writes each slot's final row begin + position (-1 past the R * maxT rows of an expert),
+//      and packed_recv_layout_range[e][s]; the CTA of the last source also has every expert's
+//      total, so it writes packed_recv_count (and adds it to the receive stats).
+// Slots that start or end on a masked rank count as masked slots.  The state words carry the
+// launch's epoch (scratch word 2, advanced by the last CTA to finish, which also resets the
+// tickets), so states of an earlier launch never match and CUDA-graph replays need no reset.
 template <int kThreads>
 __global__ void __launch_bounds__(kThreads)
-    ll_count_kernel(int R, int T, int maxT, int K, int E, const int64_t* __restrict__ topk_idx,
-                    const int32_t* __restrict__ rank_mask, int32_t* __restrict__ slot, int32_t* __restrict__ cnt,
-                    int32_t* status) {
+    ll_meta_kernel(int R, int T, int maxT, int K, int E, const int64_t* __restrict__ topk_idx,
+                   const int32_t* __restrict__ rank_mask, int32_t* __restrict__ slot,
+                   int32_t* __restrict__ packed_recv_count, int64_t* __restrict__ layout_range,
+                   int32_t* __restrict__ stats, uint32_t* __restrict__ scratch, int32_t* status) {
     pdl_enter();
     constexpr int kWarps = kThreads / kWarpSize;
     constexpr int kScanChunk = kWarps < 16 ? kWarps : 16;
     static_assert(kWarps % kScanChunk == 0, "whole scan chunks");
     extern __shared__ int32_t smem[];
-    int32_t* s_warp = smem;                   // [kWarps][E]: per-warp count -> exclusive prefix
-    int32_t* s_run = smem + kWarps * E;  // [E]: slots of this source seen so far
-    const int s = blockIdx.x;
+    int32_t* s_warp = smem;               // [kWarps][E]: per-warp count -> exclusive prefix
+    int32_t* s_run = smem + kWarps * E;   // [E]: slots of this source seen so far -> cnt[s][.]
+    int32_t* s_begin = s_run + E;         // [E]: slots of the earlier sources
+    __shared__ int s_src, s_ok, s_last;
+    __shared__ uint32_t s_epoch;
     const int tid = threadIdx.x;
     const int lane = lane_id();
     const int warp = tid / kWarpSize;
-    const int n = T * K;
-    const int64_t* idx_s = topk_idx + static_cast<int64_t>(s) * T * K;
-    int32_t* slot_s = slot + static_cast<int64_t>(s) * maxT * K;
+    const int64_t n = static_cast<int64_t>(T) * K;
+    const int EL = E / R;
+    const int64_t slots = static_cast<int64_t>(R) * maxT;
+    uint32_t* states = scratch + 4;
+    uint32_t* counts = scratch + kLLMetaCounts;
 
-    __shared__ int32_t s_mask[kMaxRanks];  // rank mask (0 everywhere without one)
-    for (int e = tid; e < E; e += kThreads) s_run[e] = 0;
-    if (tid < kMaxRanks) s_mask[tid] = rank_mask != nullptr && tid < R ? __ldg(rank_mask + tid) : 0;
-    int64_t next = tid < n ? __ldg(idx_s + tid) : -1;  // the next chunk's entry, loaded one chunk ahead
-    for (int base = 0; base < n; base += kThreads) {
+    if (tid == 0) {
+        s_src = static_cast<int>(atomicAdd(scratch, 1u));
+        s_epoch = ld_acquire_u32(scratch + 2);
+        s_ok = 1;
+    }
+    // the first chunk of the source the ticket usually gives (blockIdx.x), loaded meanwhile
+    const int guess = static_cast<int>(blockIdx.x);
+    int64_t next = tid < n ? __ldg(topk_idx + guess * n + tid) : -1;
+    for (int e = tid; e < E; e += kThreads) {
+        s_run[e] = 0;
+        s_begin[e] = 0;
+    }
+    const uint32_t rmask = __ballot_sync(kFullMask, rank_mask != nullptr && lane < R && __ldg(rank_mask + lane) != 0);
+    __syncthreads();
+    const int s = s_src;
+    const uint32_t tag = (s_epoch & 0x3fffffffu) << 2;
+    if (s != guess) next = tid < n ? __ldg(topk_idx + s * n + tid) : -1;
+    const int64_t* idx_s = topk_idx + s * n;
+    int32_t* slot_s = slot + static_cast<int64_t>(s) * maxT * K;
+    const bool src_masked = (rmask >> s) & 1u;
+
+    // 1. positions within (source, expert) and the counts
+    int64_t i_last = -1;  // this thread's slot of the last chunk, kept in registers
+    int e_last = -1;
+    int32_t p_last = -1;
+    for (int64_t base = 0; base < n; base += kThreads) {
         for (int i = tid; i < kWarps * E; i += kThreads) s_warp[i] = 0;
         __syncthreads();
-        const int i = base + tid;
+        const int64_t i = base + tid;
         const int64_t v = next;
         if (base + kThreads + tid < n) next = __ldg(idx_s + base + kThreads + tid);
         int e = -1;
@@ -72,7 +122,7 @@ __global__ void __launch_bounds__(kThreads)
             if (v >= 0 && v < E) e = static_cast<int>(v);
             else if (v != -1) report(status, EP_ERR_BAD_EXPERT);
             // a masked rank neither sends nor receives
-            if (e >= 0 && (s_mask[s] != 0 || s_mask[e / (E / R)] != 0)) e = -1;
+            if (e >= 0 && (src_masked || ((rmask >> (e / EL)) & 1u))) e = -1;
         }
         const unsigned peers = __match_any_sync(kFullMask, e);
         const int before = __popc(peers & lanemask_lt());
@@ -96,102 +146,88 @@ __global__ void __launch_bounds__(kThreads)
             s_run[x] = run;
         }
         __syncthreads();
-        if (i < n) slot_s[i] = e >= 0 ? s_warp[warp * E + e] + before : -1;
-        __syncthreads();
-    }
-    for (int e = tid; e < E; e += kThreads) cnt[static_cast<int64_t>(s) * E + e] = s_run[e];
-}
-
-// Blocks [0, expert_blocks): one warp per expert e; lane s holds the count of
-// source s, a warp scan gives each source block's begin (R <= 32).  The other
-// blocks: one thread per top-k slot turns its position within (source, expert)
-// into the final row, begin(e, s) + position, or -1 past the R * maxT capacity.
-__global__ void ll_finish_kernel(int R, int T, int maxT, int K, int E, int expert_blocks,
-                                 const int64_t* __restrict__ topk_idx, const int32_t* __restrict__ cnt,
-                                 int32_t* __restrict__ slot, int32_t* __restrict__ packed_recv_count,
-                                 int64_t* __restrict__ layout_range, int32_t* __restrict__ stats, int32_t* status) {
-    pdl_enter();
-    const int64_t slots = static_cast<int64_t>(R) * maxT;
-    if (static_cast<int>(blockIdx.x) < expert_blocks) {
-        const int lane = lane_id();
-        const int warps = blockDim.x / kWarpSize;
-        const int e = blockIdx.x * warps + threadIdx.x / kWarpSize;
-        if (e >= E) return;
-        const int32_t c = lane < R ? __ldg(cnt + static_cast<int64_t>(lane) * E + e) : 0;
-        int32_t incl = c;
-#pragma unroll
-        for (int off = 1; off < kWarpSize; off <<= 1) {
-            const int32_t o = __shfl_up_sync(kFullMask, incl, off);
-            if (lane >= off) incl += o;
-        }
-        const int32_t begin = incl - c;
-        if (lane < R)
-            layout_range[static_cast<int64_t>(e) * R + lane] =
-                static_cast<int64_t>((static_cast<uint64_t>(static_cast<uint32_t>(c)) << 32) |
-                                     static_cast<uint32_t>(begin));
-        const int32_t total = __shfl_sync(kFullMask, incl, kWarpSize - 1);
-        if (lane == 0) {
-            if (total > slots) report(status, EP_ERR_CAPACITY);
-            const int32_t n = static_cast<int32_t>(total < slots ? total : slots);
-            packed_recv_count[e] = n;
-            if (stats != nullptr) stats[e] += n;
-        }
-        return;
-    }
-    const int64_t n_slots = static_cast<int64_t>(R) * T * K;
-    const int64_t i0 = static_cast<int64_t>(blockIdx.x - expert_blocks) * blockDim.x;
-    const int64_t i = i0 + threadIdx.x;
-    // With E <= blockDim and every slot of the CTA from one source, the CTA sums the begins of
-    // that source's blocks for all experts into shared memory while its slots' expert ids and
-    // positions load: loads that need no expert id, so a slot waits for one round of loads
-    // instead of two.
-    __shared__ int32_t s_begin[kFinishThreads];
-    const int64_t i_last = (i0 + blockDim.x < n_slots ? i0 + blockDim.x : n_slots) - 1;
-    const int s_first = static_cast<int>(i0 / (static_cast<int64_t>(T) * K));
-    const bool table = E <= static_cast<int>(blockDim.x) && i0 < n_slots &&
-                       s_first == static_cast<int>(i_last / (static_cast<int64_t>(T) * K));
-    const bool live = i < n_slots;
-    int s = 0;
-    int64_t v = -1;
-    int32_t pos = -1;
-    int32_t* sp = nullptr;
-    if (live) {
-        s = static_cast<int>(i / (static_cast<int64_t>(T) * K));
-        v = __ldg(topk_idx + i);
-        sp = slot + static_cast<int64_t>(s) * maxT * K + (i - static_cast<int64_t>(s) * T * K);
-        pos = *sp;
-    }
-    if (table) {
-        const int e = threadIdx.x;
-        if (e < E) {
-            int32_t part[kMaxRanks];
-#pragma unroll
-            for (int q = 0; q < kMaxRanks; ++q) part[q] = q < s_first ? __ldg(cnt + static_cast<int64_t>(q) * E + e) : 0;
-            int32_t b = 0;
-#pragma unroll
-            for (int q = 0; q < kMaxRanks; ++q) b += part[q];
-            s_begin[e] = b;
-        }
-        __syncthreads();
-    }
-    if (!live) return;
-    int32_t row = -1;
-    if (v >= 0 && v < E && pos >= 0) {
-        int64_t begin = 0;
-        if (table) {
-            begin = s_begin[v];
+        const int32_t p = e >= 0 ? s_warp[warp * E + e] + before : -1;
+        if (base + kThreads < n) {
+            if (i < n) slot_s[i] = p;  // an earlier chunk: its position, turned into a row in step 4
         } else {
-            // the counts of the earlier sources, all loads in flight at once (R <= kMaxRanks)
-            int32_t part[kMaxRanks];
-#pragma unroll
-            for (int sp2 = 0; sp2 < kMaxRanks; ++sp2)
-                part[sp2] = sp2 < s ? __ldg(cnt + static_cast<int64_t>(sp2) * E + v) : 0;
-#pragma unroll
-            for (int sp2 = 0; sp2 < kMaxRanks; ++sp2) begin += part[sp2];
+            i_last = i < n ? i : -1;
+            e_last = e;
+            p_last = p;
         }
-        if (begin + pos < slots) row = static_cast<int32_t>(begin + pos);
+        __syncthreads();
     }
-    *sp = row;
+
+    // 2. publish the counts
+    for (int e = tid; e < E; e += kThreads) counts[static_cast<int64_t>(s) * E + e] = static_cast<uint32_t>(s_run[e]);
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) st_release_u32(states + s, tag | kLLPublished);
+
+    // 3. the earlier sources' counts: lane s' of warp 0 waits for source s', then the sums, with
+    //    kThreads / E threads per expert (each adds every parts-th source) while E < kThreads
+    if (warp == 0) {
+        const bool ok = lane >= s || ll_wait_word(states + lane, tag | kLLPublished);
+        if (!__all_sync(kFullMask, ok) && lane == 0) s_ok = 0;
+    }
+    __syncthreads();
+    const bool ok = s_ok != 0;
+    if (ok && s > 0) {
+        const int parts = E < kThreads ? kThreads / E : 1;
+        for (int w = tid; w < parts * E; w += kThreads) {
+            const int e = w % E, part = w / E;
+            int32_t sum = 0;
+#pragma unroll 4
+            for (int sp = part; sp < s; sp += parts)
+                sum += static_cast<int32_t>(__ldcg(counts + static_cast<int64_t>(sp) * E + e));
+            if (sum) atomicAdd(&s_begin[e], sum);
+        }
+    }
+    __syncthreads();
+
+    // 4. rows, layout ranges and, for the last source, the per-expert totals
+    if (ok) {
+        if (i_last >= 0) {
+            int32_t row = -1;
+            if (e_last >= 0 && static_cast<int64_t>(s_begin[e_last]) + p_last < slots) row = s_begin[e_last] + p_last;
+            slot_s[i_last] = row;
+        }
+        const int64_t n_early = n > 0 ? ((n - 1) / kThreads) * kThreads : 0;  // slots of the earlier chunks
+        for (int64_t i = tid; i < n_early; i += kThreads) {
+            const int32_t p = slot_s[i];
+            int32_t row = -1;
+            if (p >= 0) {
+                const int e = static_cast<int>(__ldg(idx_s + i));  // a valid, unmasked expert (p >= 0)
+                if (static_cast<int64_t>(s_begin[e]) + p < slots) row = s_begin[e] + p;
+            }
+            slot_s[i] = row;
+        }
+        for (int e = tid; e < E; e += kThreads) {
+            const int32_t c = s_run[e], b = s_begin[e];
+            layout_range[static_cast<int64_t>(e) * R + s] =
+                static_cast<int64_t>((static_cast<uint64_t>(static_cast<uint32_t>(c)) << 32) | static_cast<uint32_t>(b));
+            if (s == R - 1) {
+                const int64_t total = static_cast<int64_t>(b) + c;
+                if (total > slots) report(status, EP_ERR_CAPACITY);
+                const int32_t cnt = static_cast<int32_t>(total < slots ? total : slots);
+                packed_recv_count[e] = cnt;
+                if (stats != nullptr) stats[e] += cnt;
+            }
+        }
+    } else if (tid == 0) {
+        report(status, EP_ERR_TIMEOUT);
+    }
+
+    // the last CTA to finish: the next launch's tickets and epoch
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) s_last = atomicAdd(scratch + 1, 1u) == gridDim.x - 1u;
+    __syncthreads();
+    if (s_last && tid == 0) {
+        scratch[0] = 0u;
+        scratch[1] = 0u;
+        __threadfence();
+        st_release_u32(scratch + 2, s_epoch + 1u);
+    }
 }
 
 // Bulk-copy low-latency dispatch: CTA b takes the contiguous tokens [b * per_cta,
@@ -563,16 +599,16 @@ int clamp_grid(int planned, int64_t warps_needed, int warps_per_block) {
     return static_cast<int>(need < planned ? (need > 0 ? need : 1) : planned);
 }
 
-size_t ll_count_smem(int E, int threads) {
-    return sizeof(int32_t) * static_cast<size_t>(threads / kWarpSize + 1) * E;
+size_t ll_meta_smem(int E, int threads) {
+    return sizeof(int32_t) * static_cast<size_t>(threads / kWarpSize + 2) * E;
 }
 
-constexpr size_t kLLCountMaxSmem = 200u * 1024u;
+constexpr size_t kLLMetaMaxSmem = 200u * 1024u;
 
 // One chunk of 1024 top-k entries per pass while the per-warp histograms fit in shared memory
-// (measured: 57.0 against 58.6 us per ll_v3 dispatch), else 512-thread passes.
-int ll_count_threads(int E) {
-    return ll_count_smem(E, kLLCountThreadsLarge) <= kLLCountMaxSmem ? kLLCountThreadsLarge : kLLCountThreads;
+// (with the two-kernel metadata: 57.0 against 58.6 us per ll_v3 dispatch), else 512-thread passes.
+int ll_meta_threads(int E) {
+    return ll_meta_smem(E, kLLMetaThreadsLarge) <= kLLMetaMaxSmem ? kLLMetaThreadsLarge : kLLMetaThreads;
 }
 
 }  // namespace
@@ -595,31 +631,26 @@ cudaError_t plan_ll(LaunchPlan* plan, int num_experts) {
     if (err != cudaSuccess) return err;
     // both block sizes may be chosen per call (the allocation-free entry point plans for the most
     // experts and launches with fewer), so both may use the whole budget
-    err = cudaFuncSetAttribute(ll_count_kernel<kLLCountThreadsLarge>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               static_cast<int>(kLLCountMaxSmem));
+    err = cudaFuncSetAttribute(ll_meta_kernel<kLLMetaThreadsLarge>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(kLLMetaMaxSmem));
     if (err != cudaSuccess) return err;
-    return cudaFuncSetAttribute(ll_count_kernel<kLLCountThreads>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                static_cast<int>(kLLCountMaxSmem));
+    return cudaFuncSetAttribute(ll_meta_kernel<kLLMetaThreads>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                static_cast<int>(kLLMetaMaxSmem));
 }
+
+size_t ll_meta_scratch_words(int R, int E) { return kLLMetaCounts + static_cast<size_t>(R) * E; }
 
 cudaError_t launch_ll_dispatch(const LaunchPlan& plan, int R, int T, int maxT, int H, int K, int E,
                                const void* x, const int64_t* topk_idx, bool use_fp8, bool round_scale,
-                               bool use_ue8m0, const int32_t* rank_mask, int32_t* slot, int32_t* cnt,
+                               bool use_ue8m0, const int32_t* rank_mask, int32_t* slot, uint32_t* meta_scratch,
                                void* recv_msgs, int32_t* packed_recv_count, int64_t* layout_range,
                                int32_t* stats, int32_t* status, cudaStream_t stream) {
-    const int count_threads = ll_count_threads(E);
-    auto count_kernel = count_threads == kLLCountThreadsLarge ? ll_count_kernel<kLLCountThreadsLarge>
-                                                              : ll_count_kernel<kLLCountThreads>;
-    cudaError_t err = launch_kernel(count_kernel, dim3(R), dim3(count_threads), ll_count_smem(E, count_threads), stream,
-                                    1, R, T, maxT, K, E, topk_idx, rank_mask, slot, cnt, status);
-    if (err != cudaSuccess) return err;
-    const int fin_threads = kFinishThreads;
-    const int expert_blocks = (E + fin_threads / kWarpSize - 1) / (fin_threads / kWarpSize);
-    const int64_t n_slots = static_cast<int64_t>(R) * T * K;
-    const int slot_blocks = static_cast<int>((n_slots + fin_threads - 1) / fin_threads);
-    err = launch_kernel(ll_finish_kernel, dim3(expert_blocks + slot_blocks), dim3(fin_threads), 0, stream, 1, R, T,
-                        maxT, K, E, expert_blocks, topk_idx, static_cast<const int32_t*>(cnt), slot,
-                        packed_recv_count, layout_range, stats, status);
+    const int meta_threads = ll_meta_threads(E);
+    auto meta_kernel = meta_threads == kLLMetaThreadsLarge ? ll_meta_kernel<kLLMetaThreadsLarge>
+                                                           : ll_meta_kernel<kLLMetaThreads>;
+    cudaError_t err = launch_kernel(meta_kernel, dim3(R), dim3(meta_threads), ll_meta_smem(E, meta_threads), stream, 1,
+                                    R, T, maxT, K, E, topk_idx, rank_mask, slot, packed_recv_count, layout_range, stats,
+                                    meta_scratch, status);
     if (err != cudaSuccess) return err;
     const int64_t n_tokens = static_cast<int64_t>(R) * T;
     if (n_tokens == 0) return cudaSuccess;
