@@ -72,15 +72,14 @@ cudaError_t launch_combine(const LaunchPlan& plan, bool out_fp32, int R, int T, 
                            const void* bias0, const void* bias1, void* out, float* combined_topk_weights,
                            uint32_t* work, cudaStream_t stream);
 
-// Scratch of the low-latency metadata kernel: words [0, 4) tickets / finished CTAs / epoch, [4, 4 + R)
-// per-source states, from kLLMetaCounts the per-source counts [R][E].  Zero before the first
-// launch; each launch leaves it ready for the next.  Launches sharing it must be ordered.
-constexpr int kLLMetaCounts = 64;
-size_t ll_meta_scratch_words(int R, int E);
+// Whether a low-latency dispatch with up to maxT tokens per rank may compute its slot rows in two
+// launches that pass per-(source, expert) counts through cnt (int32 [R][E] of device memory);
+// otherwise one launch computes them with no memory besides its outputs, and cnt is not used.
+bool ll_slots_use_counts(int R, int maxT, int K);
 
 cudaError_t launch_ll_dispatch(const LaunchPlan& plan, int R, int T, int maxT, int H, int K, int E,
                                const void* x, const int64_t* topk_idx, bool use_fp8, bool round_scale,
-                               bool use_ue8m0, const int32_t* rank_mask, int32_t* slot, uint32_t* meta_scratch,
+                               bool use_ue8m0, const int32_t* rank_mask, int32_t* slot, int32_t* cnt,
                                void* recv_msgs, int32_t* packed_recv_count, int64_t* layout_range,
                                int32_t* stats, int32_t* status, cudaStream_t stream);
 

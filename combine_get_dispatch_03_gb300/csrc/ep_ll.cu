@@ -8,12 +8,12 @@
 // rows of its expert e: recv_msgs[e][row] with e = d*EL + j.  The pages take a
 // slot with an atomicAdd on a per-expert counter, whose order depends on
 // timing; here the rows are fixed beforehand so the layout is deterministic:
-//   1. ll_meta (one CTA per source rank, one launch): stable rank of each slot
-//      among the slots of the same (source, expert), in (token, k) order, and
-//      the per-expert count; the begin of each source block = the counts of
-//      the earlier sources, which their CTAs publish (bounded waits); the final
-//      row of every slot, which stays in the handle for the combine;
-//      packed_recv_layout_range, and from the last source's CTA
+//   1. ll_meta (one CTA per source rank, one launch, no waits): the begin of
+//      the source's block in each expert = the earlier sources' slots routed
+//      to it, which the CTA counts itself; then the stable rank of each of its
+//      slots among the slots of the same (source, expert), in (token, k)
+//      order, which gives the final row of every slot (kept in the handle for
+//      the combine); packed_recv_layout_range, and from the last source's CTA
 //      packed_recv_count and the receive stats;
 //   2. ll_dispatch: read + cast the row once into a complete message in
 //      shared memory, then one bulk store per destination slot (a register
@@ -31,86 +31,99 @@ namespace ep {
 
 namespace {
 
-constexpr int kLLMetaThreadsLarge = 1024;  // the metadata kernel's block while its histograms fit in smem
+constexpr int kLLMetaThreadsLarge = 1024;  // the slot-row kernels' block while their histograms fit in smem
+constexpr int kFinishThreads = 256;
+// Most ids of earlier sources that one CTA of ll_meta reads (ll_v3: 31 x 1024); past this the two
+// launches of ll_count + ll_finish, whose work does not grow with the number of sources, serve.
+constexpr int64_t kLLMetaMaxPrefix = 65536;
 constexpr int kLLUnroll = 4;
 constexpr int kLLCombineUnroll = 2;
 constexpr int kLLCombineFanIn = 4;         // slots loaded together before accumulation
 constexpr int kLLCombineFanInSmallK = 8;   // ... with top-k up to 8: every slot in one batch
 
-// Per-source state word of the metadata kernel: the epoch tag (bits 2..31) and 1 once the
-// source's counts are published.
-constexpr uint32_t kLLPublished = 1;
-
-// All lanes of the calling warp: true once the word holds `want` (bounded wait).
-__device__ __forceinline__ bool ll_wait_word(const uint32_t* word, uint32_t want) {
-    for (uint32_t it = 0; it < kMaxWaitIterations; ++it)
-        if (ld_acquire_u32(word) == want) return true;
-    return false;
-}
-
-// The slot rows of every source in one launch, one CTA per source.  CTAs take their source by
-// ticket, so a CTA only ever waits for sources whose CTAs already started, and for source s:
-//   1. the stable position of each of its slots among the slots of the same (source, expert), in
-//      (token, k) order: per-warp histograms (__match_any_sync) and a prefix over the warps, one
-//      chunk of kThreads slots at a time; the counts cnt[s][e] come out of the same pass;
-//   2. publishes cnt[s][.] and its state word;
-//   3. waits (bounded) for the earlier sources' state words and sums their counts: begin[e][s];
-//   4. writes each slot's final row begin + position (-1 past the R * maxT rows of an expert),
-//      and packed_recv_layout_range[e][s]; the CTA of the last source also has every expert's
-//      total, so it writes packed_recv_count (and adds it to the receive stats).
-// Slots that start or end on a masked rank count as masked slots.  The state words carry the
-// launch's epoch (scratch word 2, advanced by the last CTA to finish, which also resets the
-// tickets), so states of an earlier launch never match and CUDA-graph replays need no reset.
+// The slot rows of every source in one launch, one CTA per source, with no wait on another CTA.
+// The rows of expert e are the valid slots routed to e in (source, token, k) order, so the row of
+// a slot of source s is (slots of the earlier sources routed to e) + (its position among the
+// slots of source s routed to e).  CTA s:
+//   1. counts the earlier sources' slots per expert itself (their ids are a contiguous prefix of
+//      topk_idx, read with 16-byte loads issued together): a shared-memory histogram that starts
+//      every expert's running counter at begin[e][s];
+//   2. walks its own slots in chunks of kThreads: per-warp histograms (__match_any_sync) and a
+//      prefix over the warps continue each expert's counter, which gives every slot its final
+//      row (-1 past the R * maxT rows of an expert);
+//   3. writes packed_recv_layout_range[e][s] = (count << 32) | begin; the CTA of the last source
+//      ends with every expert's total, so it writes packed_recv_count (and the receive stats).
+// Slots that start or end on a masked rank count as masked slots.  Every CTA reads the ids of the
+// sources before it: R^2 T K / 2 ids in all, against R T K for a count pass followed by a prefix
+// pass over sources, but with no second launch and no round trip through global memory between
+// CTAs -- which is what a low-latency dispatch of a few thousand tokens waits on.
 template <int kThreads>
 __global__ void __launch_bounds__(kThreads)
     ll_meta_kernel(int R, int T, int maxT, int K, int E, const int64_t* __restrict__ topk_idx,
                    const int32_t* __restrict__ rank_mask, int32_t* __restrict__ slot,
                    int32_t* __restrict__ packed_recv_count, int64_t* __restrict__ layout_range,
-                   int32_t* __restrict__ stats, uint32_t* __restrict__ scratch, int32_t* status) {
+                   int32_t* __restrict__ stats, int32_t* status) {
     pdl_enter();
     constexpr int kWarps = kThreads / kWarpSize;
     constexpr int kScanChunk = kWarps < 16 ? kWarps : 16;
+    constexpr int kPrefixUnroll = 8;  // 16-byte loads in flight per thread while counting earlier sources
     static_assert(kWarps % kScanChunk == 0, "whole scan chunks");
     extern __shared__ int32_t smem[];
     int32_t* s_warp = smem;               // [kWarps][E]: per-warp count -> exclusive prefix
-    int32_t* s_run = smem + kWarps * E;   // [E]: slots of this source seen so far -> cnt[s][.]
-    int32_t* s_begin = s_run + E;         // [E]: slots of the earlier sources
-    __shared__ int s_src, s_ok, s_last;
-    __shared__ uint32_t s_epoch;
+    int32_t* s_run = smem + kWarps * E;   // [E]: running row counter of each expert
+    int32_t* s_begin = s_run + E;         // [E]: begin[e][s]
+    const int s = blockIdx.x;
     const int tid = threadIdx.x;
     const int lane = lane_id();
     const int warp = tid / kWarpSize;
     const int64_t n = static_cast<int64_t>(T) * K;
     const int EL = E / R;
     const int64_t slots = static_cast<int64_t>(R) * maxT;
-    uint32_t* states = scratch + 4;
-    uint32_t* counts = scratch + kLLMetaCounts;
-
-    if (tid == 0) {
-        s_src = static_cast<int>(atomicAdd(scratch, 1u));
-        s_epoch = ld_acquire_u32(scratch + 2);
-        s_ok = 1;
-    }
-    // the first chunk of the source the ticket usually gives (blockIdx.x), loaded meanwhile
-    const int guess = static_cast<int>(blockIdx.x);
-    int64_t next = tid < n ? __ldg(topk_idx + guess * n + tid) : -1;
-    for (int e = tid; e < E; e += kThreads) {
-        s_run[e] = 0;
-        s_begin[e] = 0;
-    }
-    const uint32_t rmask = __ballot_sync(kFullMask, rank_mask != nullptr && lane < R && __ldg(rank_mask + lane) != 0);
-    __syncthreads();
-    const int s = s_src;
-    const uint32_t tag = (s_epoch & 0x3fffffffu) << 2;
-    if (s != guess) next = tid < n ? __ldg(topk_idx + s * n + tid) : -1;
     const int64_t* idx_s = topk_idx + s * n;
     int32_t* slot_s = slot + static_cast<int64_t>(s) * maxT * K;
-    const bool src_masked = (rmask >> s) & 1u;
 
-    // 1. positions within (source, expert) and the counts
-    int64_t i_last = -1;  // this thread's slot of the last chunk, kept in registers
-    int e_last = -1;
-    int32_t p_last = -1;
+    const uint32_t rmask = __ballot_sync(kFullMask, rank_mask != nullptr && lane < R && __ldg(rank_mask + lane) != 0);
+    const bool src_masked = (rmask >> s) & 1u;
+    int64_t next = tid < n ? __ldg(idx_s + tid) : -1;  // this source's first chunk, loaded ahead
+    for (int e = tid; e < E; e += kThreads) s_run[e] = 0;
+    __syncthreads();
+
+    // 1. the earlier sources: the first n * s ids of topk_idx, 2 per 16-byte load.  topk_idx is
+    //    8-byte aligned: when it is not 16-byte aligned its first id, and any odd last id, take a
+    //    plain load.
+    {
+        auto count_id = [&](int64_t f, int64_t v) {  // id v at flat position f (source f / n)
+            if (v >= 0 && v < E && !((rmask >> static_cast<int>(f / n)) & 1u) && !((rmask >> (v / EL)) & 1u))
+                atomicAdd(&s_run[v], 1);
+        };
+        const int64_t total = n * s;
+        const int64_t off = (reinterpret_cast<uintptr_t>(topk_idx) & 15u) ? 1 : 0;
+        const int64_t pairs = total > off ? (total - off) / 2 : 0;
+        const int4* p2 = reinterpret_cast<const int4*>(topk_idx + off);
+        for (int64_t b = tid; b < pairs; b += static_cast<int64_t>(kThreads) * kPrefixUnroll) {
+            int4 v[kPrefixUnroll];
+#pragma unroll
+            for (int u = 0; u < kPrefixUnroll; ++u) {
+                const int64_t q = b + static_cast<int64_t>(u) * kThreads;
+                v[u] = q < pairs ? __ldg(p2 + q) : make_int4(-1, -1, -1, -1);
+            }
+#pragma unroll
+            for (int u = 0; u < kPrefixUnroll; ++u) {
+                const int64_t q = b + static_cast<int64_t>(u) * kThreads;
+                if (q >= pairs) continue;
+                count_id(off + 2 * q, (static_cast<int64_t>(v[u].y) << 32) | static_cast<uint32_t>(v[u].x));
+                count_id(off + 2 * q + 1, (static_cast<int64_t>(v[u].w) << 32) | static_cast<uint32_t>(v[u].z));
+            }
+        }
+        if (tid == 0) {
+            if (off && total > 0) count_id(0, __ldg(topk_idx));
+            if (off + 2 * pairs < total) count_id(total - 1, __ldg(topk_idx + total - 1));
+        }
+    }
+    __syncthreads();
+    for (int e = tid; e < E; e += kThreads) s_begin[e] = s_run[e];
+
+    // 2. this source's slots: final rows
     for (int64_t base = 0; base < n; base += kThreads) {
         for (int i = tid; i < kWarps * E; i += kThreads) s_warp[i] = 0;
         __syncthreads();
@@ -123,6 +136,92 @@ __global__ void __launch_bounds__(kThreads)
             else if (v != -1) report(status, EP_ERR_BAD_EXPERT);
             // a masked rank neither sends nor receives
             if (e >= 0 && (src_masked || ((rmask >> (e / EL)) & 1u))) e = -1;
+        }
+        const unsigned peers = __match_any_sync(kFullMask, e);
+        const int before = __popc(peers & lanemask_lt());
+        if (e >= 0 && before == 0) s_warp[warp * E + e] = __popc(peers);
+        __syncthreads();
+        // per expert: exclusive prefix over the warps, continuing the running counter, in chunks of
+        // 16 whose loads are all issued before the stores (a load after a store to the same array
+        // would wait for it)
+        for (int x = tid; x < E; x += kThreads) {
+            int32_t run = s_run[x];
+#pragma unroll
+            for (int w0 = 0; w0 < kWarps; w0 += kScanChunk) {
+                int32_t c[kScanChunk];
+#pragma unroll
+                for (int u = 0; u < kScanChunk; ++u) c[u] = s_warp[(w0 + u) * E + x];
+#pragma unroll
+                for (int u = 0; u < kScanChunk; ++u) {
+                    s_warp[(w0 + u) * E + x] = run;
+                    run += c[u];
+                }
+            }
+            s_run[x] = run;
+        }
+        __syncthreads();
+        if (i < n) {
+            const int64_t row = e >= 0 ? static_cast<int64_t>(s_warp[warp * E + e]) + before : -1;
+            slot_s[i] = row >= 0 && row < slots ? static_cast<int32_t>(row) : -1;
+        }
+        __syncthreads();
+    }
+
+    // 3. layout ranges; the last source's CTA holds every expert's total
+    for (int e = tid; e < E; e += kThreads) {
+        const int32_t b = s_begin[e], c = s_run[e] - b;
+        layout_range[static_cast<int64_t>(e) * R + s] =
+            static_cast<int64_t>((static_cast<uint64_t>(static_cast<uint32_t>(c)) << 32) | static_cast<uint32_t>(b));
+        if (s == R - 1) {
+            const int64_t total = s_run[e];
+            if (total > slots) report(status, EP_ERR_CAPACITY);
+            const int32_t cnt = static_cast<int32_t>(total < slots ? total : slots);
+            packed_recv_count[e] = cnt;
+            if (stats != nullptr) stats[e] += cnt;
+        }
+    }
+}
+
+// For more ids than one CTA reads quickly (kLLMetaMaxPrefix), the slot rows take two launches
+// instead, each linear in the slots: ll_count (one CTA per source) writes each slot's position
+// within (source, expert) and the per-source counts to scratch; ll_finish sums the counts over
+// sources (one warp per expert) and turns every position into its final row.
+template <int kThreads>
+__global__ void __launch_bounds__(kThreads)
+    ll_count_kernel(int R, int T, int maxT, int K, int E, const int64_t* __restrict__ topk_idx,
+                    const int32_t* __restrict__ rank_mask, int32_t* __restrict__ slot, int32_t* __restrict__ cnt,
+                    int32_t* status) {
+    pdl_enter();
+    constexpr int kWarps = kThreads / kWarpSize;
+    constexpr int kScanChunk = kWarps < 16 ? kWarps : 16;
+    static_assert(kWarps % kScanChunk == 0, "whole scan chunks");
+    extern __shared__ int32_t smem[];
+    int32_t* s_warp = smem;                   // [kWarps][E]: per-warp count -> exclusive prefix
+    int32_t* s_run = smem + kWarps * E;  // [E]: slots of this source seen so far
+    const int s = blockIdx.x;
+    const int tid = threadIdx.x;
+    const int lane = lane_id();
+    const int warp = tid / kWarpSize;
+    const int n = T * K;
+    const int64_t* idx_s = topk_idx + static_cast<int64_t>(s) * T * K;
+    int32_t* slot_s = slot + static_cast<int64_t>(s) * maxT * K;
+
+    __shared__ int32_t s_mask[kMaxRanks];  // rank mask (0 everywhere without one)
+    for (int e = tid; e < E; e += kThreads) s_run[e] = 0;
+    if (tid < kMaxRanks) s_mask[tid] = rank_mask != nullptr && tid < R ? __ldg(rank_mask + tid) : 0;
+    int64_t next = tid < n ? __ldg(idx_s + tid) : -1;  // the next chunk's entry, loaded one chunk ahead
+    for (int base = 0; base < n; base += kThreads) {
+        for (int i = tid; i < kWarps * E; i += kThreads) s_warp[i] = 0;
+        __syncthreads();
+        const int i = base + tid;
+        const int64_t v = next;
+        if (base + kThreads + tid < n) next = __ldg(idx_s + base + kThreads + tid);
+        int e = -1;
+        if (i < n) {
+            if (v >= 0 && v < E) e = static_cast<int>(v);
+            else if (v != -1) report(status, EP_ERR_BAD_EXPERT);
+            // a masked rank neither sends nor receives
+            if (e >= 0 && (s_mask[s] != 0 || s_mask[e / (E / R)] != 0)) e = -1;
         }
         const unsigned peers = __match_any_sync(kFullMask, e);
         const int before = __popc(peers & lanemask_lt());
@@ -146,88 +245,102 @@ __global__ void __launch_bounds__(kThreads)
             s_run[x] = run;
         }
         __syncthreads();
-        const int32_t p = e >= 0 ? s_warp[warp * E + e] + before : -1;
-        if (base + kThreads < n) {
-            if (i < n) slot_s[i] = p;  // an earlier chunk: its position, turned into a row in step 4
-        } else {
-            i_last = i < n ? i : -1;
-            e_last = e;
-            p_last = p;
+        if (i < n) slot_s[i] = e >= 0 ? s_warp[warp * E + e] + before : -1;
+        __syncthreads();
+    }
+    for (int e = tid; e < E; e += kThreads) cnt[static_cast<int64_t>(s) * E + e] = s_run[e];
+}
+
+// Blocks [0, expert_blocks): one warp per expert e; lane s holds the count of
+// source s, a warp scan gives each source block's begin (R <= 32).  The other
+// blocks: one thread per top-k slot turns its position within (source, expert)
+// into the final row, begin(e, s) + position, or -1 past the R * maxT capacity.
+__global__ void ll_finish_kernel(int R, int T, int maxT, int K, int E, int expert_blocks,
+                                 const int64_t* __restrict__ topk_idx, const int32_t* __restrict__ cnt,
+                                 int32_t* __restrict__ slot, int32_t* __restrict__ packed_recv_count,
+                                 int64_t* __restrict__ layout_range, int32_t* __restrict__ stats, int32_t* status) {
+    pdl_enter();
+    const int64_t slots = static_cast<int64_t>(R) * maxT;
+    if (static_cast<int>(blockIdx.x) < expert_blocks) {
+        const int lane = lane_id();
+        const int warps = blockDim.x / kWarpSize;
+        const int e = blockIdx.x * warps + threadIdx.x / kWarpSize;
+        if (e >= E) return;
+        const int32_t c = lane < R ? __ldg(cnt + static_cast<int64_t>(lane) * E + e) : 0;
+        int32_t incl = c;
+#pragma unroll
+        for (int off = 1; off < kWarpSize; off <<= 1) {
+            const int32_t o = __shfl_up_sync(kFullMask, incl, off);
+            if (lane >= off) incl += o;
+        }
+        const int32_t begin = incl - c;
+        if (lane < R)
+            layout_range[static_cast<int64_t>(e) * R + lane] =
+                static_cast<int64_t>((static_cast<uint64_t>(static_cast<uint32_t>(c)) << 32) |
+                                     static_cast<uint32_t>(begin));
+        const int32_t total = __shfl_sync(kFullMask, incl, kWarpSize - 1);
+        if (lane == 0) {
+            if (total > slots) report(status, EP_ERR_CAPACITY);
+            const int32_t n = static_cast<int32_t>(total < slots ? total : slots);
+            packed_recv_count[e] = n;
+            if (stats != nullptr) stats[e] += n;
+        }
+        return;
+    }
+    const int64_t n_slots = static_cast<int64_t>(R) * T * K;
+    const int64_t i0 = static_cast<int64_t>(blockIdx.x - expert_blocks) * blockDim.x;
+    const int64_t i = i0 + threadIdx.x;
+    // With E <= blockDim and every slot of the CTA from one source, the CTA sums the begins of
+    // that source's blocks for all experts into shared memory while its slots' expert ids and
+    // positions load: loads that need no expert id, so a slot waits for one round of loads
+    // instead of two.
+    __shared__ int32_t s_begin[kFinishThreads];
+    const int64_t i_last = (i0 + blockDim.x < n_slots ? i0 + blockDim.x : n_slots) - 1;
+    const int s_first = static_cast<int>(i0 / (static_cast<int64_t>(T) * K));
+    const bool table = E <= static_cast<int>(blockDim.x) && i0 < n_slots &&
+                       s_first == static_cast<int>(i_last / (static_cast<int64_t>(T) * K));
+    const bool live = i < n_slots;
+    int s = 0;
+    int64_t v = -1;
+    int32_t pos = -1;
+    int32_t* sp = nullptr;
+    if (live) {
+        s = static_cast<int>(i / (static_cast<int64_t>(T) * K));
+        v = __ldg(topk_idx + i);
+        sp = slot + static_cast<int64_t>(s) * maxT * K + (i - static_cast<int64_t>(s) * T * K);
+        pos = *sp;
+    }
+    if (table) {
+        const int e = threadIdx.x;
+        if (e < E) {
+            int32_t part[kMaxRanks];
+#pragma unroll
+            for (int q = 0; q < kMaxRanks; ++q) part[q] = q < s_first ? __ldg(cnt + static_cast<int64_t>(q) * E + e) : 0;
+            int32_t b = 0;
+#pragma unroll
+            for (int q = 0; q < kMaxRanks; ++q) b += part[q];
+            s_begin[e] = b;
         }
         __syncthreads();
     }
-
-    // 2. publish the counts
-    for (int e = tid; e < E; e += kThreads) counts[static_cast<int64_t>(s) * E + e] = static_cast<uint32_t>(s_run[e]);
-    __threadfence();
-    __syncthreads();
-    if (tid == 0) st_release_u32(states + s, tag | kLLPublished);
-
-    // 3. the earlier sources' counts: lane s' of warp 0 waits for source s', then the sums, with
-    //    kThreads / E threads per expert (each adds every parts-th source) while E < kThreads
-    if (warp == 0) {
-        const bool ok = lane >= s || ll_wait_word(states + lane, tag | kLLPublished);
-        if (!__all_sync(kFullMask, ok) && lane == 0) s_ok = 0;
-    }
-    __syncthreads();
-    const bool ok = s_ok != 0;
-    if (ok && s > 0) {
-        const int parts = E < kThreads ? kThreads / E : 1;
-        for (int w = tid; w < parts * E; w += kThreads) {
-            const int e = w % E, part = w / E;
-            int32_t sum = 0;
-#pragma unroll 4
-            for (int sp = part; sp < s; sp += parts)
-                sum += static_cast<int32_t>(__ldcg(counts + static_cast<int64_t>(sp) * E + e));
-            if (sum) atomicAdd(&s_begin[e], sum);
+    if (!live) return;
+    int32_t row = -1;
+    if (v >= 0 && v < E && pos >= 0) {
+        int64_t begin = 0;
+        if (table) {
+            begin = s_begin[v];
+        } else {
+            // the counts of the earlier sources, all loads in flight at once (R <= kMaxRanks)
+            int32_t part[kMaxRanks];
+#pragma unroll
+            for (int sp2 = 0; sp2 < kMaxRanks; ++sp2)
+                part[sp2] = sp2 < s ? __ldg(cnt + static_cast<int64_t>(sp2) * E + v) : 0;
+#pragma unroll
+            for (int sp2 = 0; sp2 < kMaxRanks; ++sp2) begin += part[sp2];
         }
+        if (begin + pos < slots) row = static_cast<int32_t>(begin + pos);
     }
-    __syncthreads();
-
-    // 4. rows, layout ranges and, for the last source, the per-expert totals
-    if (ok) {
-        if (i_last >= 0) {
-            int32_t row = -1;
-            if (e_last >= 0 && static_cast<int64_t>(s_begin[e_last]) + p_last < slots) row = s_begin[e_last] + p_last;
-            slot_s[i_last] = row;
-        }
-        const int64_t n_early = n > 0 ? ((n - 1) / kThreads) * kThreads : 0;  // slots of the earlier chunks
-        for (int64_t i = tid; i < n_early; i += kThreads) {
-            const int32_t p = slot_s[i];
-            int32_t row = -1;
-            if (p >= 0) {
-                const int e = static_cast<int>(__ldg(idx_s + i));  // a valid, unmasked expert (p >= 0)
-                if (static_cast<int64_t>(s_begin[e]) + p < slots) row = s_begin[e] + p;
-            }
-            slot_s[i] = row;
-        }
-        for (int e = tid; e < E; e += kThreads) {
-            const int32_t c = s_run[e], b = s_begin[e];
-            layout_range[static_cast<int64_t>(e) * R + s] =
-                static_cast<int64_t>((static_cast<uint64_t>(static_cast<uint32_t>(c)) << 32) | static_cast<uint32_t>(b));
-            if (s == R - 1) {
-                const int64_t total = static_cast<int64_t>(b) + c;
-                if (total > slots) report(status, EP_ERR_CAPACITY);
-                const int32_t cnt = static_cast<int32_t>(total < slots ? total : slots);
-                packed_recv_count[e] = cnt;
-                if (stats != nullptr) stats[e] += cnt;
-            }
-        }
-    } else if (tid == 0) {
-        report(status, EP_ERR_TIMEOUT);
-    }
-
-    // the last CTA to finish: the next launch's tickets and epoch
-    __threadfence();
-    __syncthreads();
-    if (tid == 0) s_last = atomicAdd(scratch + 1, 1u) == gridDim.x - 1u;
-    __syncthreads();
-    if (s_last && tid == 0) {
-        scratch[0] = 0u;
-        scratch[1] = 0u;
-        __threadfence();
-        st_release_u32(scratch + 2, s_epoch + 1u);
-    }
+    *sp = row;
 }
 
 // Bulk-copy low-latency dispatch: CTA b takes the contiguous tokens [b * per_cta,
@@ -599,6 +712,7 @@ int clamp_grid(int planned, int64_t warps_needed, int warps_per_block) {
     return static_cast<int>(need < planned ? (need > 0 ? need : 1) : planned);
 }
 
+// ll_meta: [kWarps][E] + 2 [E]; ll_count: [kWarps][E] + [E]
 size_t ll_meta_smem(int E, int threads) {
     return sizeof(int32_t) * static_cast<size_t>(threads / kWarpSize + 2) * E;
 }
@@ -606,7 +720,7 @@ size_t ll_meta_smem(int E, int threads) {
 constexpr size_t kLLMetaMaxSmem = 200u * 1024u;
 
 // One chunk of 1024 top-k entries per pass while the per-warp histograms fit in shared memory
-// (with the two-kernel metadata: 57.0 against 58.6 us per ll_v3 dispatch), else 512-thread passes.
+// (measured on ll_count: 57.0 against 58.6 us per ll_v3 dispatch), else 512-thread passes.
 int ll_meta_threads(int E) {
     return ll_meta_smem(E, kLLMetaThreadsLarge) <= kLLMetaMaxSmem ? kLLMetaThreadsLarge : kLLMetaThreads;
 }
@@ -633,24 +747,49 @@ cudaError_t plan_ll(LaunchPlan* plan, int num_experts) {
     // experts and launches with fewer), so both may use the whole budget
     err = cudaFuncSetAttribute(ll_meta_kernel<kLLMetaThreadsLarge>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                static_cast<int>(kLLMetaMaxSmem));
+    if (err == cudaSuccess)
+        err = cudaFuncSetAttribute(ll_meta_kernel<kLLMetaThreads>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   static_cast<int>(kLLMetaMaxSmem));
+    if (err == cudaSuccess)
+        err = cudaFuncSetAttribute(ll_count_kernel<kLLMetaThreadsLarge>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   static_cast<int>(kLLMetaMaxSmem));
     if (err != cudaSuccess) return err;
-    return cudaFuncSetAttribute(ll_meta_kernel<kLLMetaThreads>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    return cudaFuncSetAttribute(ll_count_kernel<kLLMetaThreads>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 static_cast<int>(kLLMetaMaxSmem));
 }
 
-size_t ll_meta_scratch_words(int R, int E) { return kLLMetaCounts + static_cast<size_t>(R) * E; }
+bool ll_slots_use_counts(int R, int maxT, int K) {
+    return static_cast<int64_t>(R - 1) * maxT * K > kLLMetaMaxPrefix;
+}
+
 
 cudaError_t launch_ll_dispatch(const LaunchPlan& plan, int R, int T, int maxT, int H, int K, int E,
                                const void* x, const int64_t* topk_idx, bool use_fp8, bool round_scale,
-                               bool use_ue8m0, const int32_t* rank_mask, int32_t* slot, uint32_t* meta_scratch,
+                               bool use_ue8m0, const int32_t* rank_mask, int32_t* slot, int32_t* cnt,
                                void* recv_msgs, int32_t* packed_recv_count, int64_t* layout_range,
                                int32_t* stats, int32_t* status, cudaStream_t stream) {
-    const int meta_threads = ll_meta_threads(E);
-    auto meta_kernel = meta_threads == kLLMetaThreadsLarge ? ll_meta_kernel<kLLMetaThreadsLarge>
-                                                           : ll_meta_kernel<kLLMetaThreads>;
-    cudaError_t err = launch_kernel(meta_kernel, dim3(R), dim3(meta_threads), ll_meta_smem(E, meta_threads), stream, 1,
-                                    R, T, maxT, K, E, topk_idx, rank_mask, slot, packed_recv_count, layout_range, stats,
-                                    meta_scratch, status);
+    const int threads = ll_meta_threads(E);
+    cudaError_t err;
+    if (static_cast<int64_t>(R - 1) * T * K <= kLLMetaMaxPrefix) {
+        // one launch: each source's CTA counts the earlier sources' slots itself
+        auto meta_kernel = threads == kLLMetaThreadsLarge ? ll_meta_kernel<kLLMetaThreadsLarge>
+                                                          : ll_meta_kernel<kLLMetaThreads>;
+        err = launch_kernel(meta_kernel, dim3(R), dim3(threads), ll_meta_smem(E, threads), stream, 1, R, T, maxT, K, E,
+                            topk_idx, rank_mask, slot, packed_recv_count, layout_range, stats, status);
+    } else {
+        if (cnt == nullptr) return cudaErrorInvalidValue;
+        auto count_kernel = threads == kLLMetaThreadsLarge ? ll_count_kernel<kLLMetaThreadsLarge>
+                                                           : ll_count_kernel<kLLMetaThreads>;
+        err = launch_kernel(count_kernel, dim3(R), dim3(threads), ll_meta_smem(E, threads) - sizeof(int32_t) * E,
+                            stream, 1, R, T, maxT, K, E, topk_idx, rank_mask, slot, cnt, status);
+        if (err != cudaSuccess) return err;
+        const int expert_blocks = (E + kFinishThreads / kWarpSize - 1) / (kFinishThreads / kWarpSize);
+        const int64_t n_slots = static_cast<int64_t>(R) * T * K;
+        const int slot_blocks = static_cast<int>((n_slots + kFinishThreads - 1) / kFinishThreads);
+        err = launch_kernel(ll_finish_kernel, dim3(expert_blocks + slot_blocks), dim3(kFinishThreads), 0, stream, 1, R,
+                            T, maxT, K, E, expert_blocks, topk_idx, static_cast<const int32_t*>(cnt), slot,
+                            packed_recv_count, layout_range, stats, status);
+    }
     if (err != cudaSuccess) return err;
     const int64_t n_tokens = static_cast<int64_t>(R) * T;
     if (n_tokens == 0) return cudaSuccess;

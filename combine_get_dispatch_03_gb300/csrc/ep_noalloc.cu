@@ -12,12 +12,12 @@
 // so no rank mask applies.
 //
 // The array lives in the library image, so every GPU that loads the library
-// holds its 64 KiB (plus 256 bytes of control words) until the process exits.
-// All calls on a device share it: two calls whose kernels overlap on the GPU
-// (different streams without an ordering between them) race on it.  Nothing
-// in it needs clearing between calls: the control words are zero when the
-// module loads and each launch leaves them ready for the next (the counts are
-// read only under a state word of the same launch).
+// holds its 64 KiB until the process exits.  All calls on a device share it:
+// two calls whose kernels overlap on the GPU (different streams without an
+// ordering between them) race on it.  Nothing in it needs clearing between
+// calls: the count kernel overwrites every entry that the later kernel reads.
+// The array is used only where the slot rows take two launches (more tokens
+// than the one-launch slot pass serves); smaller calls need no scratch.
 #include <mutex>
 
 #include "ep_common.cuh"
@@ -33,15 +33,13 @@ namespace {
 
 constexpr int64_t kScratchCounts = EP_LL_NOALLOC_MAX_COUNTS;  // int32 entries, R * E at most
 
-// The metadata kernel's control words (tickets, epoch, per-source states) and then the counts.
-// Zero when the module loads; every launch leaves the control words ready for the next one.
-static __device__ __align__(256) uint32_t g_ll_count_scratch[ep::kLLMetaCounts + kScratchCounts];
+static __device__ __align__(256) int32_t g_ll_count_scratch[kScratchCounts];
 
 constexpr int kMaxDevices = 64;
 
 struct DeviceSetup {
     bool ready = false;
-    uint32_t* scratch = nullptr;  // device address of g_ll_count_scratch on this device
+    int32_t* scratch = nullptr;  // device address of g_ll_count_scratch on this device
     ep::LaunchPlan plan;
 };
 
@@ -60,7 +58,7 @@ ep_status setup_device(int device, DeviceSetup** out) {
     std::lock_guard<std::mutex> lock(g_setup_mutex);
     DeviceSetup& s = g_setup[device];
     if (!s.ready) {
-        uint32_t* ptr = nullptr;
+        int32_t* ptr = nullptr;
         cudaError_t err = cudaGetSymbolAddress(reinterpret_cast<void**>(&ptr), g_ll_count_scratch);
         if (err != cudaSuccess) return reject(EP_ERR_CUDA, "cudaGetSymbolAddress of the low-latency count scratch failed");
         err = cudaDeviceGetAttribute(&s.plan.num_sms, cudaDevAttrMultiProcessorCount, device);

@@ -312,6 +312,10 @@ LL_CASES = [
     S("ll_r8_zipf", 8, 64, 2048, 64, 8, routing="zipf", mask_p=0.05, seed=32, max_tokens=64),
     S("ll_r32", 32, 12, 7168, 256, 8, seed=33, max_tokens=16),
     S("ll_r3_full", 3, 100, 512, 6, 2, seed=34, max_tokens=100),
+    # an odd number of slots per source (odd id prefixes for the one-launch slot pass)
+    S("ll_r5_odd", 5, 37, 512, 20, 3, routing="zipf", mask_p=0.1, seed=36, max_tokens=41),
+    # (R - 1) T K = 98304 ids past the one-launch slot pass's limit: the two-launch pass with counts
+    S("ll_r4_two_launch", 4, 4096, 512, 32, 8, mask_p=0.05, seed=35, max_tokens=4096),
 ]
 LL_FORMATS = ["bf16", "fp8", "fp8_round", "fp8_ue8m0"]
 
@@ -389,6 +393,25 @@ def test_ll_combine(shape):
     assert r["h"].status() == 0
     want = O.ll_combine(y_host, idx, w, r["ora"]["slot_row"], maxT, shape.E)
     np.testing.assert_array_equal(P.host(got), want)
+
+
+def test_ll_dispatch_with_8_byte_aligned_topk_idx():
+    """topk_idx needs only its natural 8-byte alignment: an offset view gives the same messages."""
+    shape = LL_CASES[2]
+    idx, _ = W.routing(shape)
+    x = W.tokens_x(shape)
+    flat = torch.full((idx.size + 1,), -1, dtype=torch.int64, device=P.DEV)
+    idx_d = flat[1:].view(idx.shape)
+    idx_d.copy_(torch.from_numpy(idx))
+    assert idx_d.data_ptr() % 16 == 8
+    h = ep.Handle(P.config_of(shape, 0))
+    out = ep.ep_ll_dispatch(h, x.to(P.DEV), idx_d, use_fp8=True, use_ue8m0=True)
+    assert h.status() == 0
+    ora = O.ll_dispatch(W.bf16_bits(x), idx, shape.max_tokens, shape.E, use_fp8=True, use_ue8m0=True)
+    np.testing.assert_array_equal(P.host(out["packed_recv_count"]), ora["packed_recv_count"])
+    np.testing.assert_array_equal(P.host(out["packed_recv_layout_range"]), ora["packed_recv_layout_range"])
+    np.testing.assert_array_equal(P.host(h.export("ll_slot_row"))[:, :shape.T], ora["slot_row"])
+    h.destroy()
 
 
 def test_ll_views():

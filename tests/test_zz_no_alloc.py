@@ -28,16 +28,18 @@ def host(t):
     return t.detach().cpu().numpy()
 
 
-# (R, maxT, H, E, K, calls): 16 ranks x 128 experts runs the metadata kernel's 1024-thread block;
-# 8 ranks x 2048 experts (R * E at the scratch's limit) its 512-thread block, whose shared-memory
-# size the first call's set-up plans for the most experts
+# (R, maxT, H, E, K, calls): 16 ranks x 128 experts run the slot pass's 1024-thread block; 8 ranks x
+# 2048 experts (R * E at the scratch's limit) its 512-thread block, whose shared-memory size the
+# first call's set-up plans for the most experts; 4 ranks x 4096 tokens x top-8 take the two-launch
+# slot pass, whose counts live in the fixed array (first call), then 2000 tokens the one-launch pass
 CASES = [
     (16, 48, 2048, 128, 8, [dict(T=48, fmt=(1, 1, 1), seed=501, mask=0.05), dict(T=37, fmt=(1, 0, 0), seed=502, mask=0.0)]),
     (8, 8, 512, 2048, 8, [dict(T=8, fmt=(1, 1, 1), seed=503, mask=0.05), dict(T=5, fmt=(0, 0, 0), seed=504, mask=0.1)]),
+    (4, 4096, 512, 32, 8, [dict(T=4096, fmt=(1, 1, 1), seed=505, mask=0.05), dict(T=2000, fmt=(1, 0, 0), seed=506, mask=0.0)]),
 ]
 
 
-@pytest.mark.parametrize("R,maxT,H,E,K,calls", CASES, ids=["r16_e128", "r8_e2048"])
+@pytest.mark.parametrize("R,maxT,H,E,K,calls", CASES, ids=["r16_e128", "r8_e2048", "r4_t4096"])
 def test_noalloc_matches_handle_dispatch_on_two_calls(R, maxT, H, E, K, calls):
     dev = torch.device("cuda", torch.cuda.current_device())
     stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
