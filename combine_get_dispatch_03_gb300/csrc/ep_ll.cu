@@ -85,39 +85,53 @@ __global__ void __launch_bounds__(kThreads)
     const uint32_t rmask = __ballot_sync(kFullMask, rank_mask != nullptr && lane < R && __ldg(rank_mask + lane) != 0);
     const bool src_masked = (rmask >> s) & 1u;
     int64_t next = tid < n ? __ldg(idx_s + tid) : -1;  // this source's first chunk, loaded ahead
-    for (int e = tid; e < E; e += kThreads) s_run[e] = 0;
-    __syncthreads();
 
-    // 1. the earlier sources: the first n * s ids of topk_idx, 2 per 16-byte load.  topk_idx is
-    //    8-byte aligned: when it is not 16-byte aligned its first id, and any odd last id, take a
-    //    plain load.
+    // 1. the earlier sources: the first n * s ids of topk_idx, 2 per 16-byte load, counted into one
+    //    histogram row per warp (one shared-memory atomic per distinct expert of the warp's ids,
+    //    __match_any_sync), then the rows are summed.  topk_idx is 8-byte aligned: when it is not
+    //    16-byte aligned its first id, and any odd last id, take a plain load.
     {
-        auto count_id = [&](int64_t f, int64_t v) {  // id v at flat position f (source f / n)
-            if (v >= 0 && v < E && !((rmask >> static_cast<int>(f / n)) & 1u) && !((rmask >> (v / EL)) & 1u))
-                atomicAdd(&s_run[v], 1);
+        for (int i = tid; i < kWarps * E; i += kThreads) s_warp[i] = 0;
+        __syncthreads();
+        int32_t* row = s_warp + warp * E;
+        const unsigned lt = lanemask_lt();
+        auto count_id = [&](bool live, int64_t f, int64_t v) {  // id v at flat position f (source f / n)
+            int e = -1;
+            if (live && v >= 0 && v < E && !((rmask >> static_cast<int>(f / n)) & 1u) && !((rmask >> (v / EL)) & 1u))
+                e = static_cast<int>(v);
+            const unsigned peers = __match_any_sync(kFullMask, e);  // every lane of the warp takes part
+            if (e >= 0 && (peers & lt) == 0) atomicAdd(&row[e], __popc(peers));
         };
         const int64_t total = n * s;
         const int64_t off = (reinterpret_cast<uintptr_t>(topk_idx) & 15u) ? 1 : 0;
         const int64_t pairs = total > off ? (total - off) / 2 : 0;
         const int4* p2 = reinterpret_cast<const int4*>(topk_idx + off);
-        for (int64_t b = tid; b < pairs; b += static_cast<int64_t>(kThreads) * kPrefixUnroll) {
+        const int64_t per_round = static_cast<int64_t>(kThreads) * kPrefixUnroll;
+        for (int64_t b = 0; b < pairs; b += per_round) {  // the same trip count for every thread
             int4 v[kPrefixUnroll];
 #pragma unroll
             for (int u = 0; u < kPrefixUnroll; ++u) {
-                const int64_t q = b + static_cast<int64_t>(u) * kThreads;
+                const int64_t q = b + static_cast<int64_t>(u) * kThreads + tid;
                 v[u] = q < pairs ? __ldg(p2 + q) : make_int4(-1, -1, -1, -1);
             }
 #pragma unroll
             for (int u = 0; u < kPrefixUnroll; ++u) {
-                const int64_t q = b + static_cast<int64_t>(u) * kThreads;
-                if (q >= pairs) continue;
-                count_id(off + 2 * q, (static_cast<int64_t>(v[u].y) << 32) | static_cast<uint32_t>(v[u].x));
-                count_id(off + 2 * q + 1, (static_cast<int64_t>(v[u].w) << 32) | static_cast<uint32_t>(v[u].z));
+                const int64_t q = b + static_cast<int64_t>(u) * kThreads + tid;
+                count_id(q < pairs, off + 2 * q, (static_cast<int64_t>(v[u].y) << 32) | static_cast<uint32_t>(v[u].x));
+                count_id(q < pairs, off + 2 * q + 1, (static_cast<int64_t>(v[u].w) << 32) | static_cast<uint32_t>(v[u].z));
             }
         }
-        if (tid == 0) {
-            if (off && total > 0) count_id(0, __ldg(topk_idx));
-            if (off + 2 * pairs < total) count_id(total - 1, __ldg(topk_idx + total - 1));
+        if (warp == 0) {
+            count_id(lane == 0 && off && total > 0, 0, lane == 0 && off && total > 0 ? __ldg(topk_idx) : -1);
+            const bool odd = lane == 0 && off + 2 * pairs < total;
+            count_id(odd, total - 1, odd ? __ldg(topk_idx + total - 1) : -1);
+        }
+        __syncthreads();
+        for (int x = tid; x < E; x += kThreads) {
+            int32_t sum = 0;
+#pragma unroll 8
+            for (int w = 0; w < kWarps; ++w) sum += s_warp[w * E + x];
+            s_run[x] = sum;
         }
     }
     __syncthreads();
