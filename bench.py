@@ -677,17 +677,21 @@ def measure_launch_model(ep, dev, peak, st, reps=10, probe_sms=(16, 32)):
                              "combine_vs_full_gpu": round(c_full / c_ms, 3)}}
 
 
-def run_ll_calls(n, small=False):
+def run_ll_calls(n, small=False, hidden=0):
     """The low-latency path of ll_v3 alone, n dispatches then n combines back to back (a short, fixed
     launch sequence for profilers); prints the CUDA-event time per call.  small: 8 ranks, 16 experts,
     1024 tokens per rank -- the combine still reads 940 MB of rows (more than L2) while the expert
-    output buffer holds 1.9 GB instead of ll_v3's 15 GB (for captures that save device memory)."""
+    output buffer holds 1.9 GB instead of ll_v3's 15 GB (for captures that save device memory).
+    hidden: ll_v3's routing with this hidden size (the slot-row kernels do not depend on it; at 512
+    the buffers hold 1.6 GB)."""
     from combine_get_dispatch_03_gb300 import ep
     dev = torch.device("cuda", 0)
     shape = W.WORKLOADS["ll_v3"]
     if small:
         shape = W.Shape("ll_v3_small", R=8, T=1024, H=shape.H, E=16, K=shape.K, routing=shape.routing,
                         max_tokens=1024, seed=shape.seed)
+    if hidden:
+        shape = W.Shape(**{**shape.__dict__, "H": hidden})
     idx, w = W.routing(shape)
     idx_d, w_d = torch.from_numpy(idx).to(dev), torch.from_numpy(w).to(dev)
     x_d = W.tokens_x(shape, device=dev)
@@ -1186,6 +1190,8 @@ def main():
                     help="only run the ll_v3 low-latency dispatch and combine this many times each (profiling)")
     ap.add_argument("--ll-small", action="store_true",
                     help="with --ll-calls: 8 ranks, 16 experts, 1024 tokens per rank instead of ll_v3")
+    ap.add_argument("--ll-hidden", type=int, default=0,
+                    help="with --ll-calls: this hidden size instead of 7168 (a multiple of 512)")
     ap.add_argument("--fp8-calls", type=int, default=0,
                     help="only run the fp8_zipf FP8 dispatch (fresh record, cast) this many times (profiling)")
     ap.add_argument("--fp8-input", action="store_true",
@@ -1200,7 +1206,7 @@ def main():
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     if args.ll_calls:
-        run_ll_calls(args.ll_calls, args.ll_small)
+        run_ll_calls(args.ll_calls, args.ll_small, args.ll_hidden)
     elif args.fp8_calls:
         run_fp8_calls(args.fp8_calls, args.tokens, args.fp8_input)
     elif args.impl == "reference":

@@ -35,8 +35,7 @@ struct ep_handle {
     int32_t* recv_src_idx = nullptr;         // [R][cap]
     int32_t* send_head = nullptr;            // [R][maxT][R]
     int32_t* ll_slot = nullptr;              // [R][maxT][K]
-    int32_t* ll_cnt = nullptr;               // [R][E] low-latency per-(source, expert) counts, when
-                                             // ll_slots_use_counts (else not allocated)
+    int32_t* ll_cnt = nullptr;               // [R][E]
     int32_t* rank_mask = nullptr;            // [R], nonzero = masked
     int32_t* rdma_channel_prefix = nullptr;    // [R][NN][C], NN = R / 8 whole nodes (see has_nodes)
     int32_t* recv_rdma_rank_prefix = nullptr;  // [R][NN]
@@ -196,12 +195,10 @@ ep_status ep_handle_create(const ep_config* cfg, ep_handle** out) {
     }
 
     const size_t R = cfg->num_ranks, C = cfg->num_channels, T = cfg->num_max_tokens, K = cfg->num_topk;
-    const size_t cap = static_cast<size_t>(cfg->recv_capacity);
+    const size_t E = cfg->num_experts, cap = static_cast<size_t>(cfg->recv_capacity);
     const size_t NN = (R + 7) / 8;
     const size_t scan_words = ep::layout_scan_scratch_words(cfg->num_ranks, cfg->num_experts, cfg->num_max_tokens);
-    const size_t ll_words = ep::ll_slots_use_counts(cfg->num_ranks, cfg->num_max_tokens, cfg->num_topk)
-                                ? static_cast<size_t>(cfg->num_ranks) * cfg->num_experts : 0;
-    const size_t sizes[] = {1, R * R, R * R * C, R * R * C, R, R * cap, R * T * R, R * T * K, ll_words, R,
+    const size_t sizes[] = {1, R * R, R * R * C, R * R * C, R, R * cap, R * T * R, R * T * K, R * E, R,
                             R * NN * C, R * NN, 2, scan_words};
     int32_t** slots[] = {&h->status,   &h->rank_prefix,  &h->channel_prefix, &h->recv_channel_prefix,
                          &h->num_recv, &h->recv_src_idx, &h->send_head,      &h->ll_slot,
@@ -549,8 +546,7 @@ ep_status ep_ll_dispatch(ep_handle* h, int32_t num_tokens, const void* x, const 
     DeviceGuard guard(h->device);
     cudaError_t err = ep::launch_ll_dispatch(h->plan, c.num_ranks, num_tokens, c.num_max_tokens, c.hidden, c.num_topk,
                                              c.num_experts, x, topk_idx, use_fp8 != 0, round_scale != 0,
-                                             use_ue8m0 != 0, h->rank_mask, h->ll_slot, h->ll_cnt, recv_msgs,
-                                             packed_recv_count,
+                                             use_ue8m0 != 0, h->rank_mask, h->ll_slot, h->ll_cnt, recv_msgs, packed_recv_count,
                                              packed_recv_layout_range, cumulative_local_expert_recv_stats, h->status,
                                              stream);
     if (err != cudaSuccess) return cuda_fail(err, "low-latency dispatch launch");

@@ -26,7 +26,7 @@ constexpr int kLayoutThreads = 1024;
 constexpr int kNotifyThreads = 1024;
 constexpr int kDispatchThreads = 512;
 constexpr int kCombineThreads = 256;
-constexpr int kLLMetaThreads = 512;  // the low-latency metadata kernel's block when E is large
+constexpr int kLLCountThreads = 512;
 constexpr int kLLDispatchThreads = 512;
 constexpr int kLLCombineThreads = 256;
 
@@ -71,11 +71,6 @@ cudaError_t launch_combine(const LaunchPlan& plan, bool out_fp32, int R, int T, 
                            const int32_t* send_head, const void* y, const float* recv_topk_weights,
                            const void* bias0, const void* bias1, void* out, float* combined_topk_weights,
                            uint32_t* work, cudaStream_t stream);
-
-// Whether a low-latency dispatch with up to maxT tokens per rank may compute its slot rows in two
-// launches that pass per-(source, expert) counts through cnt (int32 [R][E] of device memory);
-// otherwise one launch computes them with no memory besides its outputs, and cnt is not used.
-bool ll_slots_use_counts(int R, int maxT, int K);
 
 cudaError_t launch_ll_dispatch(const LaunchPlan& plan, int R, int T, int maxT, int H, int K, int E,
                                const void* x, const int64_t* topk_idx, bool use_fp8, bool round_scale,

@@ -8,14 +8,13 @@
 // rows of its expert e: recv_msgs[e][row] with e = d*EL + j.  The pages take a
 // slot with an atomicAdd on a per-expert counter, whose order depends on
 // timing; here the rows are fixed beforehand so the layout is deterministic:
-//   1. ll_meta (one CTA per source rank, one launch, no waits): the begin of
-//      the source's block in each expert = the earlier sources' slots routed
-//      to it, which the CTA counts itself; then the stable rank of each of its
-//      slots among the slots of the same (source, expert), in (token, k)
-//      order, which gives the final row of every slot (kept in the handle for
-//      the combine); packed_recv_layout_range, and from the last source's CTA
-//      packed_recv_count and the receive stats;
-//   2. ll_dispatch: read + cast the row once into a complete message in
+//   1. ll_count (one CTA per source rank): stable rank of each slot among the
+//      slots of the same (source, expert), in (token, k) order, and the count;
+//   2. ll_finish: begin of each source block = prefix over sources (one warp
+//      per expert); packed_recv_count, packed_recv_layout_range, receive
+//      stats; and the final row of every slot, which stays in the handle for
+//      the combine;
+//   3. ll_dispatch: read + cast the row once into a complete message in
 //      shared memory, then one bulk store per destination slot (a register
 //      kernel, one warp per token, serves messages too long to stage).
 // LL combine (§4.3): one warp per token gathers its K expert outputs and
@@ -31,175 +30,13 @@ namespace ep {
 
 namespace {
 
-constexpr int kLLMetaThreadsLarge = 1024;  // the slot-row kernels' block while their histograms fit in smem
+constexpr int kLLCountThreadsLarge = 1024;  // the count kernel's block while its histograms fit in smem
 constexpr int kFinishThreads = 256;
-// Most ids of earlier sources that one CTA of ll_meta reads (ll_v3: 31 x 1024); past this the two
-// launches of ll_count + ll_finish, whose work does not grow with the number of sources, serve.
-constexpr int64_t kLLMetaMaxPrefix = 65536;
 constexpr int kLLUnroll = 4;
 constexpr int kLLCombineUnroll = 2;
 constexpr int kLLCombineFanIn = 4;         // slots loaded together before accumulation
 constexpr int kLLCombineFanInSmallK = 8;   // ... with top-k up to 8: every slot in one batch
 
-// The slot rows of every source in one launch, one CTA per source, with no wait on another CTA.
-// The rows of expert e are the valid slots routed to e in (source, token, k) order, so the row of
-// a slot of source s is (slots of the earlier sources routed to e) + (its position among the
-// slots of source s routed to e).  CTA s:
-//   1. counts the earlier sources' slots per expert itself (their ids are a contiguous prefix of
-//      topk_idx, read with 16-byte loads issued together): a shared-memory histogram that starts
-//      every expert's running counter at begin[e][s];
-//   2. walks its own slots in chunks of kThreads: per-warp histograms (__match_any_sync) and a
-//      prefix over the warps continue each expert's counter, which gives every slot its final
-//      row (-1 past the R * maxT rows of an expert);
-//   3. writes packed_recv_layout_range[e][s] = (count << 32) | begin; the CTA of the last source
-//      ends with every expert's total, so it writes packed_recv_count (and the receive stats).
-// Slots that start or end on a masked rank count as masked slots.  Every CTA reads the ids of the
-// sources before it: R^2 T K / 2 ids in all, against R T K for a count pass followed by a prefix
-// pass over sources, but with no second launch and no round trip through global memory between
-// CTAs -- which is what a low-latency dispatch of a few thousand tokens waits on.
-template <int kThreads>
-__global__ void __launch_bounds__(kThreads)
-    ll_meta_kernel(int R, int T, int maxT, int K, int E, const int64_t* __restrict__ topk_idx,
-                   const int32_t* __restrict__ rank_mask, int32_t* __restrict__ slot,
-                   int32_t* __restrict__ packed_recv_count, int64_t* __restrict__ layout_range,
-                   int32_t* __restrict__ stats, int32_t* status) {
-    pdl_enter();
-    constexpr int kWarps = kThreads / kWarpSize;
-    constexpr int kScanChunk = kWarps < 16 ? kWarps : 16;
-    constexpr int kPrefixUnroll = 8;  // 16-byte loads in flight per thread while counting earlier sources
-    static_assert(kWarps % kScanChunk == 0, "whole scan chunks");
-    extern __shared__ int32_t smem[];
-    int32_t* s_warp = smem;               // [kWarps][E]: per-warp count -> exclusive prefix
-    int32_t* s_run = smem + kWarps * E;   // [E]: running row counter of each expert
-    int32_t* s_begin = s_run + E;         // [E]: begin[e][s]
-    const int s = blockIdx.x;
-    const int tid = threadIdx.x;
-    const int lane = lane_id();
-    const int warp = tid / kWarpSize;
-    const int64_t n = static_cast<int64_t>(T) * K;
-    const int EL = E / R;
-    const int64_t slots = static_cast<int64_t>(R) * maxT;
-    const int64_t* idx_s = topk_idx + s * n;
-    int32_t* slot_s = slot + static_cast<int64_t>(s) * maxT * K;
-
-    const uint32_t rmask = __ballot_sync(kFullMask, rank_mask != nullptr && lane < R && __ldg(rank_mask + lane) != 0);
-    const bool src_masked = (rmask >> s) & 1u;
-    int64_t next = tid < n ? __ldg(idx_s + tid) : -1;  // this source's first chunk, loaded ahead
-
-    // 1. the earlier sources: the first n * s ids of topk_idx, 2 per 16-byte load, counted into one
-    //    histogram row per warp (one shared-memory atomic per distinct expert of the warp's ids,
-    //    __match_any_sync), then the rows are summed.  topk_idx is 8-byte aligned: when it is not
-    //    16-byte aligned its first id, and any odd last id, take a plain load.
-    {
-        for (int i = tid; i < kWarps * E; i += kThreads) s_warp[i] = 0;
-        __syncthreads();
-        int32_t* row = s_warp + warp * E;
-        const unsigned lt = lanemask_lt();
-        auto count_id = [&](bool live, int64_t f, int64_t v) {  // id v at flat position f (source f / n)
-            int e = -1;
-            if (live && v >= 0 && v < E && !((rmask >> static_cast<int>(f / n)) & 1u) && !((rmask >> (v / EL)) & 1u))
-                e = static_cast<int>(v);
-            const unsigned peers = __match_any_sync(kFullMask, e);  // every lane of the warp takes part
-            if (e >= 0 && (peers & lt) == 0) atomicAdd(&row[e], __popc(peers));
-        };
-        const int64_t total = n * s;
-        const int64_t off = (reinterpret_cast<uintptr_t>(topk_idx) & 15u) ? 1 : 0;
-        const int64_t pairs = total > off ? (total - off) / 2 : 0;
-        const int4* p2 = reinterpret_cast<const int4*>(topk_idx + off);
-        const int64_t per_round = static_cast<int64_t>(kThreads) * kPrefixUnroll;
-        for (int64_t b = 0; b < pairs; b += per_round) {  // the same trip count for every thread
-            int4 v[kPrefixUnroll];
-#pragma unroll
-            for (int u = 0; u < kPrefixUnroll; ++u) {
-                const int64_t q = b + static_cast<int64_t>(u) * kThreads + tid;
-                v[u] = q < pairs ? __ldg(p2 + q) : make_int4(-1, -1, -1, -1);
-            }
-#pragma unroll
-            for (int u = 0; u < kPrefixUnroll; ++u) {
-                const int64_t q = b + static_cast<int64_t>(u) * kThreads + tid;
-                count_id(q < pairs, off + 2 * q, (static_cast<int64_t>(v[u].y) << 32) | static_cast<uint32_t>(v[u].x));
-                count_id(q < pairs, off + 2 * q + 1, (static_cast<int64_t>(v[u].w) << 32) | static_cast<uint32_t>(v[u].z));
-            }
-        }
-        if (warp == 0) {
-            count_id(lane == 0 && off && total > 0, 0, lane == 0 && off && total > 0 ? __ldg(topk_idx) : -1);
-            const bool odd = lane == 0 && off + 2 * pairs < total;
-            count_id(odd, total - 1, odd ? __ldg(topk_idx + total - 1) : -1);
-        }
-        __syncthreads();
-        for (int x = tid; x < E; x += kThreads) {
-            int32_t sum = 0;
-#pragma unroll 8
-            for (int w = 0; w < kWarps; ++w) sum += s_warp[w * E + x];
-            s_run[x] = sum;
-        }
-    }
-    __syncthreads();
-    for (int e = tid; e < E; e += kThreads) s_begin[e] = s_run[e];
-
-    // 2. this source's slots: final rows
-    for (int64_t base = 0; base < n; base += kThreads) {
-        for (int i = tid; i < kWarps * E; i += kThreads) s_warp[i] = 0;
-        __syncthreads();
-        const int64_t i = base + tid;
-        const int64_t v = next;
-        if (base + kThreads + tid < n) next = __ldg(idx_s + base + kThreads + tid);
-        int e = -1;
-        if (i < n) {
-            if (v >= 0 && v < E) e = static_cast<int>(v);
-            else if (v != -1) report(status, EP_ERR_BAD_EXPERT);
-            // a masked rank neither sends nor receives
-            if (e >= 0 && (src_masked || ((rmask >> (e / EL)) & 1u))) e = -1;
-        }
-        const unsigned peers = __match_any_sync(kFullMask, e);
-        const int before = __popc(peers & lanemask_lt());
-        if (e >= 0 && before == 0) s_warp[warp * E + e] = __popc(peers);
-        __syncthreads();
-        // per expert: exclusive prefix over the warps, continuing the running counter, in chunks of
-        // 16 whose loads are all issued before the stores (a load after a store to the same array
-        // would wait for it)
-        for (int x = tid; x < E; x += kThreads) {
-            int32_t run = s_run[x];
-#pragma unroll
-            for (int w0 = 0; w0 < kWarps; w0 += kScanChunk) {
-                int32_t c[kScanChunk];
-#pragma unroll
-                for (int u = 0; u < kScanChunk; ++u) c[u] = s_warp[(w0 + u) * E + x];
-#pragma unroll
-                for (int u = 0; u < kScanChunk; ++u) {
-                    s_warp[(w0 + u) * E + x] = run;
-                    run += c[u];
-                }
-            }
-            s_run[x] = run;
-        }
-        __syncthreads();
-        if (i < n) {
-            const int64_t row = e >= 0 ? static_cast<int64_t>(s_warp[warp * E + e]) + before : -1;
-            slot_s[i] = row >= 0 && row < slots ? static_cast<int32_t>(row) : -1;
-        }
-        __syncthreads();
-    }
-
-    // 3. layout ranges; the last source's CTA holds every expert's total
-    for (int e = tid; e < E; e += kThreads) {
-        const int32_t b = s_begin[e], c = s_run[e] - b;
-        layout_range[static_cast<int64_t>(e) * R + s] =
-            static_cast<int64_t>((static_cast<uint64_t>(static_cast<uint32_t>(c)) << 32) | static_cast<uint32_t>(b));
-        if (s == R - 1) {
-            const int64_t total = s_run[e];
-            if (total > slots) report(status, EP_ERR_CAPACITY);
-            const int32_t cnt = static_cast<int32_t>(total < slots ? total : slots);
-            packed_recv_count[e] = cnt;
-            if (stats != nullptr) stats[e] += cnt;
-        }
-    }
-}
-
-// For more ids than one CTA reads quickly (kLLMetaMaxPrefix), the slot rows take two launches
-// instead, each linear in the slots: ll_count (one CTA per source) writes each slot's position
-// within (source, expert) and the per-source counts to scratch; ll_finish sums the counts over
-// sources (one warp per expert) and turns every position into its final row.
 template <int kThreads>
 __global__ void __launch_bounds__(kThreads)
     ll_count_kernel(int R, int T, int maxT, int K, int E, const int64_t* __restrict__ topk_idx,
@@ -726,17 +563,16 @@ int clamp_grid(int planned, int64_t warps_needed, int warps_per_block) {
     return static_cast<int>(need < planned ? (need > 0 ? need : 1) : planned);
 }
 
-// ll_meta: [kWarps][E] + 2 [E]; ll_count: [kWarps][E] + [E]
-size_t ll_meta_smem(int E, int threads) {
-    return sizeof(int32_t) * static_cast<size_t>(threads / kWarpSize + 2) * E;
+size_t ll_count_smem(int E, int threads) {
+    return sizeof(int32_t) * static_cast<size_t>(threads / kWarpSize + 1) * E;
 }
 
-constexpr size_t kLLMetaMaxSmem = 200u * 1024u;
+constexpr size_t kLLCountMaxSmem = 200u * 1024u;
 
 // One chunk of 1024 top-k entries per pass while the per-warp histograms fit in shared memory
-// (measured on ll_count: 57.0 against 58.6 us per ll_v3 dispatch), else 512-thread passes.
-int ll_meta_threads(int E) {
-    return ll_meta_smem(E, kLLMetaThreadsLarge) <= kLLMetaMaxSmem ? kLLMetaThreadsLarge : kLLMetaThreads;
+// (measured: 57.0 against 58.6 us per ll_v3 dispatch), else 512-thread passes.
+int ll_count_threads(int E) {
+    return ll_count_smem(E, kLLCountThreadsLarge) <= kLLCountMaxSmem ? kLLCountThreadsLarge : kLLCountThreads;
 }
 
 }  // namespace
@@ -759,51 +595,31 @@ cudaError_t plan_ll(LaunchPlan* plan, int num_experts) {
     if (err != cudaSuccess) return err;
     // both block sizes may be chosen per call (the allocation-free entry point plans for the most
     // experts and launches with fewer), so both may use the whole budget
-    err = cudaFuncSetAttribute(ll_meta_kernel<kLLMetaThreadsLarge>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               static_cast<int>(kLLMetaMaxSmem));
-    if (err == cudaSuccess)
-        err = cudaFuncSetAttribute(ll_meta_kernel<kLLMetaThreads>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   static_cast<int>(kLLMetaMaxSmem));
-    if (err == cudaSuccess)
-        err = cudaFuncSetAttribute(ll_count_kernel<kLLMetaThreadsLarge>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   static_cast<int>(kLLMetaMaxSmem));
+    err = cudaFuncSetAttribute(ll_count_kernel<kLLCountThreadsLarge>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(kLLCountMaxSmem));
     if (err != cudaSuccess) return err;
-    return cudaFuncSetAttribute(ll_count_kernel<kLLMetaThreads>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                static_cast<int>(kLLMetaMaxSmem));
+    return cudaFuncSetAttribute(ll_count_kernel<kLLCountThreads>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                static_cast<int>(kLLCountMaxSmem));
 }
-
-bool ll_slots_use_counts(int R, int maxT, int K) {
-    return static_cast<int64_t>(R - 1) * maxT * K > kLLMetaMaxPrefix;
-}
-
 
 cudaError_t launch_ll_dispatch(const LaunchPlan& plan, int R, int T, int maxT, int H, int K, int E,
                                const void* x, const int64_t* topk_idx, bool use_fp8, bool round_scale,
                                bool use_ue8m0, const int32_t* rank_mask, int32_t* slot, int32_t* cnt,
                                void* recv_msgs, int32_t* packed_recv_count, int64_t* layout_range,
                                int32_t* stats, int32_t* status, cudaStream_t stream) {
-    const int threads = ll_meta_threads(E);
-    cudaError_t err;
-    if (static_cast<int64_t>(R - 1) * T * K <= kLLMetaMaxPrefix) {
-        // one launch: each source's CTA counts the earlier sources' slots itself
-        auto meta_kernel = threads == kLLMetaThreadsLarge ? ll_meta_kernel<kLLMetaThreadsLarge>
-                                                          : ll_meta_kernel<kLLMetaThreads>;
-        err = launch_kernel(meta_kernel, dim3(R), dim3(threads), ll_meta_smem(E, threads), stream, 1, R, T, maxT, K, E,
-                            topk_idx, rank_mask, slot, packed_recv_count, layout_range, stats, status);
-    } else {
-        if (cnt == nullptr) return cudaErrorInvalidValue;
-        auto count_kernel = threads == kLLMetaThreadsLarge ? ll_count_kernel<kLLMetaThreadsLarge>
-                                                           : ll_count_kernel<kLLMetaThreads>;
-        err = launch_kernel(count_kernel, dim3(R), dim3(threads), ll_meta_smem(E, threads) - sizeof(int32_t) * E,
-                            stream, 1, R, T, maxT, K, E, topk_idx, rank_mask, slot, cnt, status);
-        if (err != cudaSuccess) return err;
-        const int expert_blocks = (E + kFinishThreads / kWarpSize - 1) / (kFinishThreads / kWarpSize);
-        const int64_t n_slots = static_cast<int64_t>(R) * T * K;
-        const int slot_blocks = static_cast<int>((n_slots + kFinishThreads - 1) / kFinishThreads);
-        err = launch_kernel(ll_finish_kernel, dim3(expert_blocks + slot_blocks), dim3(kFinishThreads), 0, stream, 1, R,
-                            T, maxT, K, E, expert_blocks, topk_idx, static_cast<const int32_t*>(cnt), slot,
-                            packed_recv_count, layout_range, stats, status);
-    }
+    const int count_threads = ll_count_threads(E);
+    auto count_kernel = count_threads == kLLCountThreadsLarge ? ll_count_kernel<kLLCountThreadsLarge>
+                                                              : ll_count_kernel<kLLCountThreads>;
+    cudaError_t err = launch_kernel(count_kernel, dim3(R), dim3(count_threads), ll_count_smem(E, count_threads), stream,
+                                    1, R, T, maxT, K, E, topk_idx, rank_mask, slot, cnt, status);
+    if (err != cudaSuccess) return err;
+    const int fin_threads = kFinishThreads;
+    const int expert_blocks = (E + fin_threads / kWarpSize - 1) / (fin_threads / kWarpSize);
+    const int64_t n_slots = static_cast<int64_t>(R) * T * K;
+    const int slot_blocks = static_cast<int>((n_slots + fin_threads - 1) / fin_threads);
+    err = launch_kernel(ll_finish_kernel, dim3(expert_blocks + slot_blocks), dim3(fin_threads), 0, stream, 1, R, T,
+                        maxT, K, E, expert_blocks, topk_idx, static_cast<const int32_t*>(cnt), slot,
+                        packed_recv_count, layout_range, stats, status);
     if (err != cudaSuccess) return err;
     const int64_t n_tokens = static_cast<int64_t>(R) * T;
     if (n_tokens == 0) return cudaSuccess;

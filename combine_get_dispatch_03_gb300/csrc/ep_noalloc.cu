@@ -15,9 +15,7 @@
 // holds its 64 KiB until the process exits.  All calls on a device share it:
 // two calls whose kernels overlap on the GPU (different streams without an
 // ordering between them) race on it.  Nothing in it needs clearing between
-// calls: the count kernel overwrites every entry that the later kernel reads.
-// The array is used only where the slot rows take two launches (more tokens
-// than the one-launch slot pass serves); smaller calls need no scratch.
+// calls: the count kernel overwrites every entry that the later kernels read.
 #include <mutex>
 
 #include "ep_common.cuh"

@@ -383,13 +383,10 @@ ep_status ep_selftest_bounded_wait(ep_handle* h, uint32_t max_iterations, int32_
  *     with the map itself.
  *   status (one device int32): the kernels set it to the first error code and
  *     never clear it; the caller zeroes it.
- * Where the slot rows take two launches ((num_ranks - 1) * num_tokens *
- * num_topk > 65536 slots), the per-(source, expert) counts the two kernels
- * pass between them live in a file-scope __device__ array of
- * EP_LL_NOALLOC_MAX_COUNTS entries (smaller calls compute the rows in one
- * launch with no memory besides their outputs); num_ranks * num_experts
- * beyond that array is rejected with EP_ERR_UNSUPPORTED, whatever the
- * number of tokens, before anything is enqueued.  The function calls no cudaMalloc, cudaFree
+ * The per-(source, expert) counts the kernels pass between them live in a
+ * file-scope __device__ array of EP_LL_NOALLOC_MAX_COUNTS entries, so
+ * num_ranks * num_experts beyond that is rejected with EP_ERR_UNSUPPORTED
+ * before anything is enqueued.  The function calls no cudaMalloc, cudaFree
  * or other allocating routine.  Its first call on a device looks up the
  * array's device address and the launch shapes for that device; make that
  * first call before any stream capture.  Every call on a device shares the

@@ -312,10 +312,10 @@ LL_CASES = [
     S("ll_r8_zipf", 8, 64, 2048, 64, 8, routing="zipf", mask_p=0.05, seed=32, max_tokens=64),
     S("ll_r32", 32, 12, 7168, 256, 8, seed=33, max_tokens=16),
     S("ll_r3_full", 3, 100, 512, 6, 2, seed=34, max_tokens=100),
-    # an odd number of slots per source (odd id prefixes for the one-launch slot pass)
+    # an odd number of slots per source
     S("ll_r5_odd", 5, 37, 512, 20, 3, routing="zipf", mask_p=0.1, seed=36, max_tokens=41),
-    # (R - 1) T K = 98304 ids past the one-launch slot pass's limit: the two-launch pass with counts
-    S("ll_r4_two_launch", 4, 4096, 512, 32, 8, mask_p=0.05, seed=35, max_tokens=4096),
+    # many slots per source: 32768, in 32 chunks of the slot-row pass's 1024-thread block
+    S("ll_r4_long", 4, 4096, 512, 32, 8, mask_p=0.05, seed=35, max_tokens=4096),
 ]
 LL_FORMATS = ["bf16", "fp8", "fp8_round", "fp8_ue8m0"]
 

@@ -28,10 +28,10 @@ def host(t):
     return t.detach().cpu().numpy()
 
 
-# (R, maxT, H, E, K, calls): 16 ranks x 128 experts run the slot pass's 1024-thread block; 8 ranks x
-# 2048 experts (R * E at the scratch's limit) its 512-thread block, whose shared-memory size the
-# first call's set-up plans for the most experts; 4 ranks x 4096 tokens x top-8 take the two-launch
-# slot pass, whose counts live in the fixed array (first call), then 2000 tokens the one-launch pass
+# (R, maxT, H, E, K, calls): 16 ranks x 128 experts run the count kernel's 1024-thread block; 8 ranks
+# x 2048 experts (R * E at the scratch's limit) its 512-thread block, whose shared-memory size the
+# first call's set-up plans for the most experts; 4 ranks x 4096 tokens x top-8 count 32768 slots per
+# source in 32 chunks, then a shorter second call on the same fixed array
 CASES = [
     (16, 48, 2048, 128, 8, [dict(T=48, fmt=(1, 1, 1), seed=501, mask=0.05), dict(T=37, fmt=(1, 0, 0), seed=502, mask=0.0)]),
     (8, 8, 512, 2048, 8, [dict(T=8, fmt=(1, 1, 1), seed=503, mask=0.05), dict(T=5, fmt=(0, 0, 0), seed=504, mask=0.1)]),
