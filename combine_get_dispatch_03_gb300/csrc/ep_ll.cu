@@ -478,7 +478,7 @@ __global__ void __launch_bounds__(kLLCombineThreads)
         if (lane < K) {
             const int64_t v = __ldg(topk_idx + g * K + lane);
             const int32_t r = __ldg(slot + (static_cast<int64_t>(s) * maxT + t) * K + lane);
-            if (v >= 0 && v < E && r >= 0) {
+            if (v >= 0 && v < E && r >= 0 && r < slots) {
                 src_row = v * slots + r;
                 w = __ldg(topk_weights + g * K + lane);
             }
@@ -625,10 +625,14 @@ cudaError_t launch_ll_dispatch(const LaunchPlan& plan, int R, int T, int maxT, i
     if (n_tokens == 0) return cudaSuccess;
     const int64_t msg = ep_ll_msg_bytes(H, use_fp8 ? 1 : 0);
     const bool rs = round_scale || use_ue8m0;
-    // Bulk-copy kernel: about 64 KB of stages per CTA, 2..8 stages.
+    // Bulk-copy kernel.  FP8: one stage (the bf16 row and its message, 22 KB at 7168 channels) and one
+    // token per CTA, so 9 CTAs -- 36 casting warps -- share an SM (measured on ll_v3 against two stages
+    // and 5 CTAs per SM: 56.3 against 57.5 us per dispatch, and 59.0 against 61.1 us from a cold L2;
+    // three or four stages, more tokens per CTA, or the row loaded into registers instead of staged
+    // were all slower).  bf16: about 64 KB of stages per CTA, 2..8 stages.
     const uint32_t per_stage = ll_bulk_smem(use_fp8, H, msg, 1).total - ll_bulk_smem(use_fp8, H, msg, 0).total;
     int S = static_cast<int>(65536u / per_stage);
-    S = S < 2 ? 2 : (S > 8 ? 8 : S);
+    S = use_fp8 ? 1 : (S < 2 ? 2 : (S > 8 ? 8 : S));
     const uint32_t smem = ll_bulk_smem(use_fp8, H, msg, S).total;
     if (smem <= kLLBulkMaxSmem) {
         // contiguous token blocks: enough CTAs to fill the GPU once (CTAs resident per SM from the
