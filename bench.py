@@ -605,16 +605,22 @@ def l2_bytes(dev):
     return int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 129 << 20))
 
 
-def timed_cold(fn, reps, stream, flush, warmup=3):
+def timed_cold(fn, reps, stream, flush, warmup=3, clean=False):
     """Time of one call that starts with a cold L2: `flush` (a buffer twice the L2) is written
-    before each call, outside the events; median over `reps` calls."""
+    before each call, outside the events -- which leaves the L2 full of dirty lines that the timed
+    call writes back -- or, with clean=True, read (the L2 then holds only clean lines of the flush
+    buffer); median over `reps` calls."""
     for _ in range(warmup):
         fn()
     torch.cuda.synchronize()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     times = []
+    flush64 = flush.view(torch.int64)
     for _ in range(reps):
-        flush.zero_()
+        if clean:
+            flush64.sum()
+        else:
+            flush.zero_()
         a.record(stream)
         fn()
         b.record(stream)
@@ -866,10 +872,13 @@ def measure_other_ops(ep, dev, peak, checks, reps=10):
     ms_d = timed(fn, reps, stream)
     flush = torch.empty(2 * l2_bytes(dev), dtype=torch.uint8, device=dev)
     cold_d = timed_cold(fn, 2 * reps, stream, flush)
+    clean_d = timed_cold(fn, 2 * reps, stream, flush, clean=True)
     y = W.normal_bf16((shape.R, shape.EL, shape.R * shape.max_tokens, shape.H), shape.seed, "lly", device=dev)
     out = torch.empty((shape.R, shape.T, shape.H), dtype=torch.bfloat16, device=dev)
     ms_c = timed(lambda: ep.ep_ll_combine(h, y, idx_d, w_d, combined_x=out), reps, stream)
     cold_c = timed_cold(lambda: ep.ep_ll_combine(h, y, idx_d, w_d, combined_x=out), 2 * reps, stream, flush)
+    clean_c = timed_cold(lambda: ep.ep_ll_combine(h, y, idx_d, w_d, combined_x=out), 2 * reps, stream, flush,
+                         clean=True)
     h.check()
     checks.append(capture_ll("ll_v3.ll_dispatch_fp8_ue8m0+ll_combine", shape, h, idx, w, x_d,
                              dict(recv_msgs=msgs, packed_recv_count=cnt, packed_recv_layout_range=rng_, y=y,
@@ -877,10 +886,12 @@ def measure_other_ops(ep, dev, peak, checks, reps=10):
     n_valid = int((idx >= 0).sum())
     b = ll_bytes(shape.R, shape.T, shape.H, shape.K, n_valid, msg)
     warm = "calls back to back (the 58.7 MB of tokens can stay in the 129 MB L2)"
-    report("ll_v3.ll_dispatch_fp8_ue8m0", ms_d, b["ll_dispatch"],
-           {"note": warm, "cold_us": round(cold_d * 1e3, 2), "cold_note": "L2 written over before each call"})
-    report("ll_v3.ll_combine", ms_c, b["ll_combine"],
-           {"note": warm, "cold_us": round(cold_c * 1e3, 2), "cold_note": "L2 written over before each call"})
+    cold_note = ("cold_us: L2 written over before each call (the call also writes back the flush's dirty lines); "
+                 "cold_clean_us: L2 filled by reading a 2x-L2 buffer before each call (clean lines)")
+    for name, ms, bb, cold, clean in (("ll_v3.ll_dispatch_fp8_ue8m0", ms_d, b["ll_dispatch"], cold_d, clean_d),
+                                      ("ll_v3.ll_combine", ms_c, b["ll_combine"], cold_c, clean_c)):
+        report(name, ms, bb, {"note": warm, "cold_us": round(cold * 1e3, 2), "cold_clean_us": round(clean * 1e3, 2),
+                              "cold_clean_frac": round(total(bb) / clean / 1e6 / peak, 4), "cold_note": cold_note})
     del flush
     h.destroy()
     del msgs, y, out

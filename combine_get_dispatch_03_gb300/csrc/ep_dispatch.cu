@@ -32,10 +32,10 @@ constexpr int kCombineFanInSmallR = 8;
 constexpr int kCombineFanIn = 4;
 constexpr int kCombineWeightRanks = 8;  // source ranks whose top-k weights are loaded ahead of the rows
 constexpr bool kUseBulkDispatch = true;  // bulk-copy (TMA 1D) dispatch where the rows fit in shared memory
-// Shared memory for the stages of one CTA (bf16, cast, FP8 input).  The cast keeps fewer stages
-// (two rows of bf16 + FP8 at 7168 channels) so that more CTAs -- and their cast work -- share an
-// SM; measured on the 7168-wide workloads, with one round of the stages per CTA (a CTA takes at
-// most `stages` tokens): 652 us for fp8_zipf against 692 us with three stages and two rounds.
+// Shared memory for the stages of one CTA (bf16, cast, FP8 input).  The cast keeps the fewest
+// stages (see bulk_stages) so that more CTAs -- and their cast work -- share an SM; measured on the
+// 7168-wide workloads, with one round of the stages per CTA (a CTA takes at most `stages` tokens):
+// 652 us for fp8_zipf with two stages against 692 us with three stages and two rounds.
 constexpr uint32_t kBulkStageBudget[3] = {65536u, 45056u, 65536u};
 constexpr int kBulkCastWarps = 4;  // warps of a cast CTA
 
@@ -493,7 +493,10 @@ int clamp_grid(int planned, int64_t warps_needed, int warps_per_block) {
 }  // namespace
 
 int bulk_stages(int mode, int H) {
-    // kBulkStageBudget[mode] bytes of row buffers per CTA, between 2 and 8 stages
+    // The cast: one stage (the bf16 row and its codes + scales, 22 KB at 7168 channels), so 9 CTAs share
+    // an SM (fp8_zipf: 636.2 against 638.7 us with two stages; the low-latency FP8 dispatch gained the
+    // same way).  Otherwise kBulkStageBudget[mode] bytes of row buffers per CTA, between 2 and 8 stages.
+    if (mode == kModeCastFp8) return 1;
     const uint32_t per = bulk_smem(mode, H, 1).in_stride + bulk_smem(mode, H, 1).out_stride;
     int s = static_cast<int>(kBulkStageBudget[mode] / per);
     return s < 2 ? 2 : (s > 8 ? 8 : s);
