@@ -724,6 +724,32 @@ def run_ll_calls(n, small=False, hidden=0):
                       "ll_combine_us": round(a.elapsed_time(b) * 1e3 / n, 2)}))
 
 
+def run_scan_calls(n, workload, tokens=0):
+    """ep_layout_notify alone (the one-pass layout + record scan; with whole nodes of 8 ranks it also
+    builds the node-level record), n calls back to back on a workload's routing, for profilers;
+    prints the CUDA-event time per call."""
+    from combine_get_dispatch_03_gb300 import ep
+    dev = torch.device("cuda", 0)
+    shape = W.WORKLOADS[workload]
+    if tokens:
+        shape = shape.scaled(T=tokens)
+    idx, _ = W.routing(shape)
+    idx_d = torch.from_numpy(idx).to(dev)
+    h = ep.Handle(ep.Config(shape.R, shape.T, shape.H, shape.E, shape.K, shape.C, shape.A, receive_capacity(shape)),
+                  dev)
+    s = torch.cuda.current_stream(dev)
+    lay = ep.ep_layout_notify(h, idx_d)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(s)
+    for _ in range(n):
+        ep.ep_layout_notify(h, idx_d, **lay)
+    b.record(s)
+    b.synchronize()
+    h.check()
+    print(json.dumps({"scan_calls": n, "workload": shape.name, "R": shape.R, "T": shape.T,
+                      "layout_notify_us": round(a.elapsed_time(b) * 1e3 / n, 2)}))
+
+
 def fp8_inputs(shape, dev):
     """Already-cast tokens for the FP8-input dispatch: e4m3 codes (no NaN codes) and fp32 scales."""
     x8 = torch.randint(0, 126, (shape.R, shape.T, shape.H), dtype=torch.uint8, device=dev).view(torch.float8_e4m3fn)
@@ -1207,6 +1233,10 @@ def main():
                     help="only run the fp8_zipf FP8 dispatch (fresh record, cast) this many times (profiling)")
     ap.add_argument("--fp8-input", action="store_true",
                     help="with --fp8-calls: time cached dispatches of already-cast e4m3 tokens and scales")
+    ap.add_argument("--scan-calls", type=int, default=0,
+                    help="only run ep_layout_notify this many times on --scan-workload (profiling)")
+    ap.add_argument("--scan-workload", default="combine_heavy",
+                    help="with --scan-calls: the workload whose routing is scanned (combine_heavy: 2 nodes of 8)")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--layout-two-launches", action="store_true",
                     help="run the step's layout and notify as the two separate calls (ep_get_dispatch_layout, "
@@ -1216,7 +1246,9 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
-    if args.ll_calls:
+    if args.scan_calls:
+        run_scan_calls(args.scan_calls, args.scan_workload, args.tokens)
+    elif args.ll_calls:
         run_ll_calls(args.ll_calls, args.ll_small, args.ll_hidden)
     elif args.fp8_calls:
         run_fp8_calls(args.fp8_calls, args.tokens, args.fp8_input)
