@@ -492,11 +492,13 @@ int clamp_grid(int planned, int64_t warps_needed, int warps_per_block) {
 
 }  // namespace
 
-int bulk_stages(int mode, int H) {
+int bulk_stages(int mode, int H, bool sm_limited) {
     // The cast: one stage (the bf16 row and its codes + scales, 22 KB at 7168 channels), so 9 CTAs share
     // an SM (fp8_zipf: 636.2 against 638.7 us with two stages; the low-latency FP8 dispatch gained the
-    // same way).  Otherwise kBulkStageBudget[mode] bytes of row buffers per CTA, between 2 and 8 stages.
-    if (mode == kModeCastFp8) return 1;
+    // same way) -- unless max_sms caps the grid: a CTA then takes more tokens than it has stages, and
+    // the refill of token j-1's stage at token j needs two.  Otherwise kBulkStageBudget[mode] bytes of
+    // row buffers per CTA, between 2 and 8 stages.
+    if (mode == kModeCastFp8 && !sm_limited) return 1;
     const uint32_t per = bulk_smem(mode, H, 1).in_stride + bulk_smem(mode, H, 1).out_stride;
     int s = static_cast<int>(kBulkStageBudget[mode] / per);
     return s < 2 ? 2 : (s > 8 ? 8 : s);
@@ -511,7 +513,7 @@ int bulk_threads(int mode) {
 
 template <int kMode>
 cudaError_t plan_bulk(LaunchPlan* plan, int H) {
-    const int S = bulk_stages(kMode, H);
+    const int S = bulk_stages(kMode, H, plan->sm_limited);
     const uint32_t smem = bulk_smem(kMode, H, S).total;
     plan->bulk_stages[kMode] = 0;
     if (smem > 200u * 1024u) return cudaSuccess;  // rows too long to stage: the register kernel is used
@@ -558,6 +560,7 @@ cudaError_t launch_dispatch(const LaunchPlan& plan, int mode, int R, int T, int 
         // (with max_sms, one resident wave takes all tokens)
         const int cap_cta = plan.sm_limited ? INT32_MAX : S;
         const int per_cta = static_cast<int>(fill < 1 ? 1 : (fill > cap_cta ? cap_cta : fill));
+        if (S < 2 && per_cta > 1) return cudaErrorInvalidValue;  // the refill of a stage needs two stages
         const int grid = static_cast<int>((n_tokens + per_cta - 1) / per_cta);
         const uint32_t smem = plan.bulk_smem[mode];
         const int threads = bulk_threads(mode);
