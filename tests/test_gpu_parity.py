@@ -316,6 +316,13 @@ LL_CASES = [
     S("ll_r5_odd", 5, 37, 512, 20, 3, routing="zipf", mask_p=0.1, seed=36, max_tokens=41),
     # many slots per source: 32768, in 32 chunks of the slot-row pass's 1024-thread block
     S("ll_r4_long", 4, 4096, 512, 32, 8, mask_p=0.05, seed=35, max_tokens=4096),
+    # 20 sources, 2 local experts each, zipf routing with masked slots
+    S("ll_r20", 20, 50, 512, 40, 6, routing="zipf", mask_p=0.05, seed=37, max_tokens=50),
+    # 32 sources with 800, 2048 and 2056 slots each: one ragged chunk, two whole chunks, and two
+    # whole chunks plus an 8-slot tail in the count kernel
+    S("ll_r32_t100", 32, 100, 512, 64, 8, routing="zipf", mask_p=0.05, seed=38, max_tokens=128),
+    S("ll_r32_t256", 32, 256, 512, 64, 8, seed=39, max_tokens=256),
+    S("ll_r32_t257", 32, 257, 512, 64, 8, seed=40, max_tokens=257),
 ]
 LL_FORMATS = ["bf16", "fp8", "fp8_round", "fp8_ue8m0"]
 
