@@ -246,6 +246,20 @@ __device__ __forceinline__ void pdl_enter() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// Warm passes.  A kernel launched early sits at its grid-dependency wait while the previous kernel
+// runs.  After a call's stream of stores has gone through L2 its code is cold, and the first
+// blocks after the wait stalled for 1000-1900 SM cycles (clock64 stamps in the low-latency count
+// kernel).  A kernel whose body runs twice -- pass 0 before the wait with every global load and
+// store switched off and its loops cut short, pass 1 after the wait for real -- fetches that code
+// while it would otherwise only wait.  Only short single-wave kernels use it: in a grid of many
+// waves every later CTA would pay for a pass 0 of its own.  The pass count is opaque to the
+// compiler so that both passes run one copy of the body.
+__device__ __forceinline__ int warm_passes() {
+    int n = 2;
+    asm volatile("" : "+r"(n));
+    return n;
+}
+
 // Launch `kernel` with programmatic stream serialisation (and a 1-D cluster when cluster_x > 1).
 template <typename... KArgs, typename... Args>
 cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,

@@ -42,11 +42,10 @@ __global__ void __launch_bounds__(kThreads)
     ll_count_kernel(int R, int T, int maxT, int K, int E, const int64_t* __restrict__ topk_idx,
                     const int32_t* __restrict__ rank_mask, int32_t* __restrict__ slot, int32_t* __restrict__ cnt,
                     int32_t* status) {
-    pdl_enter();
     constexpr int kWarps = kThreads / kWarpSize;
     constexpr int kScanChunk = kWarps < 16 ? kWarps : 16;
     static_assert(kWarps % kScanChunk == 0, "whole scan chunks");
-    extern __shared__ int32_t smem[];
+    extern __shared__ __align__(16) int32_t smem[];
     int32_t* s_warp = smem;                   // [kWarps][E]: per-warp count -> exclusive prefix
     int32_t* s_run = smem + kWarps * E;  // [E]: slots of this source seen so far
     const int s = blockIdx.x;
@@ -58,66 +57,76 @@ __global__ void __launch_bounds__(kThreads)
     int32_t* slot_s = slot + static_cast<int64_t>(s) * maxT * K;
 
     __shared__ int32_t s_mask[kMaxRanks];  // rank mask (0 everywhere without one)
-    for (int e = tid; e < E; e += kThreads) s_run[e] = 0;
-    if (tid < kMaxRanks) s_mask[tid] = rank_mask != nullptr && tid < R ? __ldg(rank_mask + tid) : 0;
-    int64_t next = tid < n ? __ldg(idx_s + tid) : -1;  // the next chunk's entry, loaded one chunk ahead
-    for (int base = 0; base < n; base += kThreads) {
-        for (int i = tid; i < kWarps * E; i += kThreads) s_warp[i] = 0;
-        __syncthreads();
-        const int i = base + tid;
-        const int64_t v = next;
-        if (base + kThreads + tid < n) next = __ldg(idx_s + base + kThreads + tid);
-        int e = -1;
-        if (i < n) {
-            if (v >= 0 && v < E) e = static_cast<int>(v);
-            else if (v != -1) report(status, EP_ERR_BAD_EXPERT);
-            // a masked rank neither sends nor receives
-            if (e >= 0 && (s_mask[s] != 0 || s_mask[e / (E / R)] != 0)) e = -1;
-        }
-        const unsigned peers = __match_any_sync(kFullMask, e);
-        const int before = __popc(peers & lanemask_lt());
-        if (e >= 0 && before == 0) s_warp[warp * E + e] = __popc(peers);
-        __syncthreads();
-        // per expert: exclusive prefix over the warps, in chunks of 16 whose loads are all issued
-        // before the stores (a load after a store to the same array would wait for it)
-        for (int x = tid; x < E; x += kThreads) {
-            int32_t run = s_run[x];
-#pragma unroll
-            for (int w0 = 0; w0 < kWarps; w0 += kScanChunk) {
-                int32_t c[kScanChunk];
-#pragma unroll
-                for (int u = 0; u < kScanChunk; ++u) c[u] = s_warp[(w0 + u) * E + x];
-#pragma unroll
-                for (int u = 0; u < kScanChunk; ++u) {
-                    s_warp[(w0 + u) * E + x] = run;
-                    run += c[u];
-                }
+    const bool any_mask = rank_mask != nullptr;
+    const int EL = E / R;
+    // a warm pass first (see warm_passes): no global access, one chunk
+    const int passes = warm_passes();
+#pragma unroll 1
+    for (int pass = 0; pass < passes; ++pass) {
+        const bool live = pass == passes - 1;  // the pass after the grid-dependency wait
+        if (live) pdl_enter();
+        const int n_pass = live ? n : (n < kThreads ? n : kThreads);
+        for (int e = tid; e < E; e += kThreads) s_run[e] = 0;
+        if (tid < kMaxRanks) s_mask[tid] = live && rank_mask != nullptr && tid < R ? __ldg(rank_mask + tid) : 0;
+        int64_t next = live && tid < n ? __ldg(idx_s + tid) : -1;  // the next chunk's entry, loaded one chunk ahead
+        for (int base = 0; base < n_pass; base += kThreads) {
+            for (int i = tid; i < kWarps * E / 4; i += kThreads)  // kWarps * E is a multiple of 4
+                reinterpret_cast<int4*>(s_warp)[i] = make_int4(0, 0, 0, 0);
+            __syncthreads();
+            const int i = base + tid;
+            const int64_t v = next;
+            if (live && base + kThreads + tid < n) next = __ldg(idx_s + base + kThreads + tid);
+            int e = -1;
+            if (i < n) {
+                if (v >= 0 && v < E) e = static_cast<int>(v);
+                else if (v != -1 && live) report(status, EP_ERR_BAD_EXPERT);
+                // a masked rank neither sends nor receives
+                if (e >= 0 && any_mask && (s_mask[s] != 0 || s_mask[e / EL] != 0)) e = -1;
             }
-            s_run[x] = run;
+            const unsigned peers = __match_any_sync(kFullMask, e);
+            const int before = __popc(peers & lanemask_lt());
+            if (e >= 0 && before == 0) s_warp[warp * E + e] = __popc(peers);
+            __syncthreads();
+            // per expert: exclusive prefix over the warps, in chunks of 16 whose loads are all issued
+            // before the stores (a load after a store to the same array would wait for it)
+            for (int x = tid; x < E; x += kThreads) {
+                int32_t run = s_run[x];
+    #pragma unroll
+                for (int w0 = 0; w0 < kWarps; w0 += kScanChunk) {
+                    int32_t c[kScanChunk];
+    #pragma unroll
+                    for (int u = 0; u < kScanChunk; ++u) c[u] = s_warp[(w0 + u) * E + x];
+    #pragma unroll
+                    for (int u = 0; u < kScanChunk; ++u) {
+                        s_warp[(w0 + u) * E + x] = run;
+                        run += c[u];
+                    }
+                }
+                s_run[x] = run;
+            }
+            __syncthreads();
+            if (live && i < n) slot_s[i] = e >= 0 ? s_warp[warp * E + e] + before : -1;
+            __syncthreads();
         }
-        __syncthreads();
-        if (i < n) slot_s[i] = e >= 0 ? s_warp[warp * E + e] + before : -1;
-        __syncthreads();
+        if (live)
+            for (int e = tid; e < E; e += kThreads) cnt[static_cast<int64_t>(s) * E + e] = s_run[e];
+        __syncthreads();  // shared memory is rewritten by the next pass
     }
-    for (int e = tid; e < E; e += kThreads) cnt[static_cast<int64_t>(s) * E + e] = s_run[e];
 }
 
-// Blocks [0, expert_blocks): one warp per expert e; lane s holds the count of
-// source s, a warp scan gives each source block's begin (R <= 32).  The other
-// blocks: one thread per top-k slot turns its position within (source, expert)
-// into the final row, begin(e, s) + position, or -1 past the R * maxT capacity.
-__global__ void ll_finish_kernel(int R, int T, int maxT, int K, int E, int expert_blocks,
-                                 const int64_t* __restrict__ topk_idx, const int32_t* __restrict__ cnt,
-                                 int32_t* __restrict__ slot, int32_t* __restrict__ packed_recv_count,
-                                 int64_t* __restrict__ layout_range, int32_t* __restrict__ stats, int32_t* status) {
-    pdl_enter();
+// One pass of ll_finish_kernel; `live` false: no global access (the warm pass).
+__device__ __forceinline__ void ll_finish_pass(bool live, int R, int T, int maxT, int K, int E, int expert_blocks,
+                                               const int64_t* __restrict__ topk_idx, const int32_t* __restrict__ cnt,
+                                               int32_t* __restrict__ slot, int32_t* __restrict__ packed_recv_count,
+                                               int64_t* __restrict__ layout_range, int32_t* __restrict__ stats,
+                                               int32_t* status, int32_t* s_begin) {
     const int64_t slots = static_cast<int64_t>(R) * maxT;
     if (static_cast<int>(blockIdx.x) < expert_blocks) {
         const int lane = lane_id();
         const int warps = blockDim.x / kWarpSize;
         const int e = blockIdx.x * warps + threadIdx.x / kWarpSize;
         if (e >= E) return;
-        const int32_t c = lane < R ? __ldg(cnt + static_cast<int64_t>(lane) * E + e) : 0;
+        const int32_t c = live && lane < R ? __ldg(cnt + static_cast<int64_t>(lane) * E + e) : 0;
         int32_t incl = c;
 #pragma unroll
         for (int off = 1; off < kWarpSize; off <<= 1) {
@@ -125,12 +134,12 @@ __global__ void ll_finish_kernel(int R, int T, int maxT, int K, int E, int exper
             if (lane >= off) incl += o;
         }
         const int32_t begin = incl - c;
-        if (lane < R)
+        if (live && lane < R)
             layout_range[static_cast<int64_t>(e) * R + lane] =
                 static_cast<int64_t>((static_cast<uint64_t>(static_cast<uint32_t>(c)) << 32) |
                                      static_cast<uint32_t>(begin));
         const int32_t total = __shfl_sync(kFullMask, incl, kWarpSize - 1);
-        if (lane == 0) {
+        if (live && lane == 0) {
             if (total > slots) report(status, EP_ERR_CAPACITY);
             const int32_t n = static_cast<int32_t>(total < slots ? total : slots);
             packed_recv_count[e] = n;
@@ -145,28 +154,30 @@ __global__ void ll_finish_kernel(int R, int T, int maxT, int K, int E, int exper
     // that source's blocks for all experts into shared memory while its slots' expert ids and
     // positions load: loads that need no expert id, so a slot waits for one round of loads
     // instead of two.
-    __shared__ int32_t s_begin[kFinishThreads];
     const int64_t i_last = (i0 + blockDim.x < n_slots ? i0 + blockDim.x : n_slots) - 1;
     const int s_first = static_cast<int>(i0 / (static_cast<int64_t>(T) * K));
     const bool table = E <= static_cast<int>(blockDim.x) && i0 < n_slots &&
                        s_first == static_cast<int>(i_last / (static_cast<int64_t>(T) * K));
-    const bool live = i < n_slots;
+    const bool active = i < n_slots;
     int s = 0;
     int64_t v = -1;
     int32_t pos = -1;
     int32_t* sp = nullptr;
-    if (live) {
+    if (active) {
         s = static_cast<int>(i / (static_cast<int64_t>(T) * K));
-        v = __ldg(topk_idx + i);
         sp = slot + static_cast<int64_t>(s) * maxT * K + (i - static_cast<int64_t>(s) * T * K);
-        pos = *sp;
+        if (live) {
+            v = __ldg(topk_idx + i);
+            pos = *sp;
+        }
     }
     if (table) {
         const int e = threadIdx.x;
         if (e < E) {
             int32_t part[kMaxRanks];
 #pragma unroll
-            for (int q = 0; q < kMaxRanks; ++q) part[q] = q < s_first ? __ldg(cnt + static_cast<int64_t>(q) * E + e) : 0;
+            for (int q = 0; q < kMaxRanks; ++q)
+                part[q] = live && q < s_first ? __ldg(cnt + static_cast<int64_t>(q) * E + e) : 0;
             int32_t b = 0;
 #pragma unroll
             for (int q = 0; q < kMaxRanks; ++q) b += part[q];
@@ -174,7 +185,7 @@ __global__ void ll_finish_kernel(int R, int T, int maxT, int K, int E, int exper
         }
         __syncthreads();
     }
-    if (!live) return;
+    if (!active) return;
     int32_t row = -1;
     if (v >= 0 && v < E && pos >= 0) {
         int64_t begin = 0;
@@ -191,7 +202,28 @@ __global__ void ll_finish_kernel(int R, int T, int maxT, int K, int E, int exper
         }
         if (begin + pos < slots) row = static_cast<int32_t>(begin + pos);
     }
-    *sp = row;
+    if (live) *sp = row;
+}
+
+// Blocks [0, expert_blocks): one warp per expert e; lane s holds the count of
+// source s, a warp scan gives each source block's begin (R <= 32).  The other
+// blocks: one thread per top-k slot turns its position within (source, expert)
+// into the final row, begin(e, s) + position, or -1 past the R * maxT capacity.
+// A warm pass first (see warm_passes).
+__global__ void ll_finish_kernel(int R, int T, int maxT, int K, int E, int expert_blocks,
+                                 const int64_t* __restrict__ topk_idx, const int32_t* __restrict__ cnt,
+                                 int32_t* __restrict__ slot, int32_t* __restrict__ packed_recv_count,
+                                 int64_t* __restrict__ layout_range, int32_t* __restrict__ stats, int32_t* status) {
+    __shared__ int32_t s_begin[kFinishThreads];
+    const int passes = warm_passes();
+#pragma unroll 1
+    for (int pass = 0; pass < passes; ++pass) {
+        const bool live = pass == passes - 1;
+        if (live) pdl_enter();
+        ll_finish_pass(live, R, T, maxT, K, E, expert_blocks, topk_idx, cnt, slot, packed_recv_count, layout_range,
+                       stats, status, s_begin);
+        __syncthreads();  // s_begin is rewritten by the next pass
+    }
 }
 
 // Bulk-copy low-latency dispatch: CTA b takes the contiguous tokens [b * per_cta,
