@@ -247,9 +247,9 @@ __device__ __forceinline__ void pdl_enter() {
 }
 
 // Warm passes.  A kernel launched early sits at its grid-dependency wait while the previous kernel
-// runs.  After a call's stream of stores has gone through L2 its code is cold, and the first
-// blocks after the wait stalled for 1000-1900 SM cycles (clock64 stamps in the low-latency count
-// kernel).  A kernel whose body runs twice -- pass 0 before the wait with every global load and
+// runs.  After a call's stream of stores has gone through L2 its code is cold: the first block
+// after the wait took 1000-1900 SM cycles in the low-latency count kernel (clock64 stamps), about
+// 450 once its code was cached.  A kernel whose body runs twice -- pass 0 before the wait with every global load and
 // store switched off and its loops cut short, pass 1 after the wait for real -- fetches that code
 // while it would otherwise only wait.  Only short single-wave kernels use it: in a grid of many
 // waves every later CTA would pay for a pass 0 of its own.  The pass count is opaque to the

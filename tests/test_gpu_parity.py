@@ -402,6 +402,42 @@ def test_ll_combine(shape):
     np.testing.assert_array_equal(P.host(got), want)
 
 
+def test_ll_back_to_back_calls_with_changing_routing():
+    """Four dispatch + combine pairs queued on one handle with no host sync between them, each with
+    its own routing and token count.  Every kernel of a call may be scheduled, and run the part of
+    its body that precedes its grid-dependency wait, while the previous call's kernels still run;
+    every call's messages, counts, ranges and combine must still equal the oracle's."""
+    maxT = 64
+    shapes = [S(f"b2b{i}", 8, T, 512, 64, 8, routing="zipf", mask_p=0.05, seed=50 + i, max_tokens=maxT)
+              for i, T in enumerate([64, 33, 64, 1])]
+    h = ep.Handle(P.config_of(shapes[0], 0))
+    runs = []
+    for sh in shapes:
+        idx, w = W.routing(sh)
+        x = W.tokens_x(sh)
+        idx_d, w_d = torch.from_numpy(idx).to(P.DEV), torch.from_numpy(w).to(P.DEV)
+        out = ep.ep_ll_dispatch(h, x.to(P.DEV), idx_d, use_fp8=True, use_ue8m0=True)
+        y = W.normal_bf16((sh.R, sh.EL, sh.R * maxT, sh.H), sh.seed, "b2by", device=P.DEV)
+        got = ep.ep_ll_combine(h, y, idx_d, w_d)
+        runs.append((sh, idx, w, x, out, y, got))
+    assert h.status() == 0
+    for sh, idx, w, x, out, y, got in runs:
+        ora = O.ll_dispatch(W.bf16_bits(x), idx, maxT, sh.E, use_fp8=True, use_ue8m0=True)
+        np.testing.assert_array_equal(P.host(out["packed_recv_count"]), ora["packed_recv_count"], err_msg=sh.name)
+        np.testing.assert_array_equal(P.host(out["packed_recv_layout_range"]), ora["packed_recv_layout_range"],
+                                      err_msg=sh.name)
+        s_, t_, k_ = np.nonzero(ora["slot_row"] >= 0)
+        e = idx[s_, t_, k_]
+        msgs = P.host(out["recv_msgs"])
+        np.testing.assert_array_equal(msgs[e // sh.EL, e % sh.EL, ora["slot_row"][s_, t_, k_]],
+                                      ora["msgs_by_slot"][s_, t_, k_], err_msg=sh.name)
+        want = O.ll_combine(P.host(y), idx, w, ora["slot_row"], maxT, sh.E)
+        np.testing.assert_array_equal(P.host(got), want, err_msg=sh.name)
+    # the handle keeps the last call's slot rows
+    np.testing.assert_array_equal(P.host(h.export("ll_slot_row"))[:, :shapes[-1].T], ora["slot_row"])
+    h.destroy()
+
+
 def test_ll_dispatch_with_8_byte_aligned_topk_idx():
     """topk_idx needs only its natural 8-byte alignment: an offset view gives the same messages."""
     shape = LL_CASES[2]
