@@ -91,12 +91,12 @@ __global__ void __launch_bounds__(kThreads)
             // before the stores (a load after a store to the same array would wait for it)
             for (int x = tid; x < E; x += kThreads) {
                 int32_t run = s_run[x];
-    #pragma unroll
+#pragma unroll
                 for (int w0 = 0; w0 < kWarps; w0 += kScanChunk) {
                     int32_t c[kScanChunk];
-    #pragma unroll
+#pragma unroll
                     for (int u = 0; u < kScanChunk; ++u) c[u] = s_warp[(w0 + u) * E + x];
-    #pragma unroll
+#pragma unroll
                     for (int u = 0; u < kScanChunk; ++u) {
                         s_warp[(w0 + u) * E + x] = run;
                         run += c[u];
