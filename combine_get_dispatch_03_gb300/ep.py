@@ -115,27 +115,33 @@ def _raise(rc: int):
         raise EPError(rc, lib().ep_last_error().decode(errors="replace"))
 
 
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
 def _stream(stream, device):
-    """The raw stream handle: `stream`, else the current stream of the handle's device."""
+    """The raw stream handle (an int): `stream`, else the current stream of the handle's device."""
     if stream is None:
+        if _raw_stream is not None:  # the current stream's handle without building a Stream object
+            return _raw_stream(device.index)
         stream = torch.cuda.current_stream(device)
-    return ctypes.c_void_p(stream.cuda_stream)
+    return stream.cuda_stream
 
 
 def _ptr(t, name, dtype=None, shape=None, device=None):
+    """The device address of a checked tensor (an int; every pointer argument is declared void*)."""
     if t is None:
         return None
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
     if dtype is not None and t.dtype != dtype:
         raise TypeError(f"{name}: dtype {t.dtype}, expected {dtype}")
-    if shape is not None and tuple(t.shape) != tuple(shape):
+    if shape is not None and t.shape != shape:  # torch.Size compares equal to a tuple
         raise ValueError(f"{name}: shape {tuple(t.shape)}, expected {tuple(shape)}")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
     if device is not None and t.device != device:
         raise ValueError(f"{name} is on {t.device}, the handle lives on {device}")
-    return ctypes.c_void_p(t.data_ptr()) if t.numel() else ctypes.c_void_p(_dummy(device).data_ptr())
+    return t.data_ptr() if t.numel() else _dummy(device).data_ptr()
 
 
 _dummies = {}
