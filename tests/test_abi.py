@@ -55,3 +55,65 @@ def test_host_only_entry_points(library):
     assert L.ep_handle_create(ctypes.byref(big), ctypes.byref(h)) == 5
     assert L.ep_dispatch(None, 0, None, 0, None, 0, None, None, None, None, None, None, None, None, None,
                          None, 0, None) == 1
+
+
+BASE = dict(num_ranks=8, num_max_tokens=64, hidden=1024, num_experts=32, num_topk=4)
+BAD_CONFIGS = [  # (change to BASE, expected status, words of the message)
+    (dict(num_ranks=0), 5, "num_ranks"),
+    (dict(num_ranks=33, num_experts=33), 5, "num_ranks"),
+    (dict(num_max_tokens=-1), 1, "num_max_tokens"),
+    (dict(hidden=0), 1, "hidden"),
+    (dict(hidden=1020), 1, "hidden"),
+    (dict(num_experts=12), 1, "multiple of num_ranks"),
+    (dict(num_experts=4096), 5, "num_experts"),
+    (dict(num_topk=0), 5, "num_topk"),
+    (dict(num_topk=33), 5, "num_topk"),
+    (dict(num_channels=0), 1, "num_channels"),
+    (dict(expert_alignment=0), 1, "expert_alignment"),
+    (dict(max_sms=-1), 1, "max_sms"),
+    (dict(recv_capacity=-1), 1, "recv_capacity"),
+    (dict(recv_capacity=2**31), 1, "recv_capacity"),
+    (dict(num_ranks=32, num_experts=32, num_max_tokens=2**27), 5, "num_ranks * num_max_tokens"),
+    (dict(num_ranks=1, num_experts=8, num_max_tokens=2**27, num_topk=32), 5, "num_max_tokens * num_topk"),
+]
+
+
+@pytest.mark.parametrize("change,code,words", BAD_CONFIGS, ids=[str(b[0]) for b in BAD_CONFIGS])
+def test_config_is_rejected_before_any_cuda_call(library, change, code, words):
+    L = ep.lib()
+    cfg = ep.Config(**{**BASE, **change}).c()
+    h = ctypes.c_void_p()
+    assert L.ep_handle_create(ctypes.byref(cfg), ctypes.byref(h)) == code
+    assert words.encode() in L.ep_last_error()
+    assert not h.value
+
+
+def _noalloc(L, R=8, T=16, maxT=16, H=1024, E=32, K=4, x=16, idx=8, fp8=0, ue8m0=0, msgs=16, out=16):
+    """ep_ll_dispatch_noalloc with fake, suitably aligned addresses (the checks run before any CUDA call)."""
+    a = lambda align: None if align is None else 0x10000 + (0 if align >= 16 else align)  # noqa: E731
+    return L.ep_ll_dispatch_noalloc(R, T, maxT, H, E, K, a(x), a(idx), fp8, 0, ue8m0, a(msgs), a(out), a(out),
+                                    None, a(out), a(out), None)
+
+
+NOALLOC_BAD = [
+    (dict(R=0), 5, "num_ranks"),
+    (dict(E=30), 1, "multiple of num_ranks"),
+    (dict(R=16, E=2048), 5, "count scratch"),
+    (dict(K=0), 5, "num_topk"),
+    (dict(T=17), 1, "num_tokens"),
+    (dict(H=1020), 1, "hidden"),
+    (dict(ue8m0=1), 1, "use_ue8m0"),
+    (dict(fp8=1, H=1024 + 128), 5, "hidden % 512"),
+    (dict(x=8), 1, "x"),
+    (dict(idx=4), 1, "topk_idx"),
+    (dict(x=None), 1, "x"),
+    (dict(msgs=8), 1, "output pointer"),
+    (dict(out=None), 1, "output pointer"),
+]
+
+
+@pytest.mark.parametrize("kw,code,words", NOALLOC_BAD, ids=[str(b[0]) for b in NOALLOC_BAD])
+def test_noalloc_arguments_are_rejected_before_any_cuda_call(library, kw, code, words):
+    L = ep.lib()
+    assert _noalloc(L, **kw) == code
+    assert words.encode() in L.ep_last_error()
