@@ -313,12 +313,14 @@ def capture_normal(name, shape, h, idx, w, x_d, cap, *, mode=0, layout=None, nrp
     return rec
 
 
-def capture_ll(name, shape, h, idx, w, x_d, out):
+def capture_ll(name, shape, h, idx, w, x_d, out, use_fp8=True, use_ue8m0=True, rank_mask=None):
     """Host copies of one low-latency dispatch (messages of the sampled tokens' slots, counts, layout
-    range, the slot map whole) and combine (the sampled tokens' outputs and the rows they read)."""
+    range, the slot map whole) and combine (the sampled tokens' outputs and the rows they read; the
+    expert outputs `y` may be a strided view such as the payloads of the message buffer)."""
     toks = W.sample_tokens(shape, PARITY_TOKENS, field="bench_parity")
     t_idx = torch.from_numpy(toks).to(x_d.device)
-    rec = dict(kind="ll", name=name, shape=shape, idx=idx, w=w, toks=toks,
+    rec = dict(kind="ll", name=name, shape=shape, idx=idx, w=w, toks=toks, use_fp8=use_fp8, use_ue8m0=use_ue8m0,
+               rank_mask=rank_mask,
                x_rows=_host(x_d.reshape(-1, shape.H)[t_idx]), slot_row=_host(h.export("ll_slot_row"))[:, :shape.T])
     rec.update({k: _host(v) for k, v in out.items() if k in ("packed_recv_count", "packed_recv_layout_range")})
     sl = rec["slot_row"].reshape(-1, shape.K)[toks]          # [n][K]
@@ -329,7 +331,9 @@ def capture_ll(name, shape, h, idx, w, x_d, out):
     rec["msg_rows"] = _host(msgs[flat]).reshape(len(toks), shape.K, -1)
     rec["ok"] = ok
     if "y" in out:
-        rec["y_rows"] = _host(out["y"].reshape(-1, shape.H)[flat]).reshape(len(toks), shape.K, shape.H)
+        ee, ss = np.where(ok, e, 0).reshape(-1), np.where(ok, sl, 0).reshape(-1)
+        at = [torch.from_numpy(a.astype(np.int64)).to(x_d.device) for a in (ee // shape.EL, ee % shape.EL, ss)]
+        rec["y_rows"] = _host(out["y"][at[0], at[1], at[2]]).reshape(len(toks), shape.K, shape.H)
         rec["out_rows"] = _host(out["combined_x"].reshape(-1, shape.H)[t_idx])
     return rec
 
@@ -910,6 +914,20 @@ def measure_other_ops(ep, dev, peak, checks, reps=10):
     report("combine_heavy.combine", ms, b["combine"], {"rho": round(st["hits"] / (shape.R * shape.T), 3)})
     report("combine_heavy.dispatch_cached", ms_disp, {"payload": b["dispatch"]["payload"],
                                                       "meta": shape.R * shape.T * shape.R * 4})
+    # the one-launch layout + record with the node-level record: 16 ranks are 2 nodes of 8
+    R16, T16 = shape.R, shape.T
+    lay_n = dict(num_tokens_per_rank=torch.empty((R16, R16), dtype=torch.int32, device=dev),
+                 num_tokens_per_rdma_rank=torch.empty((R16, (R16 + 7) // 8), dtype=torch.int32, device=dev),
+                 num_tokens_per_expert=torch.empty((R16, shape.E), dtype=torch.int32, device=dev),
+                 is_token_in_rank=torch.empty((R16, T16, R16), dtype=torch.bool, device=dev),
+                 num_recv_tokens_per_expert=torch.empty((R16, shape.EL), dtype=torch.int32, device=dev))
+    ms_ln = timed(lambda: ep.ep_layout_notify(h, st["idx_d"], **lay_n), reps, stream)
+    h.check()
+    checks.append(capture_layout("combine_heavy.layout_notify_nodes", shape, h, st["idx"], lay_n))
+    res["combine_heavy.layout_notify_nodes"] = {
+        "us": round(ms_ln * 1e3, 2),
+        "note": "one launch of the look-back scan with the node-level record (2 nodes of 8 ranks); latency-bound "
+                "(about 5 MB moved), so no bandwidth fraction"}
     h.destroy()
     del d, ys, out, cw, b0, b1, st, lay
     torch.cuda.empty_cache()
@@ -949,9 +967,46 @@ def measure_other_ops(ep, dev, peak, checks, reps=10):
                                       ("ll_v3.ll_combine", ms_c, b["ll_combine"], cold_c, clean_c)):
         report(name, ms, bb, {"note": warm, "cold_us": round(cold * 1e3, 2), "cold_clean_us": round(clean * 1e3, 2),
                               "cold_clean_frac": round(total(bb) / clean / 1e6 / peak, 4), "cold_note": cold_note})
-    del flush
+    del flush, y
+
+    # the same dispatch with rank 5 masked in the mask buffer: its slots are dropped on both sides
+    masked = 5
+    hm = ep.Handle(ep.Config(shape.R, shape.max_tokens, shape.H, shape.E, shape.K, shape.C, 1, 0), dev)
+    ep.ep_update_mask_buffer(hm, masked, True)
+    ms_m = timed(lambda: ep.ep_ll_dispatch(hm, x_d, idx_d, use_fp8=True, use_ue8m0=True, recv_msgs=msgs,
+                                           packed_recv_count=cnt, packed_recv_layout_range=rng_), reps, stream)
+    hm.check()
+    mask = np.zeros(shape.R, np.int32)
+    mask[masked] = 1
+    checks.append(capture_ll("ll_v3.ll_dispatch_fp8_ue8m0_rank_masked", shape, hm, idx, w, x_d,
+                             dict(recv_msgs=msgs, packed_recv_count=cnt, packed_recv_layout_range=rng_),
+                             rank_mask=mask))
+    src = np.arange(shape.R)[:, None, None]
+    n_valid_m = int(((idx >= 0) & (src != masked) & (idx // shape.EL != masked)).sum())
+    report("ll_v3.ll_dispatch_fp8_ue8m0_rank_masked", ms_m,
+           ll_bytes(shape.R, shape.T, shape.H, shape.K, n_valid_m, msg)["ll_dispatch"],
+           {"note": f"rank {masked} masked: its {n_valid - n_valid_m} slots are dropped on both sides; every token "
+                    "row is still read"})
+    hm.destroy()
+    del msgs
+
+    # bf16 messages, and the combine reading the expert outputs in place in the message buffer (the
+    # payloads as dispatched stand for the experts' outputs: identity experts)
+    msg16 = ep.ep_ll_msg_bytes(shape.H, False)
+    msgs16 = torch.empty((shape.R, shape.EL, shape.R * shape.max_tokens, msg16), dtype=torch.uint8, device=dev)
+    ep.ep_ll_dispatch(h, x_d, idx_d, use_fp8=False, recv_msgs=msgs16, packed_recv_count=cnt,
+                      packed_recv_layout_range=rng_)
+    px, _, _ = ep.ll_views(msgs16, shape.H, False)
+    ms_z = timed(lambda: ep.ep_ll_combine(h, px, idx_d, w_d, combined_x=out), reps, stream)
+    h.check()
+    checks.append(capture_ll("ll_v3.ll_dispatch_bf16+ll_combine_zero_copy", shape, h, idx, w, x_d,
+                             dict(recv_msgs=msgs16, packed_recv_count=cnt, packed_recv_layout_range=rng_, y=px,
+                                  combined_x=out), use_fp8=False, use_ue8m0=False))
+    report("ll_v3.ll_combine_zero_copy", ms_z, b["ll_combine"],
+           {"note": "the expert outputs read in place from the payloads of the bf16 message buffer (row stride "
+                    f"{msg16} B)"})
     h.destroy()
-    del msgs, y, out
+    del msgs16, px, out
     torch.cuda.empty_cache()
 
     # the small case (L2-resident, launch-bound): eager calls and one CUDA graph of the step
@@ -1008,6 +1063,47 @@ def measure_other_ops(ep, dev, peak, checks, reps=10):
 
 
 # ----------------------------------------------------------------------------- CPU oracle
+
+def capture_layout(name, shape, h, idx, lay):
+    """Host copies of one ep_layout_notify call: layout outputs, the record and, with whole nodes of 8
+    ranks, the node-level record -- all whole."""
+    rec = dict(kind="layout", name=name, shape=shape, idx=idx, cap=h.cfg.recv_capacity,
+               layout={k: (_host(v) if v is not None else None) for k, v in lay.items()},
+               record={k: _host(h.export(k)) for k in
+                       ("rank_prefix_matrix", "channel_prefix_matrix", "recv_channel_prefix_matrix", "num_recv",
+                        "send_head", "recv_src_idx")})
+    if shape.R > 8 and shape.R % 8 == 0:
+        rec["nodes"] = {k: _host(h.export(k)) for k in ("rdma_channel_prefix_matrix", "recv_rdma_rank_prefix_sum")}
+    return rec
+
+
+def _check_layout(O, rec):
+    """The oracle on one captured layout + record call, every output whole."""
+    shape, cap = rec["shape"], rec["cap"]
+    bad = []
+    lay = O.get_dispatch_layout(rec["idx"], shape.E, with_rdma=True)
+    n = O.dispatch_notify(lay["num_tokens_per_rank"], lay["is_token_in_rank"], lay["num_tokens_per_expert"],
+                          shape.C, shape.A, cap)
+    for k, v in rec["layout"].items():
+        if k == "num_recv_tokens_per_expert":
+            if v is not None and not np.array_equal(v, n["num_recv_tokens_per_expert"]):
+                bad.append(k)
+        elif v is not None and not np.array_equal(v, lay[k]):
+            bad.append(k)
+    for k, v in rec["record"].items():
+        want = n[k]
+        if k == "recv_src_idx":
+            m = np.arange(cap)[None, :] < np.minimum(n["num_recv"], cap)[:, None]
+            v, want = v[m], want[m]
+        if not np.array_equal(v, want):
+            bad.append(k)
+    if "nodes" in rec:
+        nodes = O.rdma_prefix(lay["is_token_in_rank"], shape.C)
+        for k, v in rec["nodes"].items():
+            if not np.array_equal(v, nodes[k]):
+                bad.append(k)
+    return bad, shape.R * shape.T
+
 
 def _check_normal(O, rec):
     """The oracle on one captured normal-mode call: layout and record whole, rows and tokens sampled."""
@@ -1076,7 +1172,8 @@ def _check_ll(O, rec):
     bad = []
     x = np.zeros((R * T, H), np.uint16)
     x[toks] = rec["x_rows"]
-    o = O.ll_dispatch(x.reshape(R, T, H), rec["idx"], maxT, E, use_fp8=True, use_ue8m0=True)
+    o = O.ll_dispatch(x.reshape(R, T, H), rec["idx"], maxT, E, use_fp8=rec.get("use_fp8", True),
+                      use_ue8m0=rec.get("use_ue8m0", True), rank_mask=rec.get("rank_mask"))
     for k in ("packed_recv_count", "packed_recv_layout_range", "slot_row"):
         if not np.array_equal(rec[k], o[k]):
             bad.append(k)
@@ -1104,7 +1201,7 @@ def cpu_parity(checks):
     t0 = time.perf_counter()
     res, ok = {}, True
     for rec in checks:
-        bad, n = (_check_ll if rec["kind"] == "ll" else _check_normal)(O, rec)
+        bad, n = {"ll": _check_ll, "layout": _check_layout}.get(rec["kind"], _check_normal)(O, rec)
         res[rec["name"]] = {"status": "ok" if not bad else "MISMATCH: " + ", ".join(bad), "tokens_sampled": n}
         ok = ok and not bad
     return {"checked": True, "ok": ok, "calls": res,

@@ -149,3 +149,72 @@ def test_cpu_parity_reports_a_mismatch():
     assert res["ok"] is False
     assert res["calls"]["normal"]["status"] == "ok"
     assert res["calls"]["wrong"]["status"].startswith("MISMATCH") and "recv_x" in res["calls"]["wrong"]["status"]
+
+
+NODES = W.Shape("check_nodes", R=16, T=40, H=256, E=32, K=4, routing="zipf", mask_p=0.05, C=5, A=4, seed=7103)
+
+
+def layout_record():
+    s = NODES
+    idx, _ = W.routing(s)
+    lay = O.get_dispatch_layout(idx, s.E, with_rdma=True)
+    cap = int(lay["num_tokens_per_rank"].sum(axis=0).max())
+    n = O.dispatch_notify(lay["num_tokens_per_rank"], lay["is_token_in_rank"], lay["num_tokens_per_expert"],
+                          s.C, s.A, cap)
+    nodes = O.rdma_prefix(lay["is_token_in_rank"], s.C)
+    layout = {k: lay[k].copy() for k in ("num_tokens_per_rank", "num_tokens_per_rdma_rank", "num_tokens_per_expert",
+                                         "is_token_in_rank")}
+    layout["num_recv_tokens_per_expert"] = n["num_recv_tokens_per_expert"].copy()
+    return dict(kind="layout", name="layout", shape=s, idx=idx, cap=cap, layout=layout,
+                record={k: n[k].copy() for k in ("rank_prefix_matrix", "channel_prefix_matrix",
+                                                 "recv_channel_prefix_matrix", "num_recv", "send_head",
+                                                 "recv_src_idx")},
+                nodes={k: v.copy() for k, v in nodes.items()})
+
+
+def test_correct_layout_call_passes():
+    bad, n = bench._check_layout(O, layout_record())
+    assert bad == [] and n == NODES.R * NODES.T
+
+
+@pytest.mark.parametrize("group,key", [("layout", "num_tokens_per_rdma_rank"), ("layout", "num_recv_tokens_per_expert"),
+                                       ("record", "send_head"), ("nodes", "rdma_channel_prefix_matrix"),
+                                       ("nodes", "recv_rdma_rank_prefix_sum")])
+def test_wrong_layout_output_is_flagged(group, key):
+    rec = layout_record()
+    rec[group][key] = bump(rec[group][key])
+    assert key in bench._check_layout(O, rec)[0]
+
+
+def ll_record_with(mask=None, use_fp8=True):
+    rec = ll_record()
+    s = LL
+    x = W.bf16_bits(W.tokens_x(s))
+    o = O.ll_dispatch(x, rec["idx"], s.max_tokens, s.E, use_fp8=use_fp8, use_ue8m0=use_fp8, rank_mask=mask)
+    toks = rec["toks"]
+    sl = o["slot_row"].reshape(-1, s.K)[toks]
+    e = rec["idx"].reshape(-1, s.K)[toks]
+    rec.update(slot_row=o["slot_row"].copy(), packed_recv_count=o["packed_recv_count"].copy(),
+               packed_recv_layout_range=o["packed_recv_layout_range"].copy(),
+               msg_rows=o["msgs_by_slot"].reshape(s.R * s.T, s.K, -1)[toks].copy(), ok=(e >= 0) & (sl >= 0),
+               use_fp8=use_fp8, use_ue8m0=use_fp8, rank_mask=mask)
+    for k in ("y_rows", "out_rows"):
+        rec.pop(k)
+    return rec
+
+
+def test_masked_ll_call_passes_only_with_its_mask():
+    mask = np.zeros(LL.R, np.int32)
+    mask[1] = 1
+    rec = ll_record_with(mask)
+    assert bench._check_ll(O, rec)[0] == []
+    rec["rank_mask"] = None  # the unmasked oracle disagrees with a masked dispatch
+    assert "slot_row" in bench._check_ll(O, rec)[0]
+
+
+def test_bf16_ll_call_passes_and_its_message_is_checked():
+    rec = ll_record_with(use_fp8=False)
+    assert bench._check_ll(O, rec)[0] == []
+    i, k = np.argwhere(rec["ok"])[0]
+    rec["msg_rows"][i, k, 100] ^= 1
+    assert "messages" in bench._check_ll(O, rec)[0]
